@@ -1,0 +1,183 @@
+/*
+ * svx.h - C ABI of the chunked multi-query verification-attention library.
+ *
+ * One verification round of speculative decoding ("Resource-Efficient
+ * Speculative Decoding for Long-Context LLM Serving", section 4.2 "KV
+ * Streaming for Multi-Query Verification"): the k+1 verification queries of
+ * every request in a Cohort attend to
+ *   - the committed KV history [0, C_b) (Sealed History, section 4.1 Eq. 4),
+ *     pushed chunk by chunk; a chunk in pinned host memory is copied to HBM by
+ *     the library's copy engine, a chunk already in device memory is used in
+ *     place; every chunk serves all queries of the round, and
+ *   - the GPU-resident candidate region (Speculative Frontier) under a causal
+ *     or token-tree mask,
+ * and the partial results are merged by online softmax, Eqs. (7)-(8), so the
+ * output is full attention, Eqs. (6) and (9).
+ *
+ * Conventions
+ *   bf16   IEEE bfloat16 (as torch.bfloat16), element-contiguous.
+ *   B      requests in the round (Cohort), Hq / Hkv query / KV heads,
+ *          G = Hq / Hkv (query head h uses KV head h / G), d head dimension,
+ *          nq verification queries per request (k+1, or token-tree nodes).
+ *   Query j of request b sits at absolute position C_b + j; candidate j is
+ *   the KV of that position.  Query j always sees all history, itself and
+ *   (chain) candidates 0..j-1 or (tree) its ancestors.
+ *
+ * Ownership: the caller owns Q, the history KV (host or device), the
+ * candidate KV, O and LSE; the library owns its staging slots, fp32 state
+ * workspace, events and any stream it creates.  Pinned host history must stay
+ * unmodified until svx_round_finish's work has completed on the compute
+ * stream.  Device buffers given to a round must stay valid until then too.
+ *
+ * Errors: every call returns an svx_status; svx_last_error() gives a
+ * human-readable message for the last failing call on that context.  No call
+ * throws, aborts or exits.  After SVX_ERR_CUDA the context should be
+ * destroyed.
+ *
+ * Threads: a context is used by one host thread at a time.
+ */
+#ifndef SVX_H
+#define SVX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SVX_OK = 0,
+  SVX_ERR_INVALID_ARG = 1, /* bad pointer, size, range, layout or coverage */
+  SVX_ERR_BAD_STATE = 2,   /* call out of begin -> {push|candidates}* -> finish order */
+  SVX_ERR_OOM = 3,         /* device or pinned allocation failed in svx_create */
+  SVX_ERR_CUDA = 4,        /* a CUDA runtime call failed (message has the CUDA error) */
+  SVX_ERR_TIMEOUT = 5,     /* svx_round_finish: work not complete within timeout_ms */
+  SVX_ERR_UNSUPPORTED = 6  /* shape outside what the kernels implement */
+} svx_status;
+
+typedef struct svx_ctx_s* svx_ctx;
+
+/* svx_config.flags */
+#define SVX_FLAG_TIMING 1u /* record CUDA events around copies and kernels (svx_round_stats) */
+
+/* Context configuration.  Shapes are fixed for the context's lifetime (the
+ * Cohort compatibility rule of section 4.2: one layer shape, verification
+ * width bound, dtype, Hkv, d and chunk size per batched kernel). */
+typedef struct {
+  int32_t max_req;          /* >= 1, <= 256: requests per round */
+  int32_t n_q_heads;        /* Hq, a multiple of n_kv_heads */
+  int32_t n_kv_heads;       /* Hkv >= 1 */
+  int32_t head_dim;         /* d: 64 or 128 */
+  int32_t max_query;        /* 1..32: verification queries (= candidates) per request */
+  int32_t max_chunk_tokens; /* >= 1: capacity of one request's part in a staging slot */
+  int32_t n_slots;          /* 2 or 3 staging slots (double / triple buffering) */
+  int32_t device;           /* CUDA device ordinal */
+  void* compute_stream;     /* cudaStream_t for kernels; NULL: library creates one (highest priority) */
+  void* copy_stream;        /* cudaStream_t for H2D chunk copies; NULL: library creates one */
+  uint32_t flags;           /* SVX_FLAG_* */
+} svx_config;
+
+/* One request's contiguous slice of committed history, [tok_start, tok_start + n_tok).
+ * k, v: bf16 [n_tok][Hkv][d], 16-byte aligned.  Pinned host memory (cudaHostAlloc or
+ * cudaHostRegister) is staged through a slot by the copy engine (n_tok <= max_chunk_tokens);
+ * device memory is read in place (any n_tok).  Pageable host memory is rejected. */
+typedef struct {
+  int32_t req;
+  int32_t n_tok;
+  int64_t tok_start;
+  const void* k;
+  const void* v;
+} svx_part;
+
+/* Allocates n_slots staging slots of max_req * max_chunk_tokens * Hkv * d * 2 bf16 each, the
+ * fp32 (m, l, a) workspace and events on cfg->device.  Returns SVX_ERR_OOM, _INVALID_ARG,
+ * _UNSUPPORTED or _CUDA on failure (then *out is NULL). */
+svx_status svx_create(const svx_config* cfg, svx_ctx* out);
+
+/* Waits for the context's outstanding work, then frees everything it owns.  NULL is a no-op. */
+svx_status svx_destroy(svx_ctx ctx);
+
+/* Starts a round (one layer of one Cohort).  q_dev: device bf16 [n_req][Hq][n_query][d].
+ * hist_len_host: host int64[n_req], C_b >= 0.  scale: softmax scale; 0 means 1/sqrt(d)
+ * (Eq. 6).  Running states start at (-inf, 0, 0) (section 4.2, online softmax). */
+svx_status svx_round_begin(svx_ctx ctx, int32_t n_req, int32_t n_query, const void* q_dev,
+                           const int64_t* hist_len_host, float scale);
+
+/* Processes one Cohort chunk: at most one part per request.  Host parts are copied into the next
+ * staging slot on the copy stream (waiting until the compute stream has released that slot);
+ * the chunk kernel then updates every query's (m, l, a) with Eqs. (7)-(8).  Asynchronous: returns
+ * once the work is enqueued.  Parts may arrive in any order across calls (the result does not
+ * depend on chunk order, Eq. 9); svx_round_finish checks that they tile each [0, C_b) exactly once. */
+svx_status svx_push_chunk(svx_ctx ctx, const svx_part* parts, int32_t n_parts);
+
+/* Attention over the GPU-resident candidate region (section 4.2, the causal mask by absolute
+ * position).  k_dev, v_dev: device bf16 [n_req][n_cand][Hkv][d] with n_cand == n_query.
+ * parent_host: NULL for the causal chain (query j sees candidates 0..j), else host
+ * int32[n_req][n_cand] token-tree parents with parent[0] = -1 and 0 <= parent[i] < i
+ * (query j sees j and its ancestors).  At most once per round, in any order with the pushes. */
+svx_status svx_candidate_attn(svx_ctx ctx, const void* k_dev, const void* v_dev, int32_t n_cand,
+                              const int32_t* parent_host);
+
+/* Ends the round: checks chunk coverage, merges the split states (Eq. 8) and writes
+ * O = a / l (Eq. 9) as bf16 [n_req][Hq][n_query][d] and LSE = m + ln l as fp32
+ * [n_req][Hq][n_query] (natural log of the softmax denominator of the scaled scores) to device
+ * memory.  A query with no visible key gets O = 0 and LSE = -inf.  timeout_ms = 0 returns
+ * after enqueueing; > 0 waits on the host up to that long and returns SVX_ERR_TIMEOUT if the
+ * work has not completed (the work stays enqueued).  The context is ready for the next round
+ * either way; its work is stream-ordered after this round's. */
+svx_status svx_round_finish(svx_ctx ctx, void* o_dev, float* lse_dev, int32_t timeout_ms);
+
+/* Message for the last failing call on ctx (never NULL; "" if none).  NULL ctx: last failure of
+ * svx_create on this thread. */
+const char* svx_last_error(svx_ctx ctx);
+
+/* Per-round timing (needs SVX_FLAG_TIMING).  Waits for the last finished round to complete. */
+typedef struct {
+  double round_ms;        /* first event of the round to the end of its finish kernel */
+  double copy_busy_ms;    /* sum over pushes of H2D copy time on the copy stream */
+  double chunk_kernel_ms; /* sum over pushes of chunk-kernel time on the compute stream */
+  double cand_kernel_ms;  /* candidate-region kernel */
+  double finish_kernel_ms;
+  int64_t h2d_bytes;      /* history bytes copied from host this round */
+  int64_t device_bytes;   /* history bytes read in place from device memory this round */
+  int32_t n_chunk_launches;
+  int32_t n_copies;
+} svx_stats;
+svx_status svx_round_stats(svx_ctx ctx, svx_stats* out);
+
+/* ---- host-only bookkeeping (no GPU needed) ----------------------------------------------- */
+
+/* One entry of a cohort chunk plan. */
+typedef struct {
+  int32_t chunk;     /* cohort chunk index j */
+  int32_t slot;      /* staging slot j mod n_slots */
+  int32_t req;
+  int32_t n_tok;     /* min(chunk_tokens, C_b - tok_start) */
+  int64_t tok_start; /* j * chunk_tokens */
+} svx_plan_entry;
+
+/* Cohort chunk plan (section 4.2, "Pipelined KV transfers" and "Cohort batching"): history of
+ * each request cut into contiguous chunks of chunk_tokens; cohort chunk j holds one part per
+ * request with C_b > j * chunk_tokens, in request order.  Writes at most cap entries to out and
+ * the total count to *n_out (call with cap = 0 to size). */
+svx_status svx_plan_chunks(int32_t n_req, const int64_t* hist_len, int32_t chunk_tokens, int32_t n_slots,
+                           svx_plan_entry* out, int64_t cap, int64_t* n_out);
+
+/* Candidate visibility words: out[b * n_query + j] bit i set iff query j of request b may
+ * attend to candidate i.  parent NULL: chain (i <= j); else int32[n_req][n_query] tree
+ * parents (i == j or i an ancestor of j).  n_query <= 32.  SVX_ERR_INVALID_ARG on a bad tree. */
+svx_status svx_candidate_masks(int32_t n_req, int32_t n_query, const int32_t* parent, uint32_t* out);
+
+/* Coverage check used by svx_round_finish: *ok_out = 1 iff the parts (req, tok_start, n_tok)
+ * given as int64[n_parts][3] tile every [0, hist_len[b]) exactly once, else 0. */
+svx_status svx_check_coverage(int32_t n_req, const int64_t* hist_len, const int64_t* parts, int64_t n_parts,
+                              int32_t* ok_out);
+
+/* Library version string. */
+const char* svx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SVX_H */

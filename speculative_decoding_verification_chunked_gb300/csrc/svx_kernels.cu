@@ -1,0 +1,339 @@
+// Kernels of the chunked multi-query verification attention
+// ("Resource-Efficient Speculative Decoding for Long-Context LLM Serving",
+// section 4.2, Eqs. (6)-(9)).
+//
+//   chunk_attn_fma<D, false>  history chunk: every query of the round attends to
+//                             every token of the chunk (the chunk is shared by
+//                             the whole query group, section 4.2), chunk-local
+//                             state (Eq. 7) merged into the running state (Eq. 8).
+//   chunk_attn_fma<D, true>   candidate region: the same update under the
+//                             per-query visibility words (causal chain or
+//                             token tree, section 4.2 last paragraph).
+//   finish_kernel<D>          merges the split states (Eq. 8) and writes
+//                             O = a / l (Eq. 9) in bf16 and LSE in fp32.
+//
+// Scores are kept in log2 units (Q is pre-multiplied by scale * log2 e) so the
+// exponentials are exp2; LSE is converted back to natural log on output.
+#include <math.h>
+
+#include "svx_internal.h"
+
+namespace svx {
+namespace {
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// 2^x with the hardware approximation (ex2.approx, flush-to-zero); 2^-inf = 0.
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+constexpr float kNegInf = -INFINITY;
+
+// ---------------------------------------------------------------------------
+// Chunk attention, FMA form.
+//
+// Grid (splits, Hkv, n_parts * n_rowblk); 128 threads.  A CTA owns one
+// (request, KV head) pair, up to 32 query rows r = (h - g*G)*nq + j of that
+// KV head, and a contiguous range of 32-token tiles of the part.  K/V tiles are
+// staged in shared memory with 16-byte cp.async (double-buffered); every tile
+// serves all rows.  Warp w owns rows w, w+4, ..., lane t owns token t of the
+// tile for the scores and columns [t*D/32, (t+1)*D/32) for the value sum.
+// ---------------------------------------------------------------------------
+template <int D, bool MASKED>
+__global__ void __launch_bounds__(128) chunk_attn_fma(const __grid_constant__ ChunkParams P) {
+  constexpr int TILE = kTile;
+  constexpr int KSTR = D + 8;  // padded K row: conflict-free 16-byte reads by 32 lanes
+  constexpr int VPL = D / 32;  // value columns per lane
+  constexpr int RPW = kRowsPerBlock / 4;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* sQ = reinterpret_cast<float*>(smem_raw);                       // [32][D]
+  __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(sQ + kRowsPerBlock * D);  // [2][TILE][KSTR]
+  __nv_bfloat16* sV = sK + 2 * TILE * KSTR;                              // [2][TILE][D]
+
+  const int split = blockIdx.x;
+  const int g = blockIdx.y;
+  const int p = blockIdx.z / P.n_rowblk;
+  const int rb = blockIdx.z % P.n_rowblk;
+  const PartDesc part = P.parts[p];
+  const int64_t n_tok = part.n_tok;
+  const int64_t n_tiles = (n_tok + TILE - 1) / TILE;
+  const int64_t tile_lo = split_tile_begin(n_tiles, split, P.splits);
+  const int64_t tile_hi = split_tile_begin(n_tiles, split + 1, P.splits);
+  if (tile_lo >= tile_hi) return;  // empty split: its state slot is left untouched
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = P.group * P.n_query;
+  const int r0 = rb * kRowsPerBlock;
+  const int nr = min(kRowsPerBlock, R - r0);
+  const int b = part.req;
+  const int64_t row_base = (static_cast<int64_t>(b) * P.n_q_heads + static_cast<int64_t>(g) * P.group) * P.n_query;
+  const int64_t kv_stride = static_cast<int64_t>(P.n_kv_heads) * D;  // elements between tokens
+
+  auto load_tile = [&](int64_t tile, int buf) {
+    constexpr int CPR = D / 8;  // 16-byte pieces per row
+    const int64_t t0 = tile * TILE;
+    for (int c = threadIdx.x; c < TILE * CPR; c += 128) {
+      const int t = c / CPR, cc = c % CPR;
+      const int64_t tok = t0 + t;
+      const bool ok = tok < n_tok;
+      const int64_t off = ok ? tok * kv_stride + static_cast<int64_t>(g) * D + cc * 8 : 0;
+      cp_async16(sK + (buf * TILE + t) * KSTR + cc * 8, part.k + off, ok ? 16 : 0);
+      cp_async16(sV + (buf * TILE + t) * D + cc * 8, part.v + off, ok ? 16 : 0);
+    }
+    cp_async_commit();
+  };
+
+  load_tile(tile_lo, 0);
+
+  // Q rows of this CTA, pre-scaled into log2 units; rows past nr are zero.
+  for (int i = threadIdx.x; i < kRowsPerBlock * D / 2; i += 128) {
+    const int rr = (2 * i) / D, c = (2 * i) % D;
+    float2 qv = make_float2(0.f, 0.f);
+    if (rr < nr) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(P.q + (row_base + r0 + rr) * D + c);
+      qv = make_float2(bf16_lo(w) * P.q_scale, bf16_hi(w) * P.q_scale);
+    }
+    *reinterpret_cast<float2*>(sQ + rr * D + c) = qv;
+  }
+
+  // rows owned by this warp: rr = warp + 4*i, i < nrw
+  const int nrw = nr > warp ? (nr - warp + 3) / 4 : 0;
+  uint32_t vis_word[RPW];
+  if constexpr (MASKED) {
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+      const int rr = warp + 4 * i;
+      vis_word[i] = (i < nrw) ? P.vis[static_cast<int64_t>(b) * P.n_query + (r0 + rr) % P.n_query] : 0u;
+    }
+  }
+
+  float m[RPW], l[RPW], acc[RPW][VPL];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    m[i] = kNegInf;
+    l[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) acc[i][c] = 0.f;
+  }
+
+  for (int64_t tile = tile_lo; tile < tile_hi; ++tile) {
+    const int buf = static_cast<int>((tile - tile_lo) & 1);
+    if (tile + 1 < tile_hi) {
+      load_tile(tile + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+
+    const __nv_bfloat16* kt = sK + buf * TILE * KSTR;
+    const __nv_bfloat16* vt = sV + buf * TILE * D;
+    const int64_t tok = tile * TILE + lane;
+
+    // scores s[i] = q_i . k_lane (log2 units)
+    float s[RPW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) s[i] = 0.f;
+    const __nv_bfloat16* krow = kt + lane * KSTR;
+#pragma unroll 4
+    for (int d0 = 0; d0 < D; d0 += 8) {
+      const uint4 kw = *reinterpret_cast<const uint4*>(krow + d0);
+      const float k0 = bf16_lo(kw.x), k1 = bf16_hi(kw.x), k2 = bf16_lo(kw.y), k3 = bf16_hi(kw.y);
+      const float k4 = bf16_lo(kw.z), k5 = bf16_hi(kw.z), k6 = bf16_lo(kw.w), k7 = bf16_hi(kw.w);
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) {
+        if (i < nrw) {
+          const float* qr = sQ + (warp + 4 * i) * D + d0;
+          const float4 qa = *reinterpret_cast<const float4*>(qr);
+          const float4 qb = *reinterpret_cast<const float4*>(qr + 4);
+          float t = s[i];
+          t = fmaf(qa.x, k0, t); t = fmaf(qa.y, k1, t); t = fmaf(qa.z, k2, t); t = fmaf(qa.w, k3, t);
+          t = fmaf(qb.x, k4, t); t = fmaf(qb.y, k5, t); t = fmaf(qb.z, k6, t); t = fmaf(qb.w, k7, t);
+          s[i] = t;
+        }
+      }
+    }
+
+    // online softmax update per row (Eqs. 7-8 folded into one step per tile)
+    float pr[RPW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+      pr[i] = 0.f;
+      if (i < nrw) {
+        bool valid = tok < n_tok;
+        if constexpr (MASKED) valid = valid && tok < 32 && ((vis_word[i] >> tok) & 1u);
+        const float si = valid ? s[i] : kNegInf;
+        const float mn = fmaxf(m[i], warp_max(si));
+        if (mn != kNegInf) {
+          const float alpha = exp2_approx(m[i] - mn);  // m = -inf -> 0
+          pr[i] = valid ? exp2_approx(si - mn) : 0.f;
+          l[i] = l[i] * alpha + pr[i];  // per-lane partial denominator
+#pragma unroll
+          for (int c = 0; c < VPL; ++c) acc[i][c] *= alpha;
+          m[i] = mn;
+        }
+      }
+    }
+
+    // value sum: acc[i][c] += sum_t p_i(t) * v_t[lane*VPL + c]
+#pragma unroll 4
+    for (int t = 0; t < TILE; ++t) {
+      float vf[VPL];
+      if constexpr (VPL == 4) {
+        const uint2 vw = *reinterpret_cast<const uint2*>(vt + t * D + lane * 4);
+        vf[0] = bf16_lo(vw.x); vf[1] = bf16_hi(vw.x); vf[2] = bf16_lo(vw.y); vf[3] = bf16_hi(vw.y);
+      } else {
+        const uint32_t vw = *reinterpret_cast<const uint32_t*>(vt + t * D + lane * 2);
+        vf[0] = bf16_lo(vw); vf[1] = bf16_hi(vw);
+      }
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) {
+        if (i < nrw) {
+          const float pt = __shfl_sync(0xffffffffu, pr[i], t);
+#pragma unroll
+          for (int c = 0; c < VPL; ++c) acc[i][c] = fmaf(pt, vf[c], acc[i][c]);
+        }
+      }
+    }
+    __syncthreads();  // the buffer is refilled by the next iteration's prefetch
+  }
+
+  // merge this CTA's state into its slot (Eq. 8), or overwrite a fresh slot
+  const bool fresh = (part.init_mask >> split) & 1u;
+  const int64_t slot_row0 = static_cast<int64_t>(P.slot_base + split) * P.slot_stride + row_base + r0;
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    if (i < nrw) {
+      const int rr = warp + 4 * i;
+      const float lt = warp_sum(l[i]);
+      float mo = m[i], lo = lt;
+      float a[VPL];
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) a[c] = acc[i][c];
+      float2* mlp = P.ws_ml + slot_row0 + rr;
+      float* ap = P.ws_a + (slot_row0 + rr) * D + lane * VPL;
+      if (!fresh) {
+        const float2 old = *mlp;
+        const float mn = fmaxf(old.x, m[i]);
+        if (mn != kNegInf) {
+          const float al = exp2_approx(old.x - mn), be = exp2_approx(m[i] - mn);
+          lo = old.y * al + lt * be;
+#pragma unroll
+          for (int c = 0; c < VPL; ++c) a[c] = ap[c] * al + a[c] * be;
+          mo = mn;
+        } else {
+#pragma unroll
+          for (int c = 0; c < VPL; ++c) a[c] = 0.f;
+          lo = 0.f;
+        }
+      }
+      if (lane == 0) *mlp = make_float2(mo, lo);
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) ap[c] = a[c];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Finish: one warp per query row (b, h, j); merges the state slots that hold
+// data (Eq. 8), then O = a / l (Eq. 9), LSE = (m + log2 l) * ln 2.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ FinishParams P) {
+  constexpr int VPL = D / 32;
+  const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t n_rows = static_cast<int64_t>(P.n_req) * P.n_q_heads * P.n_query;
+  if (row >= n_rows) return;
+  const int b = static_cast<int>(row / (static_cast<int64_t>(P.n_q_heads) * P.n_query));
+  uint32_t mask = P.slot_mask[b];
+  float m = kNegInf, l = 0.f, a[VPL];
+#pragma unroll
+  for (int c = 0; c < VPL; ++c) a[c] = 0.f;
+  while (mask) {
+    const int s = __ffs(mask) - 1;
+    mask &= mask - 1;
+    const int64_t idx = static_cast<int64_t>(s) * P.slot_stride + row;
+    const float2 ml = P.ws_ml[idx];
+    const float mn = fmaxf(m, ml.x);
+    if (mn == kNegInf) continue;
+    const float al = exp2_approx(m - mn), be = exp2_approx(ml.x - mn);
+    const float* ap = P.ws_a + idx * D + lane * VPL;
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) a[c] = a[c] * al + ap[c] * be;
+    l = l * al + ml.y * be;
+    m = mn;
+  }
+  __nv_bfloat16* op = P.o + row * D + lane * VPL;
+  if (l > 0.f) {
+    const float inv = 1.f / l;
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) op[c] = __float2bfloat16_rn(a[c] * inv);
+    if (lane == 0) P.lse[row] = (m + log2f(l)) * 0.69314718055994530942f;
+  } else {
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) op[c] = __float2bfloat16_rn(0.f);
+    if (lane == 0) P.lse[row] = kNegInf;
+  }
+}
+
+template <int D, bool MASKED>
+cudaError_t launch_chunk_fma(const ChunkParams& p, cudaStream_t stream) {
+  constexpr size_t smem = kRowsPerBlock * D * sizeof(float) + 2 * kTile * (D + 8) * 2 + 2 * kTile * D * 2;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(chunk_attn_fma<D, MASKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(p.splits, p.n_kv_heads, p.n_parts * p.n_rowblk);
+  chunk_attn_fma<D, MASKED><<<grid, 128, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_attn(const ChunkParams& p, int head_dim, bool masked, cudaStream_t stream) {
+  if (head_dim == 128) return masked ? launch_chunk_fma<128, true>(p, stream) : launch_chunk_fma<128, false>(p, stream);
+  if (head_dim == 64) return masked ? launch_chunk_fma<64, true>(p, stream) : launch_chunk_fma<64, false>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_finish(const FinishParams& p, int head_dim, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(p.n_req) * p.n_q_heads * p.n_query;
+  const int blocks = static_cast<int>((rows * 32 + 255) / 256);
+  if (blocks == 0) return cudaSuccess;
+  if (head_dim == 128) finish_kernel<128><<<blocks, 256, 0, stream>>>(p);
+  else if (head_dim == 64) finish_kernel<64><<<blocks, 256, 0, stream>>>(p);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace svx

@@ -1,0 +1,691 @@
+// Host runtime of the verification-attention library: the C ABI of svx.h, the
+// round state machine, the cohort chunk planner, the copy engine (pinned host ->
+// HBM staging slots on a copy stream, fenced by events) and kernel launches.
+//
+// Design source: "Resource-Efficient Speculative Decoding for Long-Context LLM
+// Serving", section 4.2: the KV chunk is the unit of transfer and computation,
+// staging buffers are reused once the whole query group has finished with them,
+// transfers and attention run on separate streams, and a Cohort's requests are
+// processed by one batched kernel with independent states.
+#include <algorithm>
+#include <array>
+#include <chrono>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "svx.h"
+#include "svx_internal.h"
+
+using svx::ChunkParams;
+using svx::FinishParams;
+using svx::PartDesc;
+
+namespace {
+
+thread_local std::string g_create_error;
+
+enum class RoundState { kIdle, kOpen };
+
+struct PushEvents {
+  cudaEvent_t copy0, copy1, k0, k1;
+  bool has_copy;
+};
+
+}  // namespace
+
+struct svx_ctx_s {
+  svx_config cfg{};
+  int group = 1;
+  int num_sms = 0;
+  cudaStream_t cs = nullptr, xs = nullptr;
+  bool own_cs = false, own_xs = false;
+
+  // staging slots: n_slots buffers of max_req parts, each part = K then V
+  std::vector<__nv_bfloat16*> slot_buf;
+  int64_t part_elems = 0;  // max_chunk_tokens * Hkv * d
+  std::vector<cudaEvent_t> slot_ready, slot_free;
+  int next_slot = 0;
+
+  // fp32 state workspace: (max_hist_splits + 1) slots; the last one is the candidate region's
+  float2* ws_ml = nullptr;
+  float* ws_a = nullptr;
+  int64_t slot_stride = 0;
+  int max_splits = 1;
+
+  // candidate visibility words: pinned host staging and device copy
+  uint32_t* h_vis = nullptr;
+  uint32_t* d_vis = nullptr;
+  cudaEvent_t vis_copied = nullptr;
+  cudaEvent_t done = nullptr;
+
+  // round
+  RoundState state = RoundState::kIdle;
+  int n_req = 0, n_query = 0;
+  const __nv_bfloat16* q = nullptr;
+  float q_scale = 0.f;
+  std::vector<int64_t> hist_len;
+  std::vector<uint32_t> slot_mask;               // per request, slots holding data
+  std::vector<std::array<int64_t, 3>> parts_seen;  // (req, tok_start, n_tok)
+  bool cand_done = false;
+
+  // timing (SVX_FLAG_TIMING)
+  std::vector<PushEvents> ev_push;
+  int n_push = 0;
+  cudaEvent_t ev_begin = nullptr, ev_c0 = nullptr, ev_c1 = nullptr, ev_f0 = nullptr, ev_f1 = nullptr;
+  bool cand_timed = false;
+  bool stats_valid = false;
+  int64_t h2d_bytes = 0, dev_bytes = 0;
+  int n_launch = 0, n_copies = 0;
+  svx_stats last_stats{};
+  bool last_stats_pending = false;
+
+  std::string err;
+};
+
+namespace {
+
+svx_status fail(svx_ctx ctx, svx_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (ctx) ctx->err = buf;
+  else g_create_error = buf;
+  return st;
+}
+
+#define SVX_CUDA(ctx, call)                                                                            \
+  do {                                                                                                 \
+    cudaError_t e_ = (call);                                                                           \
+    if (e_ != cudaSuccess)                                                                             \
+      return fail((ctx), SVX_ERR_CUDA, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__, \
+                  __LINE__);                                                                           \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Memory kind of a pointer: 0 pageable/unknown, 1 pinned host, 2 device (or managed).
+int pointer_kind(const void* p) {
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (a.type == cudaMemoryTypeHost) return 1;
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return 2;
+  return 0;
+}
+
+svx_status masks_impl(int32_t n_req, int32_t n_query, const int32_t* parent, uint32_t* out, std::string* why) {
+  if (n_req < 0 || n_query < 1 || n_query > 32 || !out) {
+    if (why) *why = "n_req >= 0, 1 <= n_query <= 32 and out != NULL required";
+    return SVX_ERR_INVALID_ARG;
+  }
+  for (int b = 0; b < n_req; ++b) {
+    const int32_t* par = parent ? parent + static_cast<int64_t>(b) * n_query : nullptr;
+    if (par) {
+      if (par[0] != -1) {
+        if (why) *why = "tree parent[0] must be -1 (request " + std::to_string(b) + ")";
+        return SVX_ERR_INVALID_ARG;
+      }
+      for (int i = 1; i < n_query; ++i)
+        if (par[i] < 0 || par[i] >= i) {
+          if (why) *why = "tree parent[i] must lie in [0, i-1] (request " + std::to_string(b) + ")";
+          return SVX_ERR_INVALID_ARG;
+        }
+    }
+    for (int j = 0; j < n_query; ++j) {
+      uint32_t w;
+      if (!par) {
+        w = (j == 31) ? 0xffffffffu : ((1u << (j + 1)) - 1u);
+      } else {
+        w = 1u << j;  // a node's word is its own bit plus its parent's word
+        if (j > 0) w |= out[static_cast<int64_t>(b) * n_query + par[j]];
+      }
+      out[static_cast<int64_t>(b) * n_query + j] = w;
+    }
+  }
+  return SVX_OK;
+}
+
+bool coverage_impl(int32_t n_req, const int64_t* hist_len, const std::vector<std::array<int64_t, 3>>& parts,
+                   std::string* why) {
+  std::vector<std::vector<std::pair<int64_t, int64_t>>> per(static_cast<size_t>(std::max(n_req, 0)));
+  for (const auto& p : parts) {
+    const int64_t b = p[0], t0 = p[1], n = p[2];
+    if (b < 0 || b >= n_req || n <= 0 || t0 < 0 || t0 + n > hist_len[b]) {
+      if (why) *why = "part (req " + std::to_string(b) + ", start " + std::to_string(t0) + ", n " +
+                      std::to_string(n) + ") lies outside the request's history";
+      return false;
+    }
+    per[static_cast<size_t>(b)].push_back({t0, n});
+  }
+  for (int b = 0; b < n_req; ++b) {
+    auto& v = per[static_cast<size_t>(b)];
+    std::sort(v.begin(), v.end());
+    int64_t end = 0;
+    for (const auto& iv : v) {
+      if (iv.first != end) {
+        if (why) *why = "history of request " + std::to_string(b) + (iv.first < end ? " overlaps" : " has a gap") +
+                        " at token " + std::to_string(std::min(iv.first, end));
+        return false;
+      }
+      end = iv.first + iv.second;
+    }
+    if (end != hist_len[b]) {
+      if (why) *why = "history of request " + std::to_string(b) + " covered up to " + std::to_string(end) + " of " +
+                      std::to_string(hist_len[b]) + " tokens";
+      return false;
+    }
+  }
+  return true;
+}
+
+void destroy_all(svx_ctx c) {
+  if (!c) return;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  cudaSetDevice(c->cfg.device);
+  if (c->cs) cudaStreamSynchronize(c->cs);
+  if (c->xs) cudaStreamSynchronize(c->xs);
+  for (auto* p : c->slot_buf) cudaFree(p);
+  for (auto e : c->slot_ready) cudaEventDestroy(e);
+  for (auto e : c->slot_free) cudaEventDestroy(e);
+  for (auto& pe : c->ev_push) {
+    cudaEventDestroy(pe.copy0); cudaEventDestroy(pe.copy1); cudaEventDestroy(pe.k0); cudaEventDestroy(pe.k1);
+  }
+  for (cudaEvent_t e : {c->ev_begin, c->ev_c0, c->ev_c1, c->ev_f0, c->ev_f1, c->vis_copied, c->done})
+    if (e) cudaEventDestroy(e);
+  if (c->ws_ml) cudaFree(c->ws_ml);
+  if (c->ws_a) cudaFree(c->ws_a);
+  if (c->d_vis) cudaFree(c->d_vis);
+  if (c->h_vis) cudaFreeHost(c->h_vis);
+  if (c->own_cs && c->cs) cudaStreamDestroy(c->cs);
+  if (c->own_xs && c->xs) cudaStreamDestroy(c->xs);
+  if (prev >= 0) cudaSetDevice(prev);
+  delete c;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    cudaGetDevice(&prev);
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (prev >= 0 && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+cudaEvent_t make_event(bool timing) {
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreateWithFlags(&e, timing ? cudaEventDefault : cudaEventDisableTiming) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Number of token splits per part for one chunk-kernel launch: enough CTAs for
+// about two per SM, never more tiles than the longest part has.
+int choose_splits(svx_ctx c, int n_parts, int64_t max_tok, int n_rowblk) {
+  const int64_t pairs = static_cast<int64_t>(n_parts) * c->cfg.n_kv_heads * n_rowblk;
+  const int64_t target = 2LL * c->num_sms;
+  int64_t s = (target + pairs - 1) / pairs;
+  const int64_t tiles = (max_tok + svx::kTile - 1) / svx::kTile;
+  s = std::min<int64_t>(s, std::max<int64_t>(tiles, 1));
+  s = std::max<int64_t>(1, std::min<int64_t>(s, c->max_splits));
+  return static_cast<int>(s);
+}
+
+uint32_t nonempty_splits(int64_t n_tok, int splits) {
+  const int64_t n_tiles = (n_tok + svx::kTile - 1) / svx::kTile;
+  uint32_t m = 0;
+  for (int s = 0; s < splits; ++s)
+    if (svx::split_tile_begin(n_tiles, s + 1, splits) > svx::split_tile_begin(n_tiles, s, splits)) m |= 1u << s;
+  return m;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* svx_version(void) { return "svx 0.1.0 (sm_103a)"; }
+
+const char* svx_last_error(svx_ctx ctx) { return ctx ? ctx->err.c_str() : g_create_error.c_str(); }
+
+svx_status svx_create(const svx_config* cfg, svx_ctx* out) {
+  if (!out) return fail(nullptr, SVX_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!cfg) return fail(nullptr, SVX_ERR_INVALID_ARG, "cfg is NULL");
+  const svx_config& k = *cfg;
+  if (k.max_req < 1 || k.max_req > svx::kMaxReq)
+    return fail(nullptr, SVX_ERR_INVALID_ARG, "max_req must be in [1, %d]", svx::kMaxReq);
+  if (k.n_kv_heads < 1 || k.n_q_heads < k.n_kv_heads || k.n_q_heads % k.n_kv_heads)
+    return fail(nullptr, SVX_ERR_INVALID_ARG, "n_q_heads must be a positive multiple of n_kv_heads");
+  if (k.head_dim != 64 && k.head_dim != 128)
+    return fail(nullptr, SVX_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", k.head_dim);
+  if (k.max_query < 1 || k.max_query > 32)
+    return fail(nullptr, SVX_ERR_INVALID_ARG, "max_query must be in [1, 32]");
+  if (k.max_chunk_tokens < 1) return fail(nullptr, SVX_ERR_INVALID_ARG, "max_chunk_tokens must be >= 1");
+  if (k.n_slots < 2 || k.n_slots > 3) return fail(nullptr, SVX_ERR_INVALID_ARG, "n_slots must be 2 or 3");
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+    cudaGetLastError();
+    return fail(nullptr, SVX_ERR_CUDA, "no CUDA device available");
+  }
+  if (k.device < 0 || k.device >= ndev) return fail(nullptr, SVX_ERR_INVALID_ARG, "device %d out of range", k.device);
+  DeviceGuard dg(k.device);
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, k.device) != cudaSuccess)
+    return fail(nullptr, SVX_ERR_CUDA, "cudaGetDeviceProperties failed");
+  if (prop.major < 10) return fail(nullptr, SVX_ERR_UNSUPPORTED, "needs a Blackwell GPU (sm_103a build)");
+
+  svx_ctx c = new (std::nothrow) svx_ctx_s();
+  if (!c) return fail(nullptr, SVX_ERR_OOM, "host allocation failed");
+  c->cfg = k;
+  c->group = k.n_q_heads / k.n_kv_heads;
+  c->num_sms = prop.multiProcessorCount;
+  auto bail = [&](svx_status st, const char* msg) {
+    std::string m = msg;
+    destroy_all(c);
+    return fail(nullptr, st, "%s", m.c_str());
+  };
+  int lo = 0, hi = 0;
+  cudaDeviceGetStreamPriorityRange(&lo, &hi);
+  if (k.compute_stream) c->cs = static_cast<cudaStream_t>(k.compute_stream);
+  else if (cudaStreamCreateWithPriority(&c->cs, cudaStreamNonBlocking, hi) == cudaSuccess) c->own_cs = true;
+  else return bail(SVX_ERR_CUDA, "compute stream creation failed");
+  if (k.copy_stream) c->xs = static_cast<cudaStream_t>(k.copy_stream);
+  else if (cudaStreamCreateWithPriority(&c->xs, cudaStreamNonBlocking, hi) == cudaSuccess) c->own_xs = true;
+  else return bail(SVX_ERR_CUDA, "copy stream creation failed");
+
+  c->part_elems = static_cast<int64_t>(k.max_chunk_tokens) * k.n_kv_heads * k.head_dim;
+  for (int s = 0; s < k.n_slots; ++s) {
+    void* p = nullptr;
+    if (cudaMalloc(&p, static_cast<size_t>(c->part_elems) * 2 * 2 * k.max_req) != cudaSuccess) {
+      cudaGetLastError();
+      return bail(SVX_ERR_OOM, "staging slot allocation failed");
+    }
+    c->slot_buf.push_back(static_cast<__nv_bfloat16*>(p));
+    cudaEvent_t a = make_event(false), b = make_event(false);
+    if (!a || !b) return bail(SVX_ERR_CUDA, "event creation failed");
+    c->slot_ready.push_back(a);
+    c->slot_free.push_back(b);
+  }
+  // history splits: about two CTAs per SM over the (request, KV head) pairs of a full Cohort
+  const int64_t pairs = static_cast<int64_t>(k.max_req) * k.n_kv_heads;
+  c->max_splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(svx::kMaxHistSplits,
+                                                                          (2LL * c->num_sms + pairs - 1) / pairs)));
+  c->slot_stride = static_cast<int64_t>(k.max_req) * k.n_q_heads * k.max_query;
+  const int64_t n_state = static_cast<int64_t>(c->max_splits + 1) * c->slot_stride;
+  if (cudaMalloc(reinterpret_cast<void**>(&c->ws_ml), static_cast<size_t>(n_state) * sizeof(float2)) != cudaSuccess ||
+      cudaMalloc(reinterpret_cast<void**>(&c->ws_a), static_cast<size_t>(n_state) * k.head_dim * sizeof(float)) !=
+          cudaSuccess ||
+      cudaMalloc(reinterpret_cast<void**>(&c->d_vis), static_cast<size_t>(k.max_req) * 32 * sizeof(uint32_t)) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return bail(SVX_ERR_OOM, "workspace allocation failed");
+  }
+  if (cudaHostAlloc(reinterpret_cast<void**>(&c->h_vis), static_cast<size_t>(k.max_req) * 32 * sizeof(uint32_t),
+                    cudaHostAllocDefault) != cudaSuccess) {
+    cudaGetLastError();
+    return bail(SVX_ERR_OOM, "pinned mask buffer allocation failed");
+  }
+  c->vis_copied = make_event(false);
+  c->done = make_event(false);
+  if (!c->vis_copied || !c->done) return bail(SVX_ERR_CUDA, "event creation failed");
+  if (k.flags & SVX_FLAG_TIMING) {
+    c->ev_begin = make_event(true); c->ev_c0 = make_event(true); c->ev_c1 = make_event(true);
+    c->ev_f0 = make_event(true); c->ev_f1 = make_event(true);
+    if (!c->ev_begin || !c->ev_c0 || !c->ev_c1 || !c->ev_f0 || !c->ev_f1)
+      return bail(SVX_ERR_CUDA, "event creation failed");
+  }
+  *out = c;
+  return SVX_OK;
+}
+
+svx_status svx_destroy(svx_ctx ctx) {
+  destroy_all(ctx);
+  return SVX_OK;
+}
+
+svx_status svx_round_begin(svx_ctx c, int32_t n_req, int32_t n_query, const void* q_dev, const int64_t* hist_len,
+                           float scale) {
+  if (!c) return SVX_ERR_INVALID_ARG;
+  if (c->state != RoundState::kIdle) return fail(c, SVX_ERR_BAD_STATE, "svx_round_begin: a round is already open");
+  if (n_req < 1 || n_req > c->cfg.max_req)
+    return fail(c, SVX_ERR_INVALID_ARG, "n_req must be in [1, %d]", c->cfg.max_req);
+  if (n_query < 1 || n_query > c->cfg.max_query)
+    return fail(c, SVX_ERR_INVALID_ARG, "n_query must be in [1, %d]", c->cfg.max_query);
+  if (!q_dev || !aligned16(q_dev)) return fail(c, SVX_ERR_INVALID_ARG, "q_dev must be a 16-byte aligned pointer");
+  if (!hist_len) return fail(c, SVX_ERR_INVALID_ARG, "hist_len is NULL");
+  if (!(scale >= 0.f) || std::isinf(scale)) return fail(c, SVX_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  DeviceGuard dg(c->cfg.device);
+  if (pointer_kind(q_dev) != 2) return fail(c, SVX_ERR_INVALID_ARG, "q_dev is not device memory");
+  for (int b = 0; b < n_req; ++b)
+    if (hist_len[b] < 0) return fail(c, SVX_ERR_INVALID_ARG, "hist_len[%d] < 0", b);
+  c->n_req = n_req;
+  c->n_query = n_query;
+  c->q = static_cast<const __nv_bfloat16*>(q_dev);
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(c->cfg.head_dim));
+  c->q_scale = sc * 1.4426950408889634f;
+  c->hist_len.assign(hist_len, hist_len + n_req);
+  c->slot_mask.assign(static_cast<size_t>(n_req), 0u);
+  c->parts_seen.clear();
+  c->cand_done = false;
+  c->n_push = 0;
+  c->cand_timed = false;
+  c->last_stats_pending = false;
+  c->h2d_bytes = c->dev_bytes = 0;
+  c->n_launch = c->n_copies = 0;
+  if (c->cfg.flags & SVX_FLAG_TIMING) SVX_CUDA(c, cudaEventRecord(c->ev_begin, c->cs));
+  c->state = RoundState::kOpen;
+  return SVX_OK;
+}
+
+namespace {
+
+// Launches the chunk kernel over `parts` (already resolved to device pointers),
+// in batches of at most kMaxPartsPerLaunch parts.
+svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, bool masked, int slot_base, int splits_override) {
+  const int R = c->group * c->n_query;
+  const int n_rowblk = (R + svx::kRowsPerBlock - 1) / svx::kRowsPerBlock;
+  for (size_t i0 = 0; i0 < parts.size(); i0 += svx::kMaxPartsPerLaunch) {
+    const int n = static_cast<int>(std::min<size_t>(svx::kMaxPartsPerLaunch, parts.size() - i0));
+    ChunkParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = c->q;
+    p.ws_ml = c->ws_ml;
+    p.ws_a = c->ws_a;
+    p.vis = masked ? c->d_vis : nullptr;
+    p.slot_stride = c->slot_stride;
+    p.q_scale = c->q_scale;
+    p.n_q_heads = c->cfg.n_q_heads;
+    p.n_kv_heads = c->cfg.n_kv_heads;
+    p.group = c->group;
+    p.n_query = c->n_query;
+    p.slot_base = slot_base;
+    p.n_parts = n;
+    p.n_rowblk = n_rowblk;
+    int64_t max_tok = 0;
+    for (int i = 0; i < n; ++i) max_tok = std::max<int64_t>(max_tok, parts[i0 + i].n_tok);
+    p.splits = splits_override > 0 ? splits_override : choose_splits(c, n, max_tok, n_rowblk);
+    for (int i = 0; i < n; ++i) {
+      PartDesc d = parts[i0 + i];
+      const uint32_t ne = nonempty_splits(d.n_tok, p.splits) << slot_base;
+      uint32_t& used = c->slot_mask[static_cast<size_t>(d.req)];
+      d.init_mask = (ne & ~used) >> slot_base;
+      used |= ne;
+      p.parts[i] = d;
+    }
+    SVX_CUDA(c, svx::launch_chunk_attn(p, c->cfg.head_dim, masked, c->cs));
+    ++c->n_launch;
+  }
+  return SVX_OK;
+}
+
+}  // namespace
+
+svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
+  if (!c) return SVX_ERR_INVALID_ARG;
+  if (c->state != RoundState::kOpen) return fail(c, SVX_ERR_BAD_STATE, "svx_push_chunk: no open round");
+  if (n_parts < 0 || (n_parts > 0 && !parts)) return fail(c, SVX_ERR_INVALID_ARG, "bad parts array");
+  if (n_parts == 0) return SVX_OK;
+  if (n_parts > c->n_req) return fail(c, SVX_ERR_INVALID_ARG, "more parts than requests in the round");
+  DeviceGuard dg(c->cfg.device);
+  const int64_t row_elems = static_cast<int64_t>(c->cfg.n_kv_heads) * c->cfg.head_dim;
+  std::vector<char> seen(static_cast<size_t>(c->n_req), 0);
+  std::vector<int> kind(static_cast<size_t>(n_parts));
+  int n_host = 0;
+  for (int i = 0; i < n_parts; ++i) {
+    const svx_part& p = parts[i];
+    if (p.req < 0 || p.req >= c->n_req) return fail(c, SVX_ERR_INVALID_ARG, "part %d: req %d out of range", i, p.req);
+    if (seen[static_cast<size_t>(p.req)])
+      return fail(c, SVX_ERR_INVALID_ARG, "part %d: request %d appears twice in one chunk", i, p.req);
+    seen[static_cast<size_t>(p.req)] = 1;
+    if (p.n_tok < 1 || p.tok_start < 0 || p.tok_start + p.n_tok > c->hist_len[static_cast<size_t>(p.req)])
+      return fail(c, SVX_ERR_INVALID_ARG, "part %d: tokens [%lld, %lld) outside history [0, %lld) of request %d", i,
+                  static_cast<long long>(p.tok_start), static_cast<long long>(p.tok_start + p.n_tok),
+                  static_cast<long long>(c->hist_len[static_cast<size_t>(p.req)]), p.req);
+    if (!p.k || !p.v || !aligned16(p.k) || !aligned16(p.v))
+      return fail(c, SVX_ERR_INVALID_ARG, "part %d: k and v must be non-NULL and 16-byte aligned", i);
+    const int kk = pointer_kind(p.k), kv = pointer_kind(p.v);
+    if (kk == 0 || kv == 0 || kk != kv)
+      return fail(c, SVX_ERR_INVALID_ARG,
+                  "part %d: k and v must both be pinned host memory or both device memory (pageable host memory "
+                  "cannot be streamed)", i);
+    kind[static_cast<size_t>(i)] = kk;
+    if (kk == 1) {
+      if (p.n_tok > c->cfg.max_chunk_tokens)
+        return fail(c, SVX_ERR_INVALID_ARG, "part %d: %d tokens exceed max_chunk_tokens %d", i, p.n_tok,
+                    c->cfg.max_chunk_tokens);
+      ++n_host;
+    }
+  }
+  const bool timing = (c->cfg.flags & SVX_FLAG_TIMING) != 0;
+  if (timing && c->n_push >= static_cast<int>(c->ev_push.size())) {
+    PushEvents pe{make_event(true), make_event(true), make_event(true), make_event(true), false};
+    if (!pe.copy0 || !pe.copy1 || !pe.k0 || !pe.k1) return fail(c, SVX_ERR_CUDA, "event creation failed");
+    c->ev_push.push_back(pe);
+  }
+  PushEvents* pe = timing ? &c->ev_push[static_cast<size_t>(c->n_push)] : nullptr;
+
+  std::vector<PartDesc> desc(static_cast<size_t>(n_parts));
+  int slot = -1;
+  if (n_host > 0) {
+    // copy engine: wait until the compute stream released the slot, then stage the host parts
+    slot = c->next_slot;
+    c->next_slot = (c->next_slot + 1) % c->cfg.n_slots;
+    SVX_CUDA(c, cudaStreamWaitEvent(c->xs, c->slot_free[static_cast<size_t>(slot)], 0));
+    if (pe) SVX_CUDA(c, cudaEventRecord(pe->copy0, c->xs));
+    int hi = 0;
+    for (int i = 0; i < n_parts; ++i) {
+      if (kind[static_cast<size_t>(i)] != 1) continue;
+      const svx_part& p = parts[i];
+      __nv_bfloat16* dk = c->slot_buf[static_cast<size_t>(slot)] + static_cast<int64_t>(hi) * 2 * c->part_elems;
+      __nv_bfloat16* dv = dk + c->part_elems;
+      const size_t bytes = static_cast<size_t>(p.n_tok) * row_elems * 2;
+      SVX_CUDA(c, cudaMemcpyAsync(dk, p.k, bytes, cudaMemcpyHostToDevice, c->xs));
+      SVX_CUDA(c, cudaMemcpyAsync(dv, p.v, bytes, cudaMemcpyHostToDevice, c->xs));
+      desc[static_cast<size_t>(i)] = PartDesc{dk, dv, p.req, p.n_tok, 0u, 0};
+      c->h2d_bytes += 2 * static_cast<int64_t>(bytes);
+      c->n_copies += 2;
+      ++hi;
+    }
+    if (pe) SVX_CUDA(c, cudaEventRecord(pe->copy1, c->xs));
+    SVX_CUDA(c, cudaEventRecord(c->slot_ready[static_cast<size_t>(slot)], c->xs));
+    SVX_CUDA(c, cudaStreamWaitEvent(c->cs, c->slot_ready[static_cast<size_t>(slot)], 0));
+  }
+  for (int i = 0; i < n_parts; ++i) {
+    const svx_part& p = parts[i];
+    if (kind[static_cast<size_t>(i)] == 2) {
+      desc[static_cast<size_t>(i)] = PartDesc{static_cast<const __nv_bfloat16*>(p.k),
+                                              static_cast<const __nv_bfloat16*>(p.v), p.req, p.n_tok, 0u, 0};
+      c->dev_bytes += 2 * static_cast<int64_t>(p.n_tok) * row_elems * 2;
+    }
+    c->parts_seen.push_back({p.req, p.tok_start, p.n_tok});
+  }
+  if (pe) {
+    pe->has_copy = n_host > 0;
+    SVX_CUDA(c, cudaEventRecord(pe->k0, c->cs));
+  }
+  svx_status st = launch_parts(c, desc, false, 0, 0);
+  if (st != SVX_OK) return st;
+  if (pe) {
+    SVX_CUDA(c, cudaEventRecord(pe->k1, c->cs));
+    ++c->n_push;
+  }
+  if (slot >= 0) SVX_CUDA(c, cudaEventRecord(c->slot_free[static_cast<size_t>(slot)], c->cs));
+  return SVX_OK;
+}
+
+svx_status svx_candidate_attn(svx_ctx c, const void* k_dev, const void* v_dev, int32_t n_cand,
+                              const int32_t* parent_host) {
+  if (!c) return SVX_ERR_INVALID_ARG;
+  if (c->state != RoundState::kOpen) return fail(c, SVX_ERR_BAD_STATE, "svx_candidate_attn: no open round");
+  if (c->cand_done) return fail(c, SVX_ERR_BAD_STATE, "svx_candidate_attn: already called in this round");
+  if (n_cand != c->n_query)
+    return fail(c, SVX_ERR_INVALID_ARG, "n_cand (%d) must equal n_query (%d)", n_cand, c->n_query);
+  if (!k_dev || !v_dev || !aligned16(k_dev) || !aligned16(v_dev))
+    return fail(c, SVX_ERR_INVALID_ARG, "candidate k/v must be non-NULL and 16-byte aligned");
+  DeviceGuard dg(c->cfg.device);
+  if (pointer_kind(k_dev) != 2 || pointer_kind(v_dev) != 2)
+    return fail(c, SVX_ERR_INVALID_ARG, "candidate k/v must be device memory (the candidate region is GPU-resident)");
+  // the previous round's mask upload must have left the pinned staging buffer
+  SVX_CUDA(c, cudaEventSynchronize(c->vis_copied));
+  std::string why;
+  if (masks_impl(c->n_req, c->n_query, parent_host, c->h_vis, &why) != SVX_OK)
+    return fail(c, SVX_ERR_INVALID_ARG, "%s", why.c_str());
+  SVX_CUDA(c, cudaMemcpyAsync(c->d_vis, c->h_vis, static_cast<size_t>(c->n_req) * c->n_query * sizeof(uint32_t),
+                              cudaMemcpyHostToDevice, c->cs));
+  SVX_CUDA(c, cudaEventRecord(c->vis_copied, c->cs));
+  const int64_t per_req = static_cast<int64_t>(n_cand) * c->cfg.n_kv_heads * c->cfg.head_dim;
+  std::vector<PartDesc> desc(static_cast<size_t>(c->n_req));
+  for (int b = 0; b < c->n_req; ++b)
+    desc[static_cast<size_t>(b)] = PartDesc{static_cast<const __nv_bfloat16*>(k_dev) + b * per_req,
+                                            static_cast<const __nv_bfloat16*>(v_dev) + b * per_req, b, n_cand, 0u, 0};
+  const bool timing = (c->cfg.flags & SVX_FLAG_TIMING) != 0;
+  if (timing) SVX_CUDA(c, cudaEventRecord(c->ev_c0, c->cs));
+  svx_status st = launch_parts(c, desc, true, c->max_splits, 1);
+  if (st != SVX_OK) return st;
+  if (timing) {
+    SVX_CUDA(c, cudaEventRecord(c->ev_c1, c->cs));
+    c->cand_timed = true;
+  }
+  c->cand_done = true;
+  return SVX_OK;
+}
+
+svx_status svx_round_finish(svx_ctx c, void* o_dev, float* lse_dev, int32_t timeout_ms) {
+  if (!c) return SVX_ERR_INVALID_ARG;
+  if (c->state != RoundState::kOpen) return fail(c, SVX_ERR_BAD_STATE, "svx_round_finish: no open round");
+  if (!o_dev || !lse_dev || !aligned16(o_dev) || !aligned16(lse_dev))
+    return fail(c, SVX_ERR_INVALID_ARG, "o_dev and lse_dev must be non-NULL and 16-byte aligned");
+  if (timeout_ms < 0) return fail(c, SVX_ERR_INVALID_ARG, "timeout_ms must be >= 0");
+  DeviceGuard dg(c->cfg.device);
+  if (pointer_kind(o_dev) != 2 || pointer_kind(lse_dev) != 2)
+    return fail(c, SVX_ERR_INVALID_ARG, "o_dev and lse_dev must be device memory");
+  std::string why;
+  if (!coverage_impl(c->n_req, c->hist_len.data(), c->parts_seen, &why)) {
+    c->state = RoundState::kIdle;  // the round is abandoned; its enqueued work is harmless
+    return fail(c, SVX_ERR_INVALID_ARG, "chunk coverage check failed: %s", why.c_str());
+  }
+  FinishParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.ws_ml = c->ws_ml;
+  p.ws_a = c->ws_a;
+  p.slot_stride = c->slot_stride;
+  p.o = static_cast<__nv_bfloat16*>(o_dev);
+  p.lse = lse_dev;
+  p.n_req = c->n_req;
+  p.n_q_heads = c->cfg.n_q_heads;
+  p.n_query = c->n_query;
+  for (int b = 0; b < c->n_req; ++b) p.slot_mask[b] = c->slot_mask[static_cast<size_t>(b)];
+  const bool timing = (c->cfg.flags & SVX_FLAG_TIMING) != 0;
+  c->state = RoundState::kIdle;
+  if (timing) SVX_CUDA(c, cudaEventRecord(c->ev_f0, c->cs));
+  SVX_CUDA(c, svx::launch_finish(p, c->cfg.head_dim, c->cs));
+  if (timing) SVX_CUDA(c, cudaEventRecord(c->ev_f1, c->cs));
+  SVX_CUDA(c, cudaEventRecord(c->done, c->cs));
+  if (timing) {
+    c->last_stats_pending = true;
+    c->last_stats = svx_stats{};
+    c->last_stats.h2d_bytes = c->h2d_bytes;
+    c->last_stats.device_bytes = c->dev_bytes;
+    c->last_stats.n_chunk_launches = c->n_launch;
+    c->last_stats.n_copies = c->n_copies;
+  }
+  if (timeout_ms > 0) {
+    const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms);
+    for (;;) {
+      cudaError_t e = cudaEventQuery(c->done);
+      if (e == cudaSuccess) break;
+      if (e != cudaErrorNotReady) return fail(c, SVX_ERR_CUDA, "round failed: %s", cudaGetErrorString(e));
+      if (std::chrono::steady_clock::now() >= deadline)
+        return fail(c, SVX_ERR_TIMEOUT, "round not complete after %d ms", timeout_ms);
+      std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+  }
+  return SVX_OK;
+}
+
+svx_status svx_round_stats(svx_ctx c, svx_stats* out) {
+  if (!c || !out) return SVX_ERR_INVALID_ARG;
+  if (!(c->cfg.flags & SVX_FLAG_TIMING)) return fail(c, SVX_ERR_BAD_STATE, "context created without SVX_FLAG_TIMING");
+  if (!c->last_stats_pending) return fail(c, SVX_ERR_BAD_STATE, "no finished round to report");
+  DeviceGuard dg(c->cfg.device);
+  SVX_CUDA(c, cudaEventSynchronize(c->done));
+  svx_stats s = c->last_stats;
+  float ms = 0.f;
+  SVX_CUDA(c, cudaEventElapsedTime(&ms, c->ev_begin, c->ev_f1));
+  s.round_ms = ms;
+  for (int i = 0; i < c->n_push; ++i) {
+    const PushEvents& pe = c->ev_push[static_cast<size_t>(i)];
+    if (pe.has_copy) {
+      SVX_CUDA(c, cudaEventElapsedTime(&ms, pe.copy0, pe.copy1));
+      s.copy_busy_ms += ms;
+    }
+    SVX_CUDA(c, cudaEventElapsedTime(&ms, pe.k0, pe.k1));
+    s.chunk_kernel_ms += ms;
+  }
+  if (c->cand_timed) {
+    SVX_CUDA(c, cudaEventElapsedTime(&ms, c->ev_c0, c->ev_c1));
+    s.cand_kernel_ms = ms;
+  }
+  SVX_CUDA(c, cudaEventElapsedTime(&ms, c->ev_f0, c->ev_f1));
+  s.finish_kernel_ms = ms;
+  *out = s;
+  return SVX_OK;
+}
+
+svx_status svx_plan_chunks(int32_t n_req, const int64_t* hist_len, int32_t chunk_tokens, int32_t n_slots,
+                           svx_plan_entry* out, int64_t cap, int64_t* n_out) {
+  if (n_req < 0 || (n_req > 0 && !hist_len) || chunk_tokens < 1 || n_slots < 1 || cap < 0 || !n_out ||
+      (cap > 0 && !out))
+    return SVX_ERR_INVALID_ARG;
+  int64_t max_len = 0;
+  for (int b = 0; b < n_req; ++b) {
+    if (hist_len[b] < 0) return SVX_ERR_INVALID_ARG;
+    max_len = std::max(max_len, hist_len[b]);
+  }
+  int64_t n = 0;
+  const int64_t n_chunks = (max_len + chunk_tokens - 1) / chunk_tokens;
+  for (int64_t j = 0; j < n_chunks; ++j) {
+    const int64_t t0 = j * chunk_tokens;
+    for (int b = 0; b < n_req; ++b) {
+      if (hist_len[b] <= t0) continue;
+      if (n < cap)
+        out[n] = svx_plan_entry{static_cast<int32_t>(j), static_cast<int32_t>(j % n_slots), b,
+                                static_cast<int32_t>(std::min<int64_t>(chunk_tokens, hist_len[b] - t0)), t0};
+      ++n;
+    }
+  }
+  *n_out = n;
+  return SVX_OK;
+}
+
+svx_status svx_candidate_masks(int32_t n_req, int32_t n_query, const int32_t* parent, uint32_t* out) {
+  return masks_impl(n_req, n_query, parent, out, nullptr);
+}
+
+svx_status svx_check_coverage(int32_t n_req, const int64_t* hist_len, const int64_t* parts, int64_t n_parts,
+                              int32_t* ok_out) {
+  if (n_req < 0 || (n_req > 0 && !hist_len) || n_parts < 0 || (n_parts > 0 && !parts) || !ok_out)
+    return SVX_ERR_INVALID_ARG;
+  for (int b = 0; b < n_req; ++b)
+    if (hist_len[b] < 0) return SVX_ERR_INVALID_ARG;
+  std::vector<std::array<int64_t, 3>> v(static_cast<size_t>(n_parts));
+  for (int64_t i = 0; i < n_parts; ++i) v[static_cast<size_t>(i)] = {parts[3 * i], parts[3 * i + 1], parts[3 * i + 2]};
+  *ok_out = coverage_impl(n_req, hist_len, v, nullptr) ? 1 : 0;
+  return SVX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,260 @@
+"""Python binding of the svx C ABI (``include/svx.h``): argument marshalling only.
+
+Every step of the verification round runs in the CUDA library; this module
+turns torch tensors and Python sequences into the pointers and sizes the C
+calls take.  Importing it loads ``libsvx.so`` and fails loudly if the library
+has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsvx.so")
+
+OK, ERR_INVALID_ARG, ERR_BAD_STATE, ERR_OOM, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = range(7)
+STATUS_NAMES = {0: "SVX_OK", 1: "SVX_ERR_INVALID_ARG", 2: "SVX_ERR_BAD_STATE", 3: "SVX_ERR_OOM",
+                4: "SVX_ERR_CUDA", 5: "SVX_ERR_TIMEOUT", 6: "SVX_ERR_UNSUPPORTED"}
+FLAG_TIMING = 1
+
+
+class SvxError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("max_req", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("max_query", ctypes.c_int32), ("max_chunk_tokens", ctypes.c_int32),
+                ("n_slots", ctypes.c_int32), ("device", ctypes.c_int32), ("compute_stream", ctypes.c_void_p),
+                ("copy_stream", ctypes.c_void_p), ("flags", ctypes.c_uint32)]
+
+
+class Part(ctypes.Structure):
+    _fields_ = [("req", ctypes.c_int32), ("n_tok", ctypes.c_int32), ("tok_start", ctypes.c_int64),
+                ("k", ctypes.c_void_p), ("v", ctypes.c_void_p)]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [("round_ms", ctypes.c_double), ("copy_busy_ms", ctypes.c_double),
+                ("chunk_kernel_ms", ctypes.c_double), ("cand_kernel_ms", ctypes.c_double),
+                ("finish_kernel_ms", ctypes.c_double), ("h2d_bytes", ctypes.c_int64),
+                ("device_bytes", ctypes.c_int64), ("n_chunk_launches", ctypes.c_int32),
+                ("n_copies", ctypes.c_int32)]
+
+
+class PlanEntry(ctypes.Structure):
+    _fields_ = [("chunk", ctypes.c_int32), ("slot", ctypes.c_int32), ("req", ctypes.c_int32),
+                ("n_tok", ctypes.c_int32), ("tok_start", ctypes.c_int64)]
+
+
+# name -> (restype, argtypes); every symbol declared in include/svx.h
+_P = ctypes.c_void_p
+_SIGS = {
+    "svx_create": (ctypes.c_int, [ctypes.POINTER(Config), ctypes.POINTER(_P)]),
+    "svx_destroy": (ctypes.c_int, [_P]),
+    "svx_round_begin": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, _P, ctypes.POINTER(ctypes.c_int64),
+                                       ctypes.c_float]),
+    "svx_push_chunk": (ctypes.c_int, [_P, ctypes.POINTER(Part), ctypes.c_int32]),
+    "svx_candidate_attn": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
+    "svx_round_finish": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32]),
+    "svx_last_error": (ctypes.c_char_p, [_P]),
+    "svx_round_stats": (ctypes.c_int, [_P, ctypes.POINTER(Stats)]),
+    "svx_plan_chunks": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.POINTER(PlanEntry), ctypes.c_int64,
+                                       ctypes.POINTER(ctypes.c_int64)]),
+    "svx_candidate_masks": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
+                                           ctypes.POINTER(ctypes.c_uint32)]),
+    "svx_check_coverage": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_int64),
+                                          ctypes.POINTER(ctypes.c_int64), ctypes.c_int64,
+                                          ctypes.POINTER(ctypes.c_int32)]),
+    "svx_version": (ctypes.c_char_p, []),
+}
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"CUDA library not built: {_LIB_PATH} is missing (run __graft_entry__.build())")
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+SYMBOLS = tuple(_SIGS)
+
+
+def version() -> str:
+    return lib.svx_version().decode()
+
+
+def _i64(seq) -> ctypes.Array:
+    a = np.ascontiguousarray(np.asarray(seq, dtype=np.int64))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+
+
+# ------------------------------------------------------------ host-only bookkeeping
+
+
+def plan_chunks(hist_len: Sequence[int], chunk_tokens: int, n_slots: int) -> list:
+    """Cohort chunk plan as (chunk, slot, req, tok_start, n_tok) tuples."""
+    h, hp = _i64(hist_len)
+    n = ctypes.c_int64(0)
+    st = lib.svx_plan_chunks(len(h), hp, chunk_tokens, n_slots, None, 0, ctypes.byref(n))
+    if st != OK:
+        raise SvxError(st, "svx_plan_chunks: invalid arguments")
+    buf = (PlanEntry * max(1, n.value))()
+    st = lib.svx_plan_chunks(len(h), hp, chunk_tokens, n_slots, buf, n.value, ctypes.byref(n))
+    if st != OK:
+        raise SvxError(st, "svx_plan_chunks: invalid arguments")
+    return [(e.chunk, e.slot, e.req, e.tok_start, e.n_tok) for e in buf[:n.value]]
+
+
+def candidate_masks(n_req: int, n_query: int, parent: Optional[np.ndarray] = None) -> np.ndarray:
+    out = np.zeros((n_req, n_query), dtype=np.uint32)
+    par = None
+    if parent is not None:
+        parent = np.ascontiguousarray(np.asarray(parent, dtype=np.int32).reshape(n_req, n_query))
+        par = parent.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    st = lib.svx_candidate_masks(n_req, n_query, par, out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)))
+    if st != OK:
+        raise SvxError(st, "svx_candidate_masks: invalid tree or sizes")
+    return out
+
+
+def check_coverage(hist_len: Sequence[int], parts: Sequence[tuple]) -> bool:
+    """parts: (req, tok_start, n_tok) triples."""
+    h, hp = _i64(hist_len)
+    p, pp = _i64(np.asarray(parts, dtype=np.int64).reshape(-1, 3) if len(parts) else np.zeros((0, 3)))
+    ok = ctypes.c_int32(-1)
+    st = lib.svx_check_coverage(len(h), hp, pp, len(parts), ctypes.byref(ok))
+    if st != OK:
+        raise SvxError(st, "svx_check_coverage: invalid arguments")
+    return bool(ok.value)
+
+
+# ------------------------------------------------------------ the round
+
+
+def _ptr(t) -> int:
+    """Device or host address of a torch tensor (or an int address)."""
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream_handle(s) -> Optional[int]:
+    if s is None:
+        return None
+    return int(getattr(s, "cuda_stream", s))
+
+
+class Verifier:
+    """One svx context: staging slots, state workspace, streams and events."""
+
+    def __init__(self, max_req: int, n_q_heads: int, n_kv_heads: int, head_dim: int, max_query: int,
+                 max_chunk_tokens: int, n_slots: int = 2, device: int = 0, compute_stream=None, copy_stream=None,
+                 timing: bool = False):
+        self._keep = (compute_stream, copy_stream)
+        cfg = Config(max_req, n_q_heads, n_kv_heads, head_dim, max_query, max_chunk_tokens, n_slots, device,
+                     _stream_handle(compute_stream), _stream_handle(copy_stream), FLAG_TIMING if timing else 0)
+        h = ctypes.c_void_p(None)
+        st = lib.svx_create(ctypes.byref(cfg), ctypes.byref(h))
+        if st != OK:
+            raise SvxError(st, lib.svx_last_error(None).decode())
+        self._h = h
+        self.cfg = cfg
+
+    def _check(self, st: int):
+        if st != OK:
+            raise SvxError(st, lib.svx_last_error(self._h).decode())
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib.svx_destroy(self._h)
+            self._h = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def round_begin(self, q, hist_len: Sequence[int], n_query: Optional[int] = None, scale: float = 0.0):
+        """q: device bf16 [B][Hq][nq][d]."""
+        n_req = len(hist_len)
+        nq = n_query if n_query is not None else int(q.shape[2])
+        h, hp = _i64(hist_len)
+        self._check(lib.svx_round_begin(self._h, n_req, nq, _ptr(q), hp, ctypes.c_float(scale)))
+
+    def push_chunk(self, parts: Sequence[tuple]):
+        """parts: (req, tok_start, k, v) with k, v bf16 [n_tok][Hkv][d] (pinned host or device)."""
+        arr = (Part * max(1, len(parts)))()
+        for i, (req, t0, k, v) in enumerate(parts):
+            n_tok = int(k.shape[0]) if not isinstance(k, int) else None
+            arr[i] = Part(req, n_tok, t0, _ptr(k), _ptr(v))
+        self._check(lib.svx_push_chunk(self._h, arr, len(parts)))
+
+    def push_raw(self, parts: Sequence[tuple]):
+        """parts: (req, tok_start, n_tok, k_addr, v_addr) with raw addresses."""
+        arr = (Part * max(1, len(parts)))()
+        for i, (req, t0, n, k, v) in enumerate(parts):
+            arr[i] = Part(req, n, t0, k, v)
+        self._check(lib.svx_push_chunk(self._h, arr, len(parts)))
+
+    def candidate_attn(self, k, v, parent: Optional[np.ndarray] = None, n_cand: Optional[int] = None):
+        """k, v: device bf16 [B][n_cand][Hkv][d]; parent: int32 [B][n_cand] or None (chain)."""
+        nc = n_cand if n_cand is not None else int(k.shape[1])
+        par = None
+        if parent is not None:
+            self._parent = np.ascontiguousarray(np.asarray(parent, dtype=np.int32))
+            par = self._parent.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        self._check(lib.svx_candidate_attn(self._h, _ptr(k), _ptr(v), nc, par))
+
+    def round_finish(self, o, lse, timeout_ms: int = 0):
+        """o: device bf16 [B][Hq][nq][d]; lse: device fp32 [B][Hq][nq]."""
+        self._check(lib.svx_round_finish(self._h, _ptr(o), _ptr(lse), timeout_ms))
+
+    def stats(self) -> dict:
+        s = Stats()
+        self._check(lib.svx_round_stats(self._h, ctypes.byref(s)))
+        return {f: getattr(s, f) for f, _ in Stats._fields_}
+
+    def run_round(self, q, hist_len: Sequence[int], hist_k: Sequence, hist_v: Sequence, chunk_tokens: int,
+                  o, lse, cand_k=None, cand_v=None, parent: Optional[np.ndarray] = None,
+                  chunk_order: Optional[Sequence[int]] = None, timeout_ms: int = 0, scale: float = 0.0):
+        """One round through the C ABI: begin, the candidate region (issued first so it runs under the
+        first transfer), one push per cohort chunk of the plan, finish.
+
+        hist_k[b], hist_v[b]: bf16 [C_b][Hkv][d] tensors (pinned host or device) or None when C_b = 0.
+        """
+        self.round_begin(q, hist_len, scale=scale)
+        if cand_k is not None:
+            self.candidate_attn(cand_k, cand_v, parent)
+        row_bytes = self.cfg.n_kv_heads * self.cfg.head_dim * 2
+        chunks = {}
+        for j, _slot, b, t0, n in plan_chunks(hist_len, chunk_tokens, self.cfg.n_slots):
+            chunks.setdefault(j, []).append((b, t0, n))
+        base_k = [None if k is None else _ptr(k) for k in hist_k]
+        base_v = [None if v is None else _ptr(v) for v in hist_v]
+        for j in (chunk_order if chunk_order is not None else sorted(chunks)):
+            parts = chunks[j]
+            arr = (Part * len(parts))()
+            for i, (b, t0, n) in enumerate(parts):
+                arr[i] = Part(b, n, t0, base_k[b] + t0 * row_bytes, base_v[b] + t0 * row_bytes)
+            self._check(lib.svx_push_chunk(self._h, arr, len(parts)))
+        self.round_finish(o, lse, timeout_ms)

@@ -1,0 +1,78 @@
+"""Shared test plumbing: seeded inputs -> torch tensors, one GPU round through the
+C ABI, the oracle on the same inputs, and the parity bar.
+
+Tolerances (written here, used by every parity test): O max abs error <= 1e-2 and
+mean abs error <= 1e-3 against the float64 oracle (bf16 output); LSE relative error
+<= 1e-4 (fp32 output).
+"""
+import numpy as np
+
+import oracle as O
+import workloads as W
+
+O_MAX_ABS = 1e-2
+O_MEAN_ABS = 1e-3
+LSE_REL = 1e-4
+
+
+def bf16_tensor(bits, device=None):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(device) if device is not None else t
+
+
+def pinned_alloc(shape):
+    import torch
+    return torch.empty(shape, dtype=torch.int16, pin_memory=True).numpy().view(np.uint16)
+
+
+def gpu_inputs(w, layer=0, resident=False):
+    """Draw one layer; history in pinned host memory (streamed) or in device memory (resident)."""
+    import torch
+    alloc = (lambda s: np.empty(s, dtype=np.uint16)) if resident else pinned_alloc
+    x = W.layer_inputs(w, layer, hist_alloc=alloc)
+    dev = torch.device("cuda")
+    t = {
+        "q": bf16_tensor(x.q, dev),
+        "kc": bf16_tensor(x.k_cand, dev),
+        "vc": bf16_tensor(x.v_cand, dev),
+        "kh": [bf16_tensor(k, dev if resident else None) if k.shape[0] else None for k in x.k_hist],
+        "vh": [bf16_tensor(v, dev if resident else None) if v.shape[0] else None for v in x.v_hist],
+    }
+    return x, t
+
+
+def run_gpu(v, w, t, x, chunk_order=None, with_candidates=True, timeout_ms=0):
+    import torch
+    B, Hq, nq, d = w.n_req, w.n_q_heads, w.n_query, w.head_dim
+    o = torch.empty((B, Hq, nq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, Hq, nq), dtype=torch.float32, device="cuda")
+    v.run_round(t["q"], w.hist_len, t["kh"], t["vh"], w.chunk_tokens, o, lse,
+                cand_k=t["kc"] if with_candidates else None, cand_v=t["vc"], parent=x.parent,
+                chunk_order=chunk_order, timeout_ms=timeout_ms)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def oracle_out(w, x, rows=None, with_candidates=True):
+    f = W.bf16_to_f64
+    vis = O.visibility_table(w.n_req, w.n_query, x.parent)
+    if not with_candidates:
+        vis = np.zeros_like(vis)
+    return O.verify_attention(f(x.q), [f(k) for k in x.k_hist], [f(v) for v in x.v_hist], f(x.k_cand),
+                              f(x.v_cand), vis, scale=w.scale, rows=rows)
+
+
+def check_parity(o_gpu, l_gpu, o_ref, l_ref, rows=None):
+    if rows is not None:
+        idx = tuple(np.array(rows).T)
+        o_gpu, l_gpu, o_ref, l_ref = o_gpu[idx], l_gpu[idx], o_ref[idx], l_ref[idx]
+    err = np.abs(o_gpu - o_ref)
+    fin = np.isfinite(l_ref)
+    rel = np.abs(l_gpu[fin] - l_ref[fin]) / np.maximum(np.abs(l_ref[fin]), 1e-30)
+    assert np.array_equal(np.isfinite(l_gpu), fin), "LSE finiteness differs"
+    assert err.max() <= O_MAX_ABS, f"O max abs err {err.max():.3e}"
+    assert err.mean() <= O_MEAN_ABS, f"O mean abs err {err.mean():.3e}"
+    if rel.size:
+        assert rel.max() <= LSE_REL, f"LSE rel err {rel.max():.3e}"
+    return float(err.max()), float(err.mean()), float(rel.max()) if rel.size else 0.0

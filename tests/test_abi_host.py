@@ -1,0 +1,126 @@
+"""The C library loads, exports every symbol its header declares, and its host-only
+bookkeeping (chunk plan, candidate visibility words, coverage check) matches the
+oracle bit for bit.  No GPU needed: none of these calls touches a device."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "svx.h")
+
+
+@pytest.fixture(scope="module")
+def svx():
+    from speculative_decoding_verification_chunked_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build()
+    from speculative_decoding_verification_chunked_gb300 import svx as mod
+    return mod
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(svx_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(svx):
+    names = header_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(svx.lib, n), n
+    assert sorted(svx.SYMBOLS) == names
+    assert "sm_103a" in svx.version()
+
+
+def test_plan_matches_oracle_on_named_workloads(svx):
+    for name in W.NAMES:
+        w = W.named(name)
+        for ns in (2, 3):
+            assert svx.plan_chunks(w.hist_len, w.chunk_tokens, ns) == \
+                [(j, s, b, t0, n) for j, s, b, t0, n in O.cohort_chunk_plan(w.hist_len, w.chunk_tokens, ns)]
+
+
+def test_plan_matches_oracle_random(svx):
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        hist = [int(x) for x in rng.integers(0, 3000, size=int(rng.integers(1, 20)))]
+        if rng.random() < 0.2:
+            hist[0] = 0
+        c = int(rng.integers(1, 700))
+        ns = int(rng.integers(1, 4))
+        assert svx.plan_chunks(hist, c, ns) == O.cohort_chunk_plan(hist, c, ns)
+    assert svx.plan_chunks([0, 0], 5, 2) == []
+
+
+def test_masks_match_oracle(svx):
+    rng = np.random.default_rng(1)
+    for nq in (1, 2, 5, 7, 16, 31, 32):
+        assert np.array_equal(svx.candidate_masks(3, nq), O.visibility_table(3, nq, None))
+        par = np.stack([W.random_tree(np.random.default_rng([nq, b]), nq, 5) for b in range(4)])
+        assert np.array_equal(svx.candidate_masks(4, nq, par), O.visibility_table(4, nq, par))
+        par = np.stack([W.random_tree(np.random.default_rng([nq, b, 9]), nq, 40) for b in range(2)])
+        assert np.array_equal(svx.candidate_masks(2, nq, par), O.visibility_table(2, nq, par))
+    w = W.named("tree")
+    par = W.tree_parents(w)
+    assert np.array_equal(svx.candidate_masks(w.n_req, w.n_query, par), O.visibility_table(w.n_req, w.n_query, par))
+    del rng
+
+
+def test_masks_reject_bad_trees(svx):
+    for bad in ([0, 0, 1], [-1, 1, 0], [-1, 0, 3], [-1, -1, 0]):
+        with pytest.raises(svx.SvxError):
+            svx.candidate_masks(1, 3, np.array([bad]))
+        with pytest.raises(ValueError):
+            O.candidate_visibility(3, bad)
+    with pytest.raises(svx.SvxError):
+        svx.candidate_masks(1, 33)
+
+
+def test_coverage_matches_oracle(svx):
+    rng = np.random.default_rng(2)
+    for trial in range(400):
+        hist = [int(x) for x in rng.integers(0, 40, size=int(rng.integers(1, 5)))]
+        plan = O.cohort_chunk_plan(hist, int(rng.integers(1, 9)), 2)
+        parts = [(b, t0, n) for _, _, b, t0, n in plan]
+        kind = trial % 6
+        if kind == 1 and parts:
+            parts.pop(int(rng.integers(0, len(parts))))
+        elif kind == 2 and parts:
+            parts.append(parts[int(rng.integers(0, len(parts)))])
+        elif kind == 3 and parts:
+            i = int(rng.integers(0, len(parts)))
+            b, t0, n = parts[i]
+            parts[i] = (b, max(0, t0 + int(rng.integers(-2, 3))), max(1, n + int(rng.integers(-2, 3))))
+        elif kind == 4:
+            parts.append((int(rng.integers(-1, len(hist) + 1)), int(rng.integers(-1, 50)), int(rng.integers(-1, 9))))
+        elif kind == 5:
+            rng.shuffle(parts)
+        assert svx.check_coverage(hist, parts) == O.covers_exactly_once(hist, parts), (hist, parts)
+
+
+def test_create_rejects_bad_config_without_touching_a_device(svx):
+    bad = [dict(head_dim=96), dict(max_query=33), dict(n_q_heads=12, n_kv_heads=8), dict(n_slots=4),
+           dict(max_req=0), dict(max_chunk_tokens=0)]
+    for kw in bad:
+        args = dict(max_req=2, n_q_heads=8, n_kv_heads=2, head_dim=128, max_query=5, max_chunk_tokens=64)
+        args.update(kw)
+        with pytest.raises(svx.SvxError) as e:
+            svx.Verifier(**args)
+        assert e.value.status in (svx.ERR_INVALID_ARG, svx.ERR_UNSUPPORTED)
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import importlib.util
+    src = os.path.join(ROOT, "speculative_decoding_verification_chunked_gb300", "svx.py")
+    dst = tmp_path / "svx_copy.py"
+    dst.write_text(open(src).read())
+    spec = importlib.util.spec_from_file_location("svx_copy", dst)
+    mod = importlib.util.module_from_spec(spec)
+    with pytest.raises(ImportError):
+        spec.loader.exec_module(mod)

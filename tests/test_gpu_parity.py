@@ -1,0 +1,185 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle on the
+same seeded inputs.  Bar (tests/helpers.py): O max abs <= 1e-2, mean abs <= 1e-3;
+LSE relative <= 1e-4.
+
+Small cases span several 32-token tiles, ragged tails, empty histories, several
+query-row blocks and both masks; full-size cases use the named workloads'
+shapes in the launch configuration the benchmark times and check sampled rows.
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+from helpers import check_parity, gpu_inputs, oracle_out, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def svx():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_verification_chunked_gb300 import svx as mod
+    return mod
+
+
+def make_verifier(svx, w, n_slots=2, chunk=None, **kw):
+    return svx.Verifier(w.n_req, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_query, chunk or w.chunk_tokens,
+                        n_slots=n_slots, **kw)
+
+
+SMALL = [
+    W.named("tiny"),
+    W.Workload("ragged", 5, 8, 2, 128, (0, 1, 33, 700, 1031), 256, 7, seed=11),
+    W.Workload("k0", 3, 8, 2, 128, (300, 64, 97), 64, 1, seed=12),
+    W.Workload("tree64", 3, 16, 4, 128, (200, 513, 1), 128, 16, tree=True, seed=13),
+    W.Workload("g8", 2, 16, 2, 128, (450, 333), 100, 4, seed=14),
+    W.Workload("g1", 2, 4, 4, 64, (129, 70), 32, 3, seed=15),
+    W.Workload("q32", 2, 8, 4, 128, (90, 257), 64, 32, seed=16),
+    W.Workload("tree32", 2, 8, 8, 64, (40, 77), 16, 32, tree=True, tree_max_depth=40, seed=17),
+    W.Workload("kscale", 4, 32, 8, 128, (777, 2048, 5, 4000), 512, 7, k_head_scale=True, seed=18),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+@pytest.mark.parametrize("resident", [False, True], ids=["streamed", "resident"])
+def test_small_parity(svx, w, resident):
+    x, t = gpu_inputs(w, resident=resident)
+    with make_verifier(svx, w) as v:
+        o, l = run_gpu(v, w, t, x)
+    check_parity(o, l, *oracle_out(w, x))
+
+
+def test_chunk_order_does_not_matter(svx):
+    w = SMALL[1]
+    x, t = gpu_inputs(w)
+    ref = oracle_out(w, x)
+    n_chunks = max(-(-C // w.chunk_tokens) for C in w.hist_len)
+    rng = np.random.default_rng(0)
+    with make_verifier(svx, w, n_slots=3) as v:
+        for order in (list(range(n_chunks))[::-1], list(rng.permutation(n_chunks))):
+            o, l = run_gpu(v, w, t, x, chunk_order=order)
+            check_parity(o, l, *ref)
+
+
+def test_back_to_back_rounds_and_no_candidates(svx):
+    w = SMALL[0].with_(n_req=2, hist_len=(512, 300))
+    with make_verifier(svx, w) as v:
+        for layer in range(3):
+            x, t = gpu_inputs(w, layer=layer)
+            o, l = run_gpu(v, w, t, x, with_candidates=(layer != 1), timeout_ms=60000)
+            check_parity(o, l, *oracle_out(w, x, with_candidates=(layer != 1)))
+
+
+def test_query_with_nothing_visible(svx):
+    import torch
+    w = W.Workload("empty", 2, 4, 2, 64, (0, 40), 16, 2, seed=19)
+    x, t = gpu_inputs(w)
+    with make_verifier(svx, w) as v:
+        o, l = run_gpu(v, w, t, x, with_candidates=False)
+    assert np.all(o[0] == 0) and np.all(np.isneginf(l[0]))
+    ref = oracle_out(w, x, rows=[(1, h, j) for h in range(4) for j in range(2)], with_candidates=False)
+    check_parity(o[1:], l[1:], ref[0][1:], ref[1][1:])
+    del torch
+
+
+def test_mixed_host_and_device_parts_in_one_push(svx):
+    import torch
+    w = W.Workload("mixed", 4, 8, 2, 128, (300, 260, 0, 511), 128, 5, seed=20)
+    x, t = gpu_inputs(w)
+    # requests 1 and 3 keep their history on the device, 0 stays pinned host memory
+    for b in (1, 3):
+        t["kh"][b] = t["kh"][b].cuda()
+        t["vh"][b] = t["vh"][b].cuda()
+    with make_verifier(svx, w) as v:
+        o, l = run_gpu(v, w, t, x)
+    check_parity(o, l, *oracle_out(w, x))
+    del torch
+
+
+def test_user_streams_and_timing_stats(svx):
+    import torch
+    w = SMALL[1]
+    x, t = gpu_inputs(w)
+    cs, xs = torch.cuda.Stream(), torch.cuda.Stream()
+    with make_verifier(svx, w, compute_stream=cs, copy_stream=xs, timing=True) as v:
+        o, l = run_gpu(v, w, t, x)
+        st = v.stats()
+    check_parity(o, l, *oracle_out(w, x))
+    assert st["h2d_bytes"] == w.hist_bytes and st["device_bytes"] == 0
+    assert st["n_copies"] == 2 * sum(-(-C // w.chunk_tokens) for C in w.hist_len)
+    assert st["round_ms"] > 0 and st["chunk_kernel_ms"] > 0 and st["copy_busy_ms"] > 0
+
+
+# ---------------------------------------------------------------- errors
+
+
+def test_state_machine_and_argument_errors(svx):
+    import torch
+    w = W.Workload("err", 2, 8, 2, 128, (100, 50), 64, 3, seed=21)
+    x, t = gpu_inputs(w)
+    o = torch.empty((2, 8, 3, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((2, 8, 3), dtype=torch.float32, device="cuda")
+    with make_verifier(svx, w) as v:
+        def status(fn, *a, **k):
+            try:
+                fn(*a, **k)
+                return svx.OK
+            except svx.SvxError as e:
+                return e.status
+
+        kh, vh = t["kh"], t["vh"]
+        assert status(v.push_chunk, [(0, 0, kh[0][:64], vh[0][:64])]) == svx.ERR_BAD_STATE
+        assert status(v.round_finish, o, lse) == svx.ERR_BAD_STATE
+        v.round_begin(t["q"], w.hist_len)
+        assert status(v.round_begin, t["q"], w.hist_len) == svx.ERR_BAD_STATE
+        # part past the end of the history, duplicate request, too many tokens for a slot
+        assert status(v.push_chunk, [(1, 40, kh[1][:20], vh[1][:20])]) == svx.ERR_INVALID_ARG
+        assert status(v.push_chunk, [(0, 0, kh[0][:10], vh[0][:10]), (0, 10, kh[0][10:20], vh[0][10:20])]) \
+            == svx.ERR_INVALID_ARG
+        assert status(v.push_chunk, [(0, 0, kh[0][:100], vh[0][:100])]) == svx.ERR_INVALID_ARG
+        # pageable host memory cannot be streamed
+        pk = torch.zeros((10, 2, 128), dtype=torch.bfloat16)
+        assert status(v.push_chunk, [(0, 0, pk, pk)]) == svx.ERR_INVALID_ARG
+        # wrong candidate count, bad tree
+        assert status(v.candidate_attn, t["kc"], t["vc"], None, 2) == svx.ERR_INVALID_ARG
+        assert status(v.candidate_attn, t["kc"], t["vc"], np.array([[0, 0, 1], [-1, 0, 1]])) == svx.ERR_INVALID_ARG
+        # a missing chunk fails the coverage check at finish and closes the round
+        v.push_chunk([(0, 0, kh[0][:64], vh[0][:64]), (1, 0, kh[1][:50], vh[1][:50])])
+        assert status(v.round_finish, o, lse) == svx.ERR_INVALID_ARG
+        assert "coverage" in svx.lib.svx_last_error(v._h).decode()
+        # duplicate coverage is rejected too
+        v.round_begin(t["q"], w.hist_len)
+        v.push_chunk([(0, 0, kh[0][:64], vh[0][:64]), (1, 0, kh[1][:50], vh[1][:50])])
+        v.push_chunk([(0, 64, kh[0][64:], vh[0][64:])])
+        v.push_chunk([(0, 64, kh[0][64:], vh[0][64:])])
+        assert status(v.round_finish, o, lse) == svx.ERR_INVALID_ARG
+        # and the context still computes a correct round afterwards
+        o2, l2 = run_gpu(v, w, t, x, timeout_ms=60000)
+    check_parity(o2, l2, *oracle_out(w, x))
+
+
+# ---------------------------------------------------------------- full size, sampled rows
+
+
+def sample_rows(w, n, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = {(int(rng.integers(0, w.n_req)), int(rng.integers(0, w.n_q_heads)), int(rng.integers(0, w.n_query)))
+            for _ in range(n)}
+    rows |= {(w.n_req - 1, w.n_q_heads - 1, w.n_query - 1), (0, 0, 0)}
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", ["qwen3", "internlm", "tree", "fulldepth"])
+def test_full_size_sampled(svx, name):
+    w = W.named(name)
+    if name == "fulldepth":
+        w = w.with_(n_layers=1)  # one layer of the 36-layer stack: same shapes per layer
+    x, t = gpu_inputs(w)
+    with make_verifier(svx, w, n_slots=3) as v:
+        o, l = run_gpu(v, w, t, x)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
+    rows = sample_rows(w, 24)
+    ref = oracle_out(w, x, rows=rows)
+    check_parity(o, l, *ref, rows=rows)
