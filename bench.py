@@ -45,8 +45,8 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["svx", "reference"], default="svx")
     ap.add_argument("--workload", default="qwen3", choices=["tiny", "qwen3", "internlm", "tree"])
     ap.add_argument("--slots", type=int, default=3, choices=[2, 3])
@@ -376,9 +376,8 @@ def main(argv=None):
     del probe_d
 
     # ---- value: resident history (HBM-bound form)
-    with ClockSampler(local) as clk:
-        ms_res, kern_ms = timed(resident_step, a.steps, a.warmup, with_events=True)
-    clocks = clk.summary()
+    clk = ClockSampler(local).__enter__()  # sampled over both timed regions
+    ms_res, kern_ms = timed(resident_step, a.steps, a.warmup, with_events=True)
     value, ms_res_job = job_throughput(B * nq, ms_res, world, dev)
     toks_per_launch = [sum(n for _, _, n, _, _ in p) for p in res_pushes]
     k1_ms_per_launch = statistics.mean(kern_ms)
@@ -386,9 +385,9 @@ def main(argv=None):
     achieved = k1_bytes_per_launch / (k1_ms_per_launch / 1e3) / 1e9
 
     # ---- e2e: streamed from pinned host, copies in the timed region
-    with ClockSampler(local) as clk2:
-        ms_e2e, _ = timed(e2e_step, a.steps, a.warmup)
-    clocks2 = clk2.summary()
+    ms_e2e, _ = timed(e2e_step, a.steps, a.warmup)
+    clk.__exit__(None, None, None)
+    clocks = clk.summary()
     e2e_value, ms_e2e_job = job_throughput(B * nq, ms_e2e, world, dev)
     h2d_step = hist_bytes + (q_h.numel() + kc_h.numel() + vc_h.numel()) * 2
     d2h_step = o_h.numel() * 2 + lse_h.numel() * 4
@@ -449,7 +448,7 @@ def main(argv=None):
                      "resident_chunk_kernel_ms": r_chunk},
         "resident": {"hist_gb_per_s": hist_bytes / (ms_res / 1e3) / 1e9,
                      "hbm_frac": hist_bytes / (ms_res / 1e3) / 1e9 / hbm_peak},
-        "clocks": clocks, "clocks_e2e": clocks2,
+        "clocks": clocks,
     }
     if cpu:
         out["cpu_baseline"] = cpu

@@ -58,7 +58,8 @@ typedef enum {
 typedef struct svx_ctx_s* svx_ctx;
 
 /* svx_config.flags */
-#define SVX_FLAG_TIMING 1u /* record CUDA events around copies and kernels (svx_round_stats) */
+#define SVX_FLAG_TIMING 1u           /* record CUDA events around copies and kernels (svx_round_stats) */
+#define SVX_FLAG_NO_TENSOR_CORES 2u  /* run the history chunk kernel on FP32 FMA even where d = 128 */
 
 /* Context configuration.  Shapes are fixed for the context's lifetime (the
  * Cohort compatibility rule of section 4.2: one layer shape, verification

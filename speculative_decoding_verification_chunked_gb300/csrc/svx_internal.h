@@ -1,5 +1,12 @@
 // Internal interface between the host runtime (svx_runtime.cu) and the kernels
-// (svx_kernels.cu).  Not part of the C ABI.
+// (svx_kernels.cu, svx_tc_kernel.cu).  Not part of the C ABI.
+//
+// Running state.  Each (state slot, query row) holds the online-softmax state
+// of section 4.2 of "Resource-Efficient Speculative Decoding for Long-Context
+// LLM Serving": m (running maximum, log2 units), l (denominator relative to m)
+// and a[d] (un-normalised value sum), plus the round epoch that last wrote it.
+// A kernel that finds an older epoch treats the row as empty, (-inf, 0, 0), so
+// no reset pass is needed between rounds; every writer merges with Eq. (8).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -9,61 +16,80 @@
 namespace svx {
 
 constexpr int kMaxReq = 256;
-constexpr int kMaxPartsPerLaunch = 64;  // keeps the kernel parameter block near 2 KiB
-constexpr int kMaxHistSplits = 16;      // history state slots per request
+constexpr int kMaxPartsPerLaunch = 64;  // keeps the kernel parameter block near 2.5 KiB
+constexpr int kHistSlots = 8;           // history state slots per query row
 constexpr int kTile = 32;               // KV tokens per shared-memory tile (FMA kernel)
 constexpr int kRowsPerBlock = 32;       // query rows (G * nq) per CTA of the FMA kernel
+constexpr int kTcTile = 128;            // KV tokens per tile (tensor-core kernel, MMA M)
+
+// Per-row state header; a[d] lives in a separate array with the same row index.
+struct __align__(16) RowState {
+  float m;         // running max of the scaled scores, log2 units
+  float l;         // sum of 2^(s - m)
+  uint32_t epoch;  // round that wrote this row
+  uint32_t pad;
+};
 
 // One request's KV slice processed by one chunk-kernel launch.
 struct PartDesc {
   const __nv_bfloat16* k;  // [n_tok][Hkv][d]
   const __nv_bfloat16* v;
+  int64_t tile_base;  // tensor-core kernel: first global tile index of this part
   int32_t req;
   int32_t n_tok;
-  uint32_t init_mask;  // bit s: state slot (slot_base + s) holds nothing yet -> overwrite
-  int32_t pad;
 };
 
-// Parameters of the chunk kernel (history chunks) and of its masked form
-// (candidate region).
 struct ChunkParams {
   const __nv_bfloat16* q;  // [B][Hq][nq][d]
-  float2* ws_ml;           // [slots][slot_stride] running (m in log2 units, l)
-  float* ws_a;             // [slots][slot_stride][d] running un-normalised value sum
+  RowState* ws_h;          // [slots][slot_stride]
+  float* ws_a;             // [slots][slot_stride][d]
   const uint32_t* vis;     // [B][nq] candidate visibility words (masked form only)
+  int* err;                // device error word (bounded waits that gave up)
   int64_t slot_stride;     // state rows per slot (max_req * Hq * max_query)
+  int64_t total_tiles;     // tensor-core kernel: tiles over all (part, head, row block)
   float q_scale;           // softmax scale * log2(e)
+  uint32_t epoch;          // this round
   int32_t n_q_heads;
   int32_t n_kv_heads;
   int32_t group;     // G = Hq / Hkv
   int32_t n_query;   // nq
-  int32_t splits;    // token splits per part (CTAs along grid x)
-  int32_t slot_base; // state slot of split 0
+  int32_t splits;    // FMA kernel: token splits per part (grid x)
+  int32_t slot_base; // state slot of split / segment 0
   int32_t n_parts;
-  int32_t n_rowblk;  // CTAs per part along the query rows (ceil(G*nq / kRowsPerBlock))
-  int32_t pad0;
+  int32_t n_rowblk;  // CTAs (FMA) or segments (tensor core) per (part, head) along the query rows
   PartDesc parts[kMaxPartsPerLaunch];
 };
 
 struct FinishParams {
-  const float2* ws_ml;
+  const RowState* ws_h;
   const float* ws_a;
   int64_t slot_stride;
   __nv_bfloat16* o;  // [B][Hq][nq][d]
   float* lse;        // [B][Hq][nq]
+  uint32_t epoch;
   int32_t n_req;
   int32_t n_q_heads;
   int32_t n_query;
-  int32_t pad0;
-  uint32_t slot_mask[kMaxReq];  // per request: state slots that hold data
+  uint32_t slot_mask[kMaxReq];  // per request: state slots that may hold data this round
 };
 
-// Split s of a part with n_tiles tiles covers tiles [s*n/S, (s+1)*n/S).
+// FMA kernel: split s of a part with n_tiles tiles covers tiles [s*n/S, (s+1)*n/S).
 __host__ __device__ inline int64_t split_tile_begin(int64_t n_tiles, int s, int splits) {
   return (n_tiles * s) / splits;
 }
 
+// Tensor-core kernel work split ("stream-K" over tiles): CTA k of n owns the
+// global tiles [k*T/n, (k+1)*T/n); the CTA holding tile x is cta_of_tile(x).
+__host__ __device__ inline int64_t cta_tile_begin(int64_t k, int64_t n, int64_t T) { return (k * T) / n; }
+__host__ __device__ inline int64_t cta_of_tile(int64_t x, int64_t n, int64_t T) { return ((x + 1) * n - 1) / T; }
+
 cudaError_t launch_chunk_attn(const ChunkParams& p, int head_dim, bool masked, cudaStream_t stream);
 cudaError_t launch_finish(const FinishParams& p, int head_dim, cudaStream_t stream);
+
+// Tensor-core chunk kernel (d = 128, rows per (part, head) block padded to ncol = 32 or 64).
+bool tc_supported(int head_dim, int rows);
+int tc_ncol(int rows);
+int tc_max_ctas(int num_sms);
+cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int ncol, int n_ctas, cudaStream_t stream);
 
 }  // namespace svx

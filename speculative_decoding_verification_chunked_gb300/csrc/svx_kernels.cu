@@ -224,38 +224,35 @@ __global__ void __launch_bounds__(128) chunk_attn_fma(const __grid_constant__ Ch
     __syncthreads();  // the buffer is refilled by the next iteration's prefetch
   }
 
-  // merge this CTA's state into its slot (Eq. 8), or overwrite a fresh slot
-  const bool fresh = (part.init_mask >> split) & 1u;
+  // merge this CTA's state into its slot (Eq. 8); a row last written by an
+  // older round counts as empty
   const int64_t slot_row0 = static_cast<int64_t>(P.slot_base + split) * P.slot_stride + row_base + r0;
 #pragma unroll
   for (int i = 0; i < RPW; ++i) {
     if (i < nrw) {
       const int rr = warp + 4 * i;
       const float lt = warp_sum(l[i]);
+      RowState* hp = P.ws_h + slot_row0 + rr;
+      float* ap = P.ws_a + (slot_row0 + rr) * D + lane * VPL;
+      const RowState old = *hp;
       float mo = m[i], lo = lt;
       float a[VPL];
 #pragma unroll
       for (int c = 0; c < VPL; ++c) a[c] = acc[i][c];
-      float2* mlp = P.ws_ml + slot_row0 + rr;
-      float* ap = P.ws_a + (slot_row0 + rr) * D + lane * VPL;
-      if (!fresh) {
-        const float2 old = *mlp;
-        const float mn = fmaxf(old.x, m[i]);
+      if (old.epoch == P.epoch) {
+        const float mn = fmaxf(old.m, m[i]);
         if (mn != kNegInf) {
-          const float al = exp2_approx(old.x - mn), be = exp2_approx(m[i] - mn);
-          lo = old.y * al + lt * be;
+          const float al = exp2_approx(old.m - mn), be = exp2_approx(m[i] - mn);
+          lo = old.l * al + lt * be;
 #pragma unroll
           for (int c = 0; c < VPL; ++c) a[c] = ap[c] * al + a[c] * be;
           mo = mn;
-        } else {
-#pragma unroll
-          for (int c = 0; c < VPL; ++c) a[c] = 0.f;
-          lo = 0.f;
         }
       }
-      if (lane == 0) *mlp = make_float2(mo, lo);
+      __syncwarp();  // every lane has read the old header before lane 0 replaces it
 #pragma unroll
       for (int c = 0; c < VPL; ++c) ap[c] = a[c];
+      if (lane == 0) *hp = RowState{mo, lo, P.epoch, 0u};
     }
   }
 }
@@ -280,14 +277,15 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
     const int s = __ffs(mask) - 1;
     mask &= mask - 1;
     const int64_t idx = static_cast<int64_t>(s) * P.slot_stride + row;
-    const float2 ml = P.ws_ml[idx];
-    const float mn = fmaxf(m, ml.x);
+    const RowState h = P.ws_h[idx];
+    if (h.epoch != P.epoch) continue;  // slot not written for this row in this round
+    const float mn = fmaxf(m, h.m);
     if (mn == kNegInf) continue;
-    const float al = exp2_approx(m - mn), be = exp2_approx(ml.x - mn);
+    const float al = exp2_approx(m - mn), be = exp2_approx(h.m - mn);
     const float* ap = P.ws_a + idx * D + lane * VPL;
 #pragma unroll
     for (int c = 0; c < VPL; ++c) a[c] = a[c] * al + ap[c] * be;
-    l = l * al + ml.y * be;
+    l = l * al + h.l * be;
     m = mn;
   }
   __nv_bfloat16* op = P.o + row * D + lane * VPL;

@@ -52,11 +52,14 @@ struct svx_ctx_s {
   std::vector<cudaEvent_t> slot_ready, slot_free;
   int next_slot = 0;
 
-  // fp32 state workspace: (max_hist_splits + 1) slots; the last one is the candidate region's
-  float2* ws_ml = nullptr;
+  // fp32 state workspace: kHistSlots history slots + 1 candidate-region slot,
+  // rows stamped with the round epoch that wrote them
+  svx::RowState* ws_h = nullptr;
   float* ws_a = nullptr;
   int64_t slot_stride = 0;
-  int max_splits = 1;
+  uint32_t epoch = 0;
+  int* d_err = nullptr;   // device error word: a kernel's bounded wait gave up
+  bool use_tc = false;    // chunk kernel on the tensor cores (d = 128)
 
   // candidate visibility words: pinned host staging and device copy
   uint32_t* h_vis = nullptr;
@@ -204,7 +207,8 @@ void destroy_all(svx_ctx c) {
   }
   for (cudaEvent_t e : {c->ev_begin, c->ev_c0, c->ev_c1, c->ev_f0, c->ev_f1, c->vis_copied, c->done})
     if (e) cudaEventDestroy(e);
-  if (c->ws_ml) cudaFree(c->ws_ml);
+  if (c->ws_h) cudaFree(c->ws_h);
+  if (c->d_err) cudaFree(c->d_err);
   if (c->ws_a) cudaFree(c->ws_a);
   if (c->d_vis) cudaFree(c->d_vis);
   if (c->h_vis) cudaFreeHost(c->h_vis);
@@ -233,16 +237,29 @@ cudaEvent_t make_event(bool timing) {
   return e;
 }
 
-// Number of token splits per part for one chunk-kernel launch: enough CTAs for
-// about two per SM, never more tiles than the longest part has.
+// Number of token splits per part for one FMA chunk-kernel launch: enough CTAs
+// for about two per SM, never more tiles than the longest part has.
 int choose_splits(svx_ctx c, int n_parts, int64_t max_tok, int n_rowblk) {
   const int64_t pairs = static_cast<int64_t>(n_parts) * c->cfg.n_kv_heads * n_rowblk;
   const int64_t target = 2LL * c->num_sms;
   int64_t s = (target + pairs - 1) / pairs;
   const int64_t tiles = (max_tok + svx::kTile - 1) / svx::kTile;
   s = std::min<int64_t>(s, std::max<int64_t>(tiles, 1));
-  s = std::max<int64_t>(1, std::min<int64_t>(s, c->max_splits));
+  s = std::max<int64_t>(1, std::min<int64_t>(s, svx::kHistSlots));
   return static_cast<int>(s);
+}
+
+// Largest number of CTAs that one (part, head, row block) pair spreads over
+// when T tiles are split evenly over n CTAs.
+int64_t max_segments(const std::vector<int64_t>& pair_first, const std::vector<int64_t>& pair_tiles, int64_t n,
+                     int64_t T) {
+  int64_t worst = 0;
+  for (size_t i = 0; i < pair_first.size(); ++i) {
+    const int64_t a = svx::cta_of_tile(pair_first[i], n, T);
+    const int64_t b = svx::cta_of_tile(pair_first[i] + pair_tiles[i] - 1, n, T);
+    worst = std::max(worst, b - a + 1);
+  }
+  return worst;
 }
 
 uint32_t nonempty_splits(int64_t n_tok, int splits) {
@@ -320,19 +337,24 @@ svx_status svx_create(const svx_config* cfg, svx_ctx* out) {
     c->slot_ready.push_back(a);
     c->slot_free.push_back(b);
   }
-  // history splits: about two CTAs per SM over the (request, KV head) pairs of a full Cohort
-  const int64_t pairs = static_cast<int64_t>(k.max_req) * k.n_kv_heads;
-  c->max_splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(svx::kMaxHistSplits,
-                                                                          (2LL * c->num_sms + pairs - 1) / pairs)));
+  c->use_tc = !(k.flags & SVX_FLAG_NO_TENSOR_CORES) && svx::tc_supported(k.head_dim, c->group * k.max_query);
   c->slot_stride = static_cast<int64_t>(k.max_req) * k.n_q_heads * k.max_query;
-  const int64_t n_state = static_cast<int64_t>(c->max_splits + 1) * c->slot_stride;
-  if (cudaMalloc(reinterpret_cast<void**>(&c->ws_ml), static_cast<size_t>(n_state) * sizeof(float2)) != cudaSuccess ||
+  const int64_t n_state = static_cast<int64_t>(svx::kHistSlots + 1) * c->slot_stride;
+  if (cudaMalloc(reinterpret_cast<void**>(&c->ws_h), static_cast<size_t>(n_state) * sizeof(svx::RowState)) !=
+          cudaSuccess ||
       cudaMalloc(reinterpret_cast<void**>(&c->ws_a), static_cast<size_t>(n_state) * k.head_dim * sizeof(float)) !=
           cudaSuccess ||
       cudaMalloc(reinterpret_cast<void**>(&c->d_vis), static_cast<size_t>(k.max_req) * 32 * sizeof(uint32_t)) !=
-          cudaSuccess) {
+          cudaSuccess ||
+      cudaMalloc(reinterpret_cast<void**>(&c->d_err), sizeof(int)) != cudaSuccess) {
     cudaGetLastError();
     return bail(SVX_ERR_OOM, "workspace allocation failed");
+  }
+  // epoch 0 marks every state row as never written (rounds count from 1)
+  if (cudaMemset(c->ws_h, 0, static_cast<size_t>(n_state) * sizeof(svx::RowState)) != cudaSuccess ||
+      cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return bail(SVX_ERR_CUDA, "workspace initialisation failed");
   }
   if (cudaHostAlloc(reinterpret_cast<void**>(&c->h_vis), static_cast<size_t>(k.max_req) * 32 * sizeof(uint32_t),
                     cudaHostAllocDefault) != cudaSuccess) {
@@ -386,6 +408,7 @@ svx_status svx_round_begin(svx_ctx c, int32_t n_req, int32_t n_query, const void
   c->last_stats_pending = false;
   c->h2d_bytes = c->dev_bytes = 0;
   c->n_launch = c->n_copies = 0;
+  c->epoch = c->epoch == 0xffffffffu ? 1u : c->epoch + 1u;
   if (c->cfg.flags & SVX_FLAG_TIMING) SVX_CUDA(c, cudaEventRecord(c->ev_begin, c->cs));
   c->state = RoundState::kOpen;
   return SVX_OK;
@@ -394,39 +417,62 @@ svx_status svx_round_begin(svx_ctx c, int32_t n_req, int32_t n_query, const void
 namespace {
 
 // Launches the chunk kernel over `parts` (already resolved to device pointers),
-// in batches of at most kMaxPartsPerLaunch parts.
+// in batches of at most kMaxPartsPerLaunch parts, and records which state slots
+// each request may now hold.
 svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, bool masked, int slot_base, int splits_override) {
   const int R = c->group * c->n_query;
-  const int n_rowblk = (R + svx::kRowsPerBlock - 1) / svx::kRowsPerBlock;
   for (size_t i0 = 0; i0 < parts.size(); i0 += svx::kMaxPartsPerLaunch) {
     const int n = static_cast<int>(std::min<size_t>(svx::kMaxPartsPerLaunch, parts.size() - i0));
     ChunkParams p;
     std::memset(&p, 0, sizeof(p));
     p.q = c->q;
-    p.ws_ml = c->ws_ml;
+    p.ws_h = c->ws_h;
     p.ws_a = c->ws_a;
     p.vis = masked ? c->d_vis : nullptr;
+    p.err = c->d_err;
     p.slot_stride = c->slot_stride;
     p.q_scale = c->q_scale;
+    p.epoch = c->epoch;
     p.n_q_heads = c->cfg.n_q_heads;
     p.n_kv_heads = c->cfg.n_kv_heads;
     p.group = c->group;
     p.n_query = c->n_query;
     p.slot_base = slot_base;
     p.n_parts = n;
-    p.n_rowblk = n_rowblk;
-    int64_t max_tok = 0;
-    for (int i = 0; i < n; ++i) max_tok = std::max<int64_t>(max_tok, parts[i0 + i].n_tok);
-    p.splits = splits_override > 0 ? splits_override : choose_splits(c, n, max_tok, n_rowblk);
-    for (int i = 0; i < n; ++i) {
-      PartDesc d = parts[i0 + i];
-      const uint32_t ne = nonempty_splits(d.n_tok, p.splits) << slot_base;
-      uint32_t& used = c->slot_mask[static_cast<size_t>(d.req)];
-      d.init_mask = (ne & ~used) >> slot_base;
-      used |= ne;
-      p.parts[i] = d;
+    for (int i = 0; i < n; ++i) p.parts[i] = parts[i0 + i];
+    if (c->use_tc && !masked) {
+      // tensor-core kernel: tiles of all (part, head, row block) pairs split evenly over the CTAs
+      const int ncol = svx::tc_ncol(R);
+      p.n_rowblk = (R + ncol - 1) / ncol;
+      std::vector<int64_t> pair_first, pair_tiles;
+      int64_t T = 0;
+      for (int i = 0; i < n; ++i) {
+        const int64_t nt = (static_cast<int64_t>(p.parts[i].n_tok) + svx::kTcTile - 1) / svx::kTcTile;
+        p.parts[i].tile_base = T;
+        for (int pr = 0; pr < c->cfg.n_kv_heads * p.n_rowblk; ++pr) {
+          pair_first.push_back(T + pr * nt);
+          pair_tiles.push_back(nt);
+        }
+        T += nt * c->cfg.n_kv_heads * p.n_rowblk;
+      }
+      p.total_tiles = T;
+      int64_t ctas = std::min<int64_t>(svx::tc_max_ctas(c->num_sms), T);
+      while (ctas > 1 && max_segments(pair_first, pair_tiles, ctas, T) > svx::kHistSlots) --ctas;
+      const int64_t segs = max_segments(pair_first, pair_tiles, ctas, T);
+      for (int i = 0; i < n; ++i) {
+        uint32_t& used = c->slot_mask[static_cast<size_t>(p.parts[i].req)];
+        used |= ((segs >= 32 ? 0xffffffffu : ((1u << segs) - 1u)) << slot_base);
+      }
+      SVX_CUDA(c, svx::launch_chunk_attn_tc(p, ncol, static_cast<int>(ctas), c->cs));
+    } else {
+      p.n_rowblk = (R + svx::kRowsPerBlock - 1) / svx::kRowsPerBlock;
+      int64_t max_tok = 0;
+      for (int i = 0; i < n; ++i) max_tok = std::max<int64_t>(max_tok, p.parts[i].n_tok);
+      p.splits = splits_override > 0 ? splits_override : choose_splits(c, n, max_tok, p.n_rowblk);
+      for (int i = 0; i < n; ++i)
+        c->slot_mask[static_cast<size_t>(p.parts[i].req)] |= nonempty_splits(p.parts[i].n_tok, p.splits) << slot_base;
+      SVX_CUDA(c, svx::launch_chunk_attn(p, c->cfg.head_dim, masked, c->cs));
     }
-    SVX_CUDA(c, svx::launch_chunk_attn(p, c->cfg.head_dim, masked, c->cs));
     ++c->n_launch;
   }
   return SVX_OK;
@@ -495,7 +541,7 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
       const size_t bytes = static_cast<size_t>(p.n_tok) * row_elems * 2;
       SVX_CUDA(c, cudaMemcpyAsync(dk, p.k, bytes, cudaMemcpyHostToDevice, c->xs));
       SVX_CUDA(c, cudaMemcpyAsync(dv, p.v, bytes, cudaMemcpyHostToDevice, c->xs));
-      desc[static_cast<size_t>(i)] = PartDesc{dk, dv, p.req, p.n_tok, 0u, 0};
+      desc[static_cast<size_t>(i)] = PartDesc{dk, dv, 0, p.req, p.n_tok};
       c->h2d_bytes += 2 * static_cast<int64_t>(bytes);
       c->n_copies += 2;
       ++hi;
@@ -508,7 +554,7 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
     const svx_part& p = parts[i];
     if (kind[static_cast<size_t>(i)] == 2) {
       desc[static_cast<size_t>(i)] = PartDesc{static_cast<const __nv_bfloat16*>(p.k),
-                                              static_cast<const __nv_bfloat16*>(p.v), p.req, p.n_tok, 0u, 0};
+                                              static_cast<const __nv_bfloat16*>(p.v), 0, p.req, p.n_tok};
       c->dev_bytes += 2 * static_cast<int64_t>(p.n_tok) * row_elems * 2;
     }
     c->parts_seen.push_back({p.req, p.tok_start, p.n_tok});
@@ -551,10 +597,10 @@ svx_status svx_candidate_attn(svx_ctx c, const void* k_dev, const void* v_dev, i
   std::vector<PartDesc> desc(static_cast<size_t>(c->n_req));
   for (int b = 0; b < c->n_req; ++b)
     desc[static_cast<size_t>(b)] = PartDesc{static_cast<const __nv_bfloat16*>(k_dev) + b * per_req,
-                                            static_cast<const __nv_bfloat16*>(v_dev) + b * per_req, b, n_cand, 0u, 0};
+                                            static_cast<const __nv_bfloat16*>(v_dev) + b * per_req, 0, b, n_cand};
   const bool timing = (c->cfg.flags & SVX_FLAG_TIMING) != 0;
   if (timing) SVX_CUDA(c, cudaEventRecord(c->ev_c0, c->cs));
-  svx_status st = launch_parts(c, desc, true, c->max_splits, 1);
+  svx_status st = launch_parts(c, desc, true, svx::kHistSlots, 1);
   if (st != SVX_OK) return st;
   if (timing) {
     SVX_CUDA(c, cudaEventRecord(c->ev_c1, c->cs));
@@ -580,9 +626,10 @@ svx_status svx_round_finish(svx_ctx c, void* o_dev, float* lse_dev, int32_t time
   }
   FinishParams p;
   std::memset(&p, 0, sizeof(p));
-  p.ws_ml = c->ws_ml;
+  p.ws_h = c->ws_h;
   p.ws_a = c->ws_a;
   p.slot_stride = c->slot_stride;
+  p.epoch = c->epoch;
   p.o = static_cast<__nv_bfloat16*>(o_dev);
   p.lse = lse_dev;
   p.n_req = c->n_req;
@@ -607,7 +654,12 @@ svx_status svx_round_finish(svx_ctx c, void* o_dev, float* lse_dev, int32_t time
     const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms);
     for (;;) {
       cudaError_t e = cudaEventQuery(c->done);
-      if (e == cudaSuccess) break;
+      if (e == cudaSuccess) {
+        int dev_err = 0;
+        SVX_CUDA(c, cudaMemcpy(&dev_err, c->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+        if (dev_err) return fail(c, SVX_ERR_CUDA, "a kernel gave up waiting (device error word %d)", dev_err);
+        break;
+      }
       if (e != cudaErrorNotReady) return fail(c, SVX_ERR_CUDA, "round failed: %s", cudaGetErrorString(e));
       if (std::chrono::steady_clock::now() >= deadline)
         return fail(c, SVX_ERR_TIMEOUT, "round not complete after %d ms", timeout_ms);

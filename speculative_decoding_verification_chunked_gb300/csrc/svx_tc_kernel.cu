@@ -1,0 +1,644 @@
+// Chunk attention on the 5th-generation tensor cores (tcgen05, TMEM), d = 128.
+//
+// One history chunk of "Resource-Efficient Speculative Decoding for
+// Long-Context LLM Serving", section 4.2, is shared by every verification query
+// of the round: for a (request, KV head) pair the G*nq query rows attend to all
+// tokens of the chunk, and the chunk-local online-softmax state (Eq. 7) is
+// merged into the running state (Eq. 8).
+//
+// Shape of the work.  A KV tile of 128 tokens sits on the MMA M dimension and
+// the (padded) query rows on N, so a small query group (20-64 rows) does not
+// waste a 128-row MMA:
+//   S^T  = K_tile . Q^T      M = 128 tokens, N = NCOL rows, K = d      (TMEM)
+//   P^T  = 2^(S^T*scale - m) per row, written bf16 to shared memory
+//   O^T  = V_tile^T . P^T    M = d = 128,    N = NCOL rows, K = 128 tokens (TMEM)
+// and the fp32 output accumulator lives in registers (thread = one of the 128
+// output dimensions), updated one tile behind the MMAs: acc = acc*alpha + O^T.
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warps 0-3  softmax and accumulation; thread t owns TMEM lane t (token t of
+//              the S tile, output dimension t of the O tile)
+//   warp 4     producer: 16-byte cp.async of K/V tiles into a ring of stages,
+//              written in the 128-byte-swizzled layout the MMA descriptors name
+//   warp 5     one thread issues the MMAs and their commits
+// Work split: "stream-K" over the tiles of all (part, KV head, row block)
+// pairs, so every CTA gets the same number of tiles; a CTA that covers part of
+// a pair writes that segment's state into its own state slot, and the finish
+// kernel merges the slots.
+//
+// Every mbarrier wait is bounded (2 s of global time); a wait that gives up
+// raises the device error word and makes every role of the CTA stop, drain its
+// copies and MMAs, free TMEM and exit.
+#include <math.h>
+
+#include "svx_internal.h"
+
+namespace svx {
+namespace {
+
+constexpr int TOK = kTcTile;  // tokens per tile
+constexpr int D = 128;
+constexpr int NUM_THREADS = 192;
+constexpr int TILE_BYTES = TOK * D * 2;  // one K or V tile, 32 KiB
+constexpr int HALF_BYTES = TOK * 64 * 2; // 64 of the 128 dimensions of a tile, 16 KiB
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+template <int NCOL>
+struct TcCfg {
+  static constexpr int STAGES = (NCOL == 32) ? 3 : 2;
+  static constexpr int Q_BYTES = NCOL * D * 2;
+  static constexpr int P_BYTES = NCOL * TOK * 2;
+  static constexpr int OFF_KV = 0;
+  static constexpr int OFF_Q = STAGES * 2 * TILE_BYTES;
+  static constexpr int OFF_P = OFF_Q + Q_BYTES;
+  static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;    // float [4][NCOL]
+  static constexpr int OFF_MNEW = OFF_RED + 4 * NCOL * 4;  // float [NCOL]
+  static constexpr int OFF_ALPHA = OFF_MNEW + NCOL * 4;  // float [2][NCOL]
+  static constexpr int OFF_FIN = OFF_ALPHA + 2 * NCOL * 4;  // float [2][NCOL]: final m, l
+  static constexpr int N_BAR = 2 * STAGES + 10 + 2;
+  static constexpr int OFF_BAR = OFF_FIN + 2 * NCOL * 4;
+  static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;  // [0] TMEM base, [1] abort flag
+  static constexpr int BYTES = OFF_MISC + 16;
+  static constexpr int SMEM = BYTES + 1024;  // slack to align the base to 1024 bytes
+  static constexpr uint32_t TMEM_COLS = (4 * NCOL <= 128) ? 128u : 256u;
+  static constexpr uint32_t S_COL = 0;         // S^T buffers at columns [0, 2*NCOL)
+  static constexpr uint32_t O_COL = 2 * NCOL;  // O^T buffers at [2*NCOL, 4*NCOL)
+  static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0 && P_BYTES % 1024 == 0, "swizzle atoms need 1 KiB alignment");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier among the 128 softmax threads that also ANDs their flags, so a wait
+// that gave up in one thread makes all of them leave together.
+__device__ __forceinline__ bool softmax_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(ok))
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void st_shared_b16(uint32_t addr, unsigned short v) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes into v[OFF..OFF+31]
+// (thread = lane); the wait is in the same statement so no value is used early.
+template <int OFF, int N>
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[N]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[OFF + i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4)                                   // D format: f32
+         | (1u << 7)                                 // A format: bf16
+         | (1u << 10)                                // B format: bf16
+         | ((a_mn_major ? 1u : 0u) << 15)            // A major-ness
+         | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (atoms of 8 rows x 128 B).
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version of the tcgen05 family
+  d |= static_cast<uint64_t>(2) << 61;  // swizzle: 128 bytes
+  return d;
+}
+
+// Byte offset of 16-byte piece `chunk` (0..15 along the 128 dimensions) of row
+// `row` in a K-major, 128-byte-swizzled [rows][128] bf16 tile: two atoms
+// columns of 64 dimensions, `half_bytes` apart.
+__device__ __forceinline__ uint32_t swz_offset(int row, int chunk, uint32_t half_bytes) {
+  return static_cast<uint32_t>(chunk >> 3) * half_bytes + static_cast<uint32_t>(row) * 128u +
+         (static_cast<uint32_t>((chunk & 7) ^ (row & 7)) << 4);
+}
+
+// Butterfly transpose-reduction: on return, lane L holds the reduction over the
+// warp's 32 lanes of column OFF + L (31 shuffles instead of 32 x 5).
+template <int OFF, int N, bool MAX>
+__device__ __forceinline__ float xpose_reduce(const float (&v)[N], int lane) {
+  float w[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) w[j] = v[OFF + j];
+#pragma unroll
+  for (int step = 16; step >= 1; step >>= 1) {
+    const bool up = (lane & step) != 0;
+#pragma unroll
+    for (int j = 0; j < step; ++j) {
+      const float send = up ? w[j] : w[j + step];
+      const float keep = up ? w[j + step] : w[j];
+      const float got = __shfl_xor_sync(0xffffffffu, send, step);
+      w[j] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  return w[0];
+}
+
+struct Seg {
+  int part, g, rb, slot;
+  int64_t tile0;   // first tile of the segment within its part
+  int64_t n_tiles;
+};
+
+// The segment of this CTA that starts at global tile x: it runs to the end of
+// its (part, head, row block) pair or to the end of the CTA's range.
+__device__ __forceinline__ Seg seg_at(const ChunkParams& P, int64_t x, int64_t x_end, int& hint) {
+  int i = hint;
+  while (i + 1 < P.n_parts && P.parts[i + 1].tile_base <= x) ++i;
+  hint = i;
+  const int64_t nt = (static_cast<int64_t>(P.parts[i].n_tok) + TOK - 1) / TOK;
+  const int64_t local = x - P.parts[i].tile_base;
+  const int64_t pair = local / nt;
+  Seg s;
+  s.part = i;
+  s.g = static_cast<int>(pair / P.n_rowblk);
+  s.rb = static_cast<int>(pair % P.n_rowblk);
+  s.tile0 = local % nt;
+  const int64_t first = P.parts[i].tile_base + pair * nt;
+  s.n_tiles = min(x_end, first + nt) - x;
+  s.slot = static_cast<int>(static_cast<int64_t>(blockIdx.x) - cta_of_tile(first, gridDim.x, P.total_tiles));
+  return s;
+}
+
+struct Waiter {
+  volatile uint32_t* abort;
+  int* err;
+  // Bounded wait that ignores the abort flag (draining in-flight MMAs).
+  __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+      if (global_ns() - t0 > kWaitLimitNs) {
+        atomicOr(err, 1);
+        return;
+      }
+  }
+  // Bounded wait on an mbarrier phase; false if the CTA is aborting.
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((it & 255u) == 0) {
+        if (*abort) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+          *abort = 1u;
+          atomicOr(err, 1);
+          return false;
+        }
+      }
+    }
+  }
+};
+
+template <int NCOL>
+__global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_constant__ ChunkParams P) {
+  using C = TcCfg<NCOL>;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const uint32_t bar0 = base + C::OFF_BAR;
+  const uint32_t FULL = bar0, EMPTY = bar0 + 8u * C::STAGES;
+  const uint32_t SFULL = bar0 + 16u * C::STAGES, SEMPTY = SFULL + 16u, PFULL = SEMPTY + 16u, OFULL = PFULL + 16u,
+                 OEMPTY = OFULL + 16u, QFULL = OEMPTY + 16u, DRAIN = QFULL + 8u;
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_MISC);
+  float* red = reinterpret_cast<float*>(gbase + C::OFF_RED);
+  float* mnew = reinterpret_cast<float*>(gbase + C::OFF_MNEW);
+  float* alpha = reinterpret_cast<float*>(gbase + C::OFF_ALPHA);
+  float* fin = reinterpret_cast<float*>(gbase + C::OFF_FIN);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(FULL + 8u * s, 32);
+      mbar_init(EMPTY + 8u * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(SFULL + 8u * b, 1);
+      mbar_init(SEMPTY + 8u * b, 128);
+      mbar_init(PFULL + 8u * b, 128);
+      mbar_init(OFULL + 8u * b, 1);
+      mbar_init(OEMPTY + 8u * b, 128);
+    }
+    mbar_init(QFULL, 128);
+    mbar_init(DRAIN, 1);
+    misc[1] = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async();
+  }
+  if (warp == 0) tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  Waiter W{misc + 1, P.err};
+
+  const int64_t T = P.total_tiles;
+  const int64_t x_begin = cta_tile_begin(blockIdx.x, gridDim.x, T);
+  const int64_t x_end = cta_tile_begin(blockIdx.x + 1, gridDim.x, T);
+  const int64_t kv_stride = static_cast<int64_t>(P.n_kv_heads) * D;
+
+  if (warp == 4) {
+    // ---------------- producer: K/V tiles into the stage ring
+    int hint = 0;
+    int64_t i = 0;
+    bool ok = true;
+    for (int64_t x = x_begin; x < x_end && ok;) {
+      const Seg sg = seg_at(P, x, x_end, hint);
+      const PartDesc& pd = P.parts[sg.part];
+      const int64_t n_tok = pd.n_tok;
+      const __nv_bfloat16* kb = pd.k + static_cast<int64_t>(sg.g) * D;
+      const __nv_bfloat16* vb = pd.v + static_cast<int64_t>(sg.g) * D;
+      for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
+        const int stage = static_cast<int>(i % C::STAGES);
+        const uint32_t use = static_cast<uint32_t>(i / C::STAGES);
+        if (i >= C::STAGES && !W.wait(EMPTY + 8u * stage, (use - 1u) & 1u)) {
+          ok = false;
+          break;
+        }
+        const int64_t tok0 = (sg.tile0 + t) * TOK;
+        const uint32_t kdst = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES;
+        const uint32_t vdst = kdst + TILE_BYTES;
+#pragma unroll 8
+        for (int j = 0; j < 64; ++j) {
+          const int piece = lane + 32 * j;  // 16 pieces of 16 bytes per token row
+          const int row = piece >> 4, c = piece & 15;
+          const int64_t tok = tok0 + row;
+          const bool in = tok < n_tok;
+          const int64_t off = in ? tok * kv_stride + c * 8 : 0;
+          const uint32_t so = swz_offset(row, c, HALF_BYTES);
+          cp_async16(kdst + so, kb + off, in ? 16 : 0);
+          cp_async16(vdst + so, vb + off, in ? 16 : 0);
+        }
+        cp_async_arrive_noinc(FULL + 8u * stage);
+      }
+      x += sg.n_tiles;
+    }
+    cp_async_wait_all();
+  } else if (warp == 5) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc(128, NCOL, false, false);
+      constexpr uint32_t idesc_o = make_idesc(128, NCOL, true, false);
+      auto issue_s = [&](int64_t j) -> bool {
+        const int stage = static_cast<int>(j % C::STAGES);
+        const uint32_t use = static_cast<uint32_t>(j / C::STAGES);
+        if (!W.wait(FULL + 8u * stage, use & 1u)) return false;
+        if (j >= 2 && !W.wait(SEMPTY + 8u * (j & 1), ((static_cast<uint32_t>(j >> 1)) & 1u) ^ 1u)) return false;
+        fence_proxy_async();  // cp.async writes (generic proxy) before tensor-core reads (async proxy)
+        tc_fence_after();
+        const uint32_t kaddr = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES;
+        const uint32_t qaddr = base + C::OFF_Q;
+        const uint32_t d = tmem + C::S_COL + static_cast<uint32_t>(j & 1) * NCOL;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = make_sdesc(kaddr + (kk >> 2) * HALF_BYTES + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = make_sdesc(qaddr + (kk >> 2) * (NCOL * 128) + (kk & 3) * 32, 16, 1024);
+          mma_bf16(d, a, b, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(SFULL + 8u * (j & 1));
+        return true;
+      };
+      int hint = 0;
+      int64_t i = 0;
+      uint32_t seg_idx = 0;
+      bool ok = true;
+      for (int64_t x = x_begin; x < x_end && ok; ++seg_idx) {
+        const Seg sg = seg_at(P, x, x_end, hint);
+        if (!W.wait(QFULL, seg_idx & 1u)) break;
+        tc_fence_after();
+        if (!issue_s(i)) break;
+        for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
+          if (t + 1 < sg.n_tiles && !issue_s(i + 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t par = static_cast<uint32_t>(i >> 1) & 1u;
+          if (!W.wait(PFULL + 8u * (i & 1), par)) {
+            ok = false;
+            break;
+          }
+          if (i >= 2 && !W.wait(OEMPTY + 8u * (i & 1), par ^ 1u)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async();  // P^T was written with ordinary stores
+          tc_fence_after();
+          const int stage = static_cast<int>(i % C::STAGES);
+          const uint32_t vaddr = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES + TILE_BYTES;
+          const uint32_t paddr = base + C::OFF_P + static_cast<uint32_t>(i & 1) * C::P_BYTES;
+          const uint32_t d = tmem + C::O_COL + static_cast<uint32_t>(i & 1) * NCOL;
+#pragma unroll
+          for (int kk = 0; kk < TOK / 16; ++kk) {
+            // A = V^T: dimension-major (MN-major); 64-dimension halves 16 KiB apart, 8-token groups 1 KiB apart
+            const uint64_t a = make_sdesc(vaddr + kk * 2048, HALF_BYTES, 1024);
+            const uint64_t b = make_sdesc(paddr + (kk >> 2) * (NCOL * 128) + (kk & 3) * 32, 16, 1024);
+            mma_bf16(d, a, b, idesc_o, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(OFULL + 8u * (i & 1));
+          mma_commit(EMPTY + 8u * stage);
+        }
+        x += sg.n_tiles;
+      }
+      // drain: every MMA issued by this thread has completed before TMEM is freed
+      mma_commit(DRAIN);
+      W.drain(DRAIN, 0u);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- softmax and accumulation (warps 0-3)
+    const int tid = threadIdx.x;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    constexpr int NH = NCOL / 32;  // columns per lane after a transpose-reduction
+    float acc[NCOL];
+    float s[NCOL];
+    float m_run[NH], l_w[NH];
+    int hint = 0;
+    int64_t i = 0;
+    bool ok = true;
+
+    auto accumulate = [&](int64_t j) -> bool {
+      if (!softmax_all(W.wait(OFULL + 8u * (j & 1), static_cast<uint32_t>(j >> 1) & 1u))) return false;
+      tc_fence_after();
+      const uint32_t ta = tmem + lane_base + C::O_COL + static_cast<uint32_t>(j & 1) * NCOL;
+      tmem_ld32<0>(ta, s);
+      if constexpr (NCOL == 64) tmem_ld32<32>(ta + 32, s);
+      tc_fence_before();
+      mbar_arrive(OEMPTY + 8u * (j & 1));
+      const float4* al4 = reinterpret_cast<const float4*>(alpha + (j & 1) * NCOL);
+#pragma unroll
+      for (int c4 = 0; c4 < NCOL / 4; ++c4) {
+        const float4 a = al4[c4];
+        acc[4 * c4 + 0] = fmaf(acc[4 * c4 + 0], a.x, s[4 * c4 + 0]);
+        acc[4 * c4 + 1] = fmaf(acc[4 * c4 + 1], a.y, s[4 * c4 + 1]);
+        acc[4 * c4 + 2] = fmaf(acc[4 * c4 + 2], a.z, s[4 * c4 + 2]);
+        acc[4 * c4 + 3] = fmaf(acc[4 * c4 + 3], a.w, s[4 * c4 + 3]);
+      }
+      return true;
+    };
+
+    for (int64_t x = x_begin; x < x_end && ok;) {
+      const Seg sg = seg_at(P, x, x_end, hint);
+      const PartDesc& pd = P.parts[sg.part];
+      const int b = pd.req;
+      const int R = P.group * P.n_query;
+      const int r0 = sg.rb * NCOL;
+      const int nr = min(NCOL, R - r0);
+      const int64_t row_base =
+          (static_cast<int64_t>(b) * P.n_q_heads + static_cast<int64_t>(sg.g) * P.group) * P.n_query + r0;
+
+      // Q rows of the pair into shared memory (K-major, swizzled); padding rows are zero
+      for (int idx = tid; idx < NCOL * 16; idx += 128) {
+        const int c = idx >> 4, ch = idx & 15;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (c < nr) v = *reinterpret_cast<const uint4*>(P.q + (row_base + c) * D + ch * 8);
+        st_shared_v4(base + C::OFF_Q + swz_offset(c, ch, NCOL * 128), v);
+      }
+      fence_proxy_async();
+      mbar_arrive(QFULL);
+
+#pragma unroll
+      for (int c = 0; c < NCOL; ++c) acc[c] = 0.f;
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        m_run[h] = -INFINITY;
+        l_w[h] = 0.f;
+      }
+
+      for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
+        const bool tok_valid = (sg.tile0 + t) * TOK + tid < pd.n_tok;
+        if (!softmax_all(W.wait(SFULL + 8u * (i & 1), static_cast<uint32_t>(i >> 1) & 1u))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ta = tmem + lane_base + C::S_COL + static_cast<uint32_t>(i & 1) * NCOL;
+        tmem_ld32<0>(ta, s);
+        if constexpr (NCOL == 64) tmem_ld32<32>(ta + 32, s);
+        tc_fence_before();
+        mbar_arrive(SEMPTY + 8u * (i & 1));
+#pragma unroll
+        for (int c = 0; c < NCOL; ++c) s[c] = tok_valid ? s[c] * P.q_scale : -INFINITY;
+
+        // tile maximum per row: warp-level transpose-reduction, then across the 4 warps
+        red[warp * NCOL + lane] = xpose_reduce<0, NCOL, true>(s, lane);
+        if constexpr (NCOL == 64) red[warp * NCOL + 32 + lane] = xpose_reduce<32, NCOL, true>(s, lane);
+        named_sync_softmax();
+        if (warp == 0) {
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const int c = lane + 32 * h;
+            const float tm = fmaxf(fmaxf(red[c], red[NCOL + c]), fmaxf(red[2 * NCOL + c], red[3 * NCOL + c]));
+            const float mn = fmaxf(m_run[h], tm);
+            alpha[(i & 1) * NCOL + c] = (m_run[h] == -INFINITY) ? 0.f : exp2_approx(m_run[h] - mn);
+            mnew[c] = mn;
+            m_run[h] = mn;
+          }
+        }
+        named_sync_softmax();
+
+        // P^T = 2^(s - m_new), bf16, into the K-major swizzled B operand of the PV product
+        const uint32_t pbase = base + C::OFF_P + static_cast<uint32_t>(i & 1) * C::P_BYTES +
+                               static_cast<uint32_t>(tid >> 6) * (NCOL * 128) + static_cast<uint32_t>((tid & 7) << 1);
+        const float4* mn4 = reinterpret_cast<const float4*>(mnew);
+#pragma unroll
+        for (int c4 = 0; c4 < NCOL / 4; ++c4) {
+          const float4 mm = mn4[c4];
+          s[4 * c4 + 0] = exp2_approx(s[4 * c4 + 0] - mm.x);
+          s[4 * c4 + 1] = exp2_approx(s[4 * c4 + 1] - mm.y);
+          s[4 * c4 + 2] = exp2_approx(s[4 * c4 + 2] - mm.z);
+          s[4 * c4 + 3] = exp2_approx(s[4 * c4 + 3] - mm.w);
+        }
+#pragma unroll
+        for (int c = 0; c < NCOL; ++c) {
+          const uint32_t off = static_cast<uint32_t>(c) * 128u +
+                               (static_cast<uint32_t>(((tid & 63) >> 3) ^ (c & 7)) << 4);
+          st_shared_b16(pbase + off, __bfloat16_as_ushort(__float2bfloat16_rn(s[c])));
+        }
+        fence_proxy_async();
+        mbar_arrive(PFULL + 8u * (i & 1));
+
+        // per-warp running denominators (lane = row), rescaled like the value sum
+        {
+          const float ts0 = xpose_reduce<0, NCOL, false>(s, lane);
+          l_w[0] = l_w[0] * alpha[(i & 1) * NCOL + lane] + ts0;
+          if constexpr (NCOL == 64) {
+            const float ts1 = xpose_reduce<32, NCOL, false>(s, lane);
+            l_w[NH - 1] = l_w[NH - 1] * alpha[(i & 1) * NCOL + 32 + lane] + ts1;
+          }
+        }
+        if (t > 0 && !accumulate(i - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok || !accumulate(i - 1)) break;
+
+      // segment state: m (warp 0 lanes), l (sum of the per-warp partials), a = acc
+#pragma unroll
+      for (int h = 0; h < NH; ++h) red[warp * NCOL + 32 * h + lane] = l_w[h];
+      named_sync_softmax();
+      if (warp == 0) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const int c = lane + 32 * h;
+          fin[c] = m_run[h];
+          fin[NCOL + c] = red[c] + red[NCOL + c] + red[2 * NCOL + c] + red[3 * NCOL + c];
+        }
+      }
+      named_sync_softmax();
+      const int64_t srow0 = static_cast<int64_t>(P.slot_base + sg.slot) * P.slot_stride + row_base;
+#pragma unroll
+      for (int c = 0; c < NCOL; ++c) {
+        if (c < nr) {
+          const RowState old = P.ws_h[srow0 + c];
+          const float m = fin[c];
+          float a = acc[c];
+          float* ap = P.ws_a + (srow0 + c) * D + tid;
+          if (old.epoch == P.epoch) {
+            const float mn = fmaxf(old.m, m);
+            if (mn != -INFINITY) a = *ap * exp2_approx(old.m - mn) + a * exp2_approx(m - mn);
+          }
+          *ap = a;
+        }
+      }
+      named_sync_softmax();  // every thread has read the old headers
+      if (tid < nr) {
+        RowState* hp = P.ws_h + srow0 + tid;
+        const RowState old = *hp;
+        float m = fin[tid], l = fin[NCOL + tid];
+        if (old.epoch == P.epoch) {
+          const float mn = fmaxf(old.m, m);
+          if (mn != -INFINITY) {
+            l = old.l * exp2_approx(old.m - mn) + l * exp2_approx(m - mn);
+            m = mn;
+          }
+        }
+        *hp = RowState{m, l, P.epoch, 0u};
+      }
+      x += sg.n_tiles;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int NCOL>
+cudaError_t launch_tc(const ChunkParams& p, int n_ctas, cudaStream_t stream) {
+  using C = TcCfg<NCOL>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(chunk_attn_tc<NCOL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  chunk_attn_tc<NCOL><<<n_ctas, NUM_THREADS, C::SMEM, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(int head_dim, int rows) { return head_dim == 128 && rows >= 1; }
+int tc_ncol(int rows) { return rows <= 32 ? 32 : 64; }
+int tc_max_ctas(int num_sms) { return num_sms; }  // one CTA per SM (shared memory)
+
+cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int ncol, int n_ctas, cudaStream_t stream) {
+  if (n_ctas < 1) return cudaSuccess;
+  if (ncol == 32) return launch_tc<32>(p, n_ctas, stream);
+  if (ncol == 64) return launch_tc<64>(p, n_ctas, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace svx

@@ -19,6 +19,7 @@ OK, ERR_INVALID_ARG, ERR_BAD_STATE, ERR_OOM, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPOR
 STATUS_NAMES = {0: "SVX_OK", 1: "SVX_ERR_INVALID_ARG", 2: "SVX_ERR_BAD_STATE", 3: "SVX_ERR_OOM",
                 4: "SVX_ERR_CUDA", 5: "SVX_ERR_TIMEOUT", 6: "SVX_ERR_UNSUPPORTED"}
 FLAG_TIMING = 1
+FLAG_NO_TENSOR_CORES = 2
 
 
 class SvxError(RuntimeError):
@@ -162,10 +163,11 @@ class Verifier:
 
     def __init__(self, max_req: int, n_q_heads: int, n_kv_heads: int, head_dim: int, max_query: int,
                  max_chunk_tokens: int, n_slots: int = 2, device: int = 0, compute_stream=None, copy_stream=None,
-                 timing: bool = False):
+                 timing: bool = False, tensor_cores: bool = True):
         self._keep = (compute_stream, copy_stream)
+        flags = (FLAG_TIMING if timing else 0) | (0 if tensor_cores else FLAG_NO_TENSOR_CORES)
         cfg = Config(max_req, n_q_heads, n_kv_heads, head_dim, max_query, max_chunk_tokens, n_slots, device,
-                     _stream_handle(compute_stream), _stream_handle(copy_stream), FLAG_TIMING if timing else 0)
+                     _stream_handle(compute_stream), _stream_handle(copy_stream), flags)
         h = ctypes.c_void_p(None)
         st = lib.svx_create(ctypes.byref(cfg), ctypes.byref(h))
         if st != OK:

@@ -44,8 +44,19 @@ SMALL = [
 
 @pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
 @pytest.mark.parametrize("resident", [False, True], ids=["streamed", "resident"])
-def test_small_parity(svx, w, resident):
+@pytest.mark.parametrize("tc", [True, False], ids=["tc", "fma"])
+def test_small_parity(svx, w, resident, tc):
     x, t = gpu_inputs(w, resident=resident)
+    with make_verifier(svx, w, tensor_cores=tc) as v:
+        o, l = run_gpu(v, w, t, x)
+    check_parity(o, l, *oracle_out(w, x))
+
+
+@pytest.mark.parametrize("hist", [(1,), (127,), (128,), (129,), (4095, 1, 300), (20000, 7000)])
+def test_tile_edges_tensor_core_path(svx, hist):
+    """Token counts around the 128-token tile and a stream-K split of unequal parts."""
+    w = W.Workload("edge", len(hist), 32, 8, 128, hist, 4096, 5, seed=30 + len(hist))
+    x, t = gpu_inputs(w, resident=True)
     with make_verifier(svx, w) as v:
         o, l = run_gpu(v, w, t, x)
     check_parity(o, l, *oracle_out(w, x))
