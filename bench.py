@@ -438,7 +438,8 @@ def main(argv=None):
                 "d2h_bytes_per_step": int(d2h_step), "ms_per_step": ms_e2e_job},
         "gpu_launches": launches_per_step * a.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None, "kernel": "chunk_attn",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "kernel": "chunk_attn_tc" if (d == 128) else "chunk_attn_fma",
                      "peak_source": f"{hbm_src} hbm_gbs (burst copy)",
                      "algorithmic_bytes_per_launch": int(k1_bytes_per_launch),
                      "ms_per_launch": k1_ms_per_launch},
