@@ -129,7 +129,7 @@ svx_status svx_candidate_attn(svx_ctx ctx, const void* k_dev, const void* v_dev,
 svx_status svx_round_finish(svx_ctx ctx, void* o_dev, float* lse_dev, int32_t timeout_ms);
 
 /* Message for the last failing call on ctx (never NULL; "" if none).  NULL ctx: last failure of
- * svx_create on this thread. */
+ * svx_create or svx_verify_static on this thread. */
 const char* svx_last_error(svx_ctx ctx);
 
 /* Per-round timing (needs SVX_FLAG_TIMING).  Waits for the last finished round to complete. */
@@ -173,6 +173,42 @@ svx_status svx_candidate_masks(int32_t n_req, int32_t n_query, const int32_t* pa
  * given as int64[n_parts][3] tile every [0, hist_len[b]) exactly once, else 0. */
 svx_status svx_check_coverage(int32_t n_req, const int64_t* hist_len, const int64_t* parts, int64_t n_parts,
                               int32_t* ok_out);
+
+/* ---- a round that allocates nothing ------------------------------------------------------ */
+
+/* Size of the library's static device scratch array (per GPU, held until the process exits). */
+#define SVX_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* One whole verification round over device-resident KV without allocating any memory.  The paper
+ * has no counterpart to this call: it exists for callers that cannot call cudaMalloc while they
+ * run - an engine whose memory manager owns all device memory after start-up, or a decode loop
+ * that cannot accept an allocation's cost or implicit synchronisation.  The fp32 (m, l, a)
+ * state, the candidate visibility words and an error word live in a static __device__ array of
+ * SVX_STATIC_SCRATCH_BYTES that every GPU loading the library holds; the caller passes all
+ * inputs and outputs.
+ *
+ * Computes what svx_round_begin + one in-place part per request + svx_candidate_attn +
+ * svx_round_finish compute, on `stream` (cudaStream_t, NULL = default stream) of the calling
+ * thread's current device, and returns once the work is enqueued.
+ *   q_dev            bf16 [n_req][n_q_heads][n_query][head_dim]
+ *   hist_len_host    int64[n_req], 0 <= C_b < 2^31
+ *   k/v_hist_dev     host arrays of n_req device pointers, bf16 [C_b][n_kv_heads][head_dim]
+ *                    (entries for C_b = 0 are ignored)
+ *   k/v_cand_dev     bf16 [n_req][n_query][n_kv_heads][head_dim], or both NULL (no candidates)
+ *   parent_host      NULL (causal chain) or int32[n_req][n_query] token-tree parents
+ *   scale            0 means 1/sqrt(head_dim)
+ *   o_dev, lse_dev   bf16 [n_req][n_q_heads][n_query][head_dim], fp32 [n_req][n_q_heads][n_query]
+ * Rounds whose state does not fit (about 3,500 query rows at head_dim 128) return
+ * SVX_ERR_INVALID_ARG and enqueue nothing.  The first call on a device sets up the scratch
+ * (cudaGetSymbolAddress and a zeroing cudaMemset, synchronous); make that first call before any
+ * stream capture.  All calls share the one array: calls whose GPU work overlaps (different
+ * streams, or several host threads) race and give wrong results - order them on one stream.
+ * Errors: SVX_ERR_INVALID_ARG, _UNSUPPORTED, _CUDA; message from svx_last_error(NULL). */
+svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                             int32_t n_query, const void* q_dev, const int64_t* hist_len_host,
+                             const void* const* k_hist_dev, const void* const* v_hist_dev,
+                             const void* k_cand_dev, const void* v_cand_dev, const int32_t* parent_host,
+                             float scale, void* o_dev, float* lse_dev, void* stream);
 
 /* Library version string. */
 const char* svx_version(void);

@@ -39,6 +39,11 @@ struct PushEvents {
 
 }  // namespace
 
+namespace svx {
+// Message returned by svx_last_error(NULL) on this thread.
+void set_thread_error(const char* msg) { g_create_error = msg; }
+}  // namespace svx
+
 struct svx_ctx_s {
   svx_config cfg{};
   int group = 1;

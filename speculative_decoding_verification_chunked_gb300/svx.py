@@ -74,6 +74,10 @@ _SIGS = {
     "svx_check_coverage": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_int64),
                                           ctypes.POINTER(ctypes.c_int64), ctypes.c_int64,
                                           ctypes.POINTER(ctypes.c_int32)]),
+    "svx_verify_static": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, _P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(_P),
+                                         ctypes.POINTER(_P), _P, _P, ctypes.POINTER(ctypes.c_int32), ctypes.c_float,
+                                         _P, _P, _P]),
     "svx_version": (ctypes.c_char_p, []),
 }
 
@@ -140,6 +144,39 @@ def check_coverage(hist_len: Sequence[int], parts: Sequence[tuple]) -> bool:
     if st != OK:
         raise SvxError(st, "svx_check_coverage: invalid arguments")
     return bool(ok.value)
+
+
+# ------------------------------------------------------------ a round that allocates nothing
+
+
+STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def verify_static(q, hist_len: Sequence[int], hist_k: Sequence, hist_v: Sequence, o, lse, cand_k=None, cand_v=None,
+                  parent: Optional[np.ndarray] = None, scale: float = 0.0, stream=None,
+                  n_kv_heads: Optional[int] = None):
+    """svx_verify_static: a whole round over device-resident KV using the library's static device
+    scratch instead of any allocation (for callers that cannot call cudaMalloc).
+
+    q: device bf16 [B][Hq][nq][d]; hist_k[b], hist_v[b]: device bf16 [C_b][Hkv][d] (or None when
+    C_b = 0); cand_k, cand_v: device bf16 [B][nq][Hkv][d] or None; o, lse: device outputs.
+    """
+    B, Hq, nq, d = (int(x) for x in q.shape)
+    if n_kv_heads is None:
+        src = next((k for k in hist_k if k is not None), cand_k)
+        n_kv_heads = int(src.shape[-2])
+    h, hp = _i64(hist_len)
+    ks = (_P * B)(*[None if k is None else _ptr(k) for k in hist_k])
+    vs = (_P * B)(*[None if v is None else _ptr(v) for v in hist_v])
+    par = None
+    if parent is not None:
+        parent = np.ascontiguousarray(np.asarray(parent, dtype=np.int32))
+        par = parent.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    st = lib.svx_verify_static(B, Hq, n_kv_heads, d, nq, _ptr(q), hp, ks, vs,
+                               None if cand_k is None else _ptr(cand_k), None if cand_v is None else _ptr(cand_v),
+                               par, ctypes.c_float(scale), _ptr(o), _ptr(lse), _stream_handle(stream))
+    if st != OK:
+        raise SvxError(st, lib.svx_last_error(None).decode())
 
 
 # ------------------------------------------------------------ the round
