@@ -60,6 +60,8 @@ typedef struct svx_ctx_s* svx_ctx;
 /* svx_config.flags */
 #define SVX_FLAG_TIMING 1u           /* record CUDA events around copies and kernels (svx_round_stats) */
 #define SVX_FLAG_NO_TENSOR_CORES 2u  /* run the history chunk kernel on FP32 FMA even where d = 128 */
+#define SVX_FLAG_ZERO_COPY 4u        /* read pinned host parts in place over the host link (no staging copy);
+                                        the chunk kernel then runs at link speed on zero_copy_ctas SMs */
 
 /* Context configuration.  Shapes are fixed for the context's lifetime (the
  * Cohort compatibility rule of section 4.2: one layer shape, verification
@@ -76,11 +78,14 @@ typedef struct {
   void* compute_stream;     /* cudaStream_t for kernels; NULL: library creates one (highest priority) */
   void* copy_stream;        /* cudaStream_t for H2D chunk copies; NULL: library creates one */
   uint32_t flags;           /* SVX_FLAG_* */
+  int32_t zero_copy_ctas;   /* with SVX_FLAG_ZERO_COPY: CTAs (one per SM) of a launch that reads host
+                               parts; 0 = all SMs.  Fewer leave SMs free for co-running work. */
 } svx_config;
 
 /* One request's contiguous slice of committed history, [tok_start, tok_start + n_tok).
  * k, v: bf16 [n_tok][Hkv][d], 16-byte aligned.  Pinned host memory (cudaHostAlloc or
- * cudaHostRegister) is staged through a slot by the copy engine (n_tok <= max_chunk_tokens);
+ * cudaHostRegister) is staged through a slot by the copy engine (n_tok <= max_chunk_tokens), or,
+ * with SVX_FLAG_ZERO_COPY, read in place by the chunk kernel over the host link (any n_tok);
  * device memory is read in place (any n_tok).  Pageable host memory is rejected. */
 typedef struct {
   int32_t req;
@@ -111,15 +116,19 @@ svx_status svx_round_begin(svx_ctx ctx, int32_t n_req, int32_t n_query, const vo
  * depend on chunk order, Eq. 9); svx_round_finish checks that they tile each [0, C_b) exactly once. */
 svx_status svx_push_chunk(svx_ctx ctx, const svx_part* parts, int32_t n_parts);
 
-/* Attention over the GPU-resident candidate region (section 4.2, the causal mask by absolute
- * position).  k_dev, v_dev: device bf16 [n_req][n_cand][Hkv][d] with n_cand == n_query.
- * parent_host: NULL for the causal chain (query j sees candidates 0..j), else host
- * int32[n_req][n_cand] token-tree parents with parent[0] = -1 and 0 <= parent[i] < i
- * (query j sees j and its ancestors).  At most once per round, in any order with the pushes. */
+/* The GPU-resident candidate region of the round (section 4.2, the causal mask by absolute
+ * position).  k_dev, v_dev: device bf16 [n_req][n_cand][Hkv][d] with n_cand == n_query; they must
+ * stay valid until the round's finish work has run.  parent_host: NULL for the causal chain
+ * (query j sees candidates 0..j), else host int32[n_req][n_cand] token-tree parents with
+ * parent[0] = -1 and 0 <= parent[i] < i (query j sees j and its ancestors); copied by this call.
+ * The attention over the region is computed by svx_round_finish's kernel (one launch fewer per
+ * round), so this call only validates and records.  At most once per round, in any order with
+ * the pushes. */
 svx_status svx_candidate_attn(svx_ctx ctx, const void* k_dev, const void* v_dev, int32_t n_cand,
                               const int32_t* parent_host);
 
-/* Ends the round: checks chunk coverage, merges the split states (Eq. 8) and writes
+/* Ends the round: checks chunk coverage, attends over the candidate region if one was given,
+ * merges it with the history states (Eq. 8) and writes
  * O = a / l (Eq. 9) as bf16 [n_req][Hq][n_query][d] and LSE = m + ln l as fp32
  * [n_req][Hq][n_query] (natural log of the softmax denominator of the scaled scores) to device
  * memory.  A query with no visible key gets O = 0 and LSE = -inf.  timeout_ms = 0 returns
@@ -136,13 +145,16 @@ const char* svx_last_error(svx_ctx ctx);
 typedef struct {
   double round_ms;        /* first event of the round to the end of its finish kernel */
   double copy_busy_ms;    /* sum over pushes of H2D copy time on the copy stream */
-  double chunk_kernel_ms; /* sum over pushes of chunk-kernel time on the compute stream */
-  double cand_kernel_ms;  /* candidate-region kernel */
-  double finish_kernel_ms;
+  double chunk_kernel_ms; /* sum over pushes of chunk-kernel time on the compute stream (from the
+                             moment its staging slot is ready) */
+  double cand_kernel_ms;  /* always 0: the candidate region runs inside the finish kernel */
+  double finish_kernel_ms; /* candidate region + merge + finalize */
   int64_t h2d_bytes;      /* history bytes copied from host this round */
   int64_t device_bytes;   /* history bytes read in place from device memory this round */
   int32_t n_chunk_launches;
   int32_t n_copies;
+  double chunk_kernel_exposed_ms; /* chunk-kernel time outside every H2D copy interval of the round;
+                                     1 - exposed / chunk_kernel_ms is the compute hidden under transfer */
 } svx_stats;
 svx_status svx_round_stats(svx_ctx ctx, svx_stats* out);
 
@@ -183,7 +195,7 @@ svx_status svx_check_coverage(int32_t n_req, const int64_t* hist_len, const int6
  * has no counterpart to this call: it exists for callers that cannot call cudaMalloc while they
  * run - an engine whose memory manager owns all device memory after start-up, or a decode loop
  * that cannot accept an allocation's cost or implicit synchronisation.  The fp32 (m, l, a)
- * state, the candidate visibility words and an error word live in a static __device__ array of
+ * state and an error word live in a static __device__ array of
  * SVX_STATIC_SCRATCH_BYTES that every GPU loading the library holds; the caller passes all
  * inputs and outputs.
  *
@@ -209,6 +221,51 @@ svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_t n_kv_head
                              const void* const* k_hist_dev, const void* const* v_hist_dev,
                              const void* k_cand_dev, const void* v_cand_dev, const int32_t* parent_host,
                              float scale, void* o_dev, float* lse_dev, void* stream);
+
+/* ---- commit-aware KV tiering (host side of the history that the rounds stream) ------------- */
+
+/* One request's Target KV regions (section 4.1, Eq. 4): Sealed History [0, H) in host memory,
+ * Active Tail [H, C) and Speculative Frontier [C, L) on the GPU, 0 <= H <= C <= L.  Zero-initialise
+ * with pending = -1.  `event` is owned by the library while a migration is in flight. */
+typedef struct {
+  int64_t H;        /* history confirmed in host memory */
+  int64_t C;        /* committed prefix C_r */
+  int64_t L;        /* logical length L_r, committed plus candidates */
+  int64_t pending;  /* endpoint E of the migration in flight, or -1 */
+  void* event;      /* CUDA event of that migration (library-owned), or NULL */
+} svx_tier_state;
+
+/* Eq. (5): E = max{H, g * floor(max(0, C - T) / g)}; T = Active Tail target, g = migration
+ * granularity.  Needs g >= 1, T >= 0, 0 <= H <= C and H a multiple of g.  Host-only. */
+svx_status svx_migration_endpoint(int64_t H, int64_t C, int64_t T, int64_t g, int64_t* E_out);
+
+/* A new round: committed prefix C (never shrinks) and logical length L >= C.  Host-only. */
+svx_status svx_tier_round(svx_tier_state* s, int64_t C, int64_t L);
+
+/* Plans a migration with Eq. (5): if none is in flight and E > H, marks [H, E) pending and returns it
+ * in [*begin, *end); otherwise *begin = *end = H.  Host-only (the caller copies). */
+svx_status svx_tier_plan(svx_tier_state* s, int64_t T, int64_t g, int64_t* begin, int64_t* end);
+
+/* The caller's copy of the pending interval has completed: H advances to its endpoint. */
+svx_status svx_tier_complete(svx_tier_state* s);
+
+/* End of round: keep the prefix [0, C_new), C <= C_new <= L, and release [C_new, L) on the GPU (the
+ * released interval is returned).  It never meets [0, H) (SVX_ERR_BAD_STATE if it would). */
+svx_status svx_tier_commit(svx_tier_state* s, int64_t C_new, int64_t* rel_begin, int64_t* rel_end);
+
+/* Plans with Eq. (5) and, if E > H, enqueues on `stream` (cudaStream_t) the device-to-host copy of
+ * rows [H, E) of K and V: k_dev_at_H / v_dev_at_H are the device addresses of position H, k_host /
+ * v_host pinned host addresses of position 0 of the request's history; row_bytes = Hkv * d * 2.
+ * H does not move until svx_tier_poll reports the copy complete (section 4.1).  *E_out = E (= H if
+ * nothing moves).  SVX_ERR_BAD_STATE while a previous migration is still unpolled. */
+svx_status svx_tier_migrate(svx_tier_state* s, int64_t T, int64_t g, int64_t row_bytes, const void* k_dev_at_H,
+                            const void* v_dev_at_H, void* k_host, void* v_host, void* stream, int64_t* E_out);
+
+/* *done = 1 and H advanced if the migration in flight has completed (or none was in flight), else 0. */
+svx_status svx_tier_poll(svx_tier_state* s, int32_t* done);
+
+/* Waits for a migration in flight, advances H and frees its event. */
+svx_status svx_tier_release(svx_tier_state* s);
 
 /* Library version string. */
 const char* svx_version(void);

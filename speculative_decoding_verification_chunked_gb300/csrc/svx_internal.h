@@ -17,7 +17,7 @@ namespace svx {
 
 constexpr int kMaxReq = 256;
 constexpr int kMaxPartsPerLaunch = 64;  // keeps the kernel parameter block near 2.5 KiB
-constexpr int kHistSlots = 8;           // history state slots per query row
+constexpr int kHistSlots = 8;           // state slots per query row (history segments)
 constexpr int kTile = 32;               // KV tokens per shared-memory tile (FMA kernel)
 constexpr int kRowsPerBlock = 32;       // query rows (G * nq) per CTA of the FMA kernel
 constexpr int kTcTile = 128;            // KV tokens per tile (tensor-core kernel, MMA M)
@@ -43,7 +43,6 @@ struct ChunkParams {
   const __nv_bfloat16* q;  // [B][Hq][nq][d]
   RowState* ws_h;          // [slots][slot_stride]
   float* ws_a;             // [slots][slot_stride][d]
-  const uint32_t* vis;     // [B][nq] candidate visibility words (masked form only)
   int* err;                // device error word (bounded waits that gave up)
   int64_t slot_stride;     // state rows per slot (max_req * Hq * max_query)
   int64_t total_tiles;     // tensor-core kernel: tiles over all (part, head, row block)
@@ -60,17 +59,28 @@ struct ChunkParams {
   PartDesc parts[kMaxPartsPerLaunch];
 };
 
+// Finish kernel: candidate region, merge and finalize.
 struct FinishParams {
   const RowState* ws_h;
   const float* ws_a;
   int64_t slot_stride;
-  __nv_bfloat16* o;  // [B][Hq][nq][d]
-  float* lse;        // [B][Hq][nq]
+  __nv_bfloat16* o;              // [B][Hq][nq][d]
+  float* lse;                    // [B][Hq][nq]
+  const __nv_bfloat16* q;        // [B][Hq][nq][d]
+  const __nv_bfloat16* k_cand;   // [B][n_cand][Hkv][d], or nullptr: no candidate region this round
+  const __nv_bfloat16* v_cand;
+  float q_scale;                 // softmax scale * log2(e)
   uint32_t epoch;
   int32_t n_req;
   int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t group;
   int32_t n_query;
-  uint32_t slot_mask[kMaxReq];  // per request: state slots that may hold data this round
+  int32_t n_cand;                // == n_query
+  int32_t tree;                  // 0: causal chain; 1: token tree given by parent[]
+  int32_t pad0;
+  uint32_t slot_mask[kMaxReq];   // per request: history state slots that may hold data this round
+  int8_t parent[kMaxReq * 32];   // tree parents, request b node i at [b * n_query + i]; root -1
 };
 
 // FMA kernel: split s of a part with n_tiles tiles covers tiles [s*n/S, (s+1)*n/S).
@@ -83,7 +93,7 @@ __host__ __device__ inline int64_t split_tile_begin(int64_t n_tiles, int s, int 
 __host__ __device__ inline int64_t cta_tile_begin(int64_t k, int64_t n, int64_t T) { return (k * T) / n; }
 __host__ __device__ inline int64_t cta_of_tile(int64_t x, int64_t n, int64_t T) { return ((x + 1) * n - 1) / T; }
 
-cudaError_t launch_chunk_attn(const ChunkParams& p, int head_dim, bool masked, cudaStream_t stream);
+cudaError_t launch_chunk_attn(const ChunkParams& p, int head_dim, cudaStream_t stream);
 cudaError_t launch_finish(const FinishParams& p, int head_dim, cudaStream_t stream);
 
 // Tensor-core chunk kernel (d = 128, rows per (part, head) block padded to ncol = 32 or 64).

@@ -2,15 +2,15 @@
 // ("Resource-Efficient Speculative Decoding for Long-Context LLM Serving",
 // section 4.2, Eqs. (6)-(9)).
 //
-//   chunk_attn_fma<D, false>  history chunk: every query of the round attends to
+//   chunk_attn_fma<D>         history chunk: every query of the round attends to
 //                             every token of the chunk (the chunk is shared by
 //                             the whole query group, section 4.2), chunk-local
 //                             state (Eq. 7) merged into the running state (Eq. 8).
-//   chunk_attn_fma<D, true>   candidate region: the same update under the
-//                             per-query visibility words (causal chain or
-//                             token tree, section 4.2 last paragraph).
-//   finish_kernel<D>          merges the split states (Eq. 8) and writes
-//                             O = a / l (Eq. 9) in bf16 and LSE in fp32.
+//                             (FP32-FMA form; d = 128 runs on the tensor cores.)
+//   finish_kernel<D>          the candidate region under its causal / token-tree
+//                             mask (section 4.2, last paragraph), then the merge
+//                             of all states (Eq. 8), O = a / l (Eq. 9) in bf16
+//                             and LSE in fp32.
 //
 // Scores are kept in log2 units (Q is pre-multiplied by scale * log2 e) so the
 // exponentials are exp2; LSE is converted back to natural log on output.
@@ -65,7 +65,7 @@ constexpr float kNegInf = -INFINITY;
 // serves all rows.  Warp w owns rows w, w+4, ..., lane t owns token t of the
 // tile for the scores and columns [t*D/32, (t+1)*D/32) for the value sum.
 // ---------------------------------------------------------------------------
-template <int D, bool MASKED>
+template <int D>
 __global__ void __launch_bounds__(128) chunk_attn_fma(const __grid_constant__ ChunkParams P) {
   constexpr int TILE = kTile;
   constexpr int KSTR = D + 8;  // padded K row: conflict-free 16-byte reads by 32 lanes
@@ -124,15 +124,6 @@ __global__ void __launch_bounds__(128) chunk_attn_fma(const __grid_constant__ Ch
 
   // rows owned by this warp: rr = warp + 4*i, i < nrw
   const int nrw = nr > warp ? (nr - warp + 3) / 4 : 0;
-  uint32_t vis_word[RPW];
-  if constexpr (MASKED) {
-#pragma unroll
-    for (int i = 0; i < RPW; ++i) {
-      const int rr = warp + 4 * i;
-      vis_word[i] = (i < nrw) ? P.vis[static_cast<int64_t>(b) * P.n_query + (r0 + rr) % P.n_query] : 0u;
-    }
-  }
-
   float m[RPW], l[RPW], acc[RPW][VPL];
 #pragma unroll
   for (int i = 0; i < RPW; ++i) {
@@ -186,8 +177,7 @@ __global__ void __launch_bounds__(128) chunk_attn_fma(const __grid_constant__ Ch
     for (int i = 0; i < RPW; ++i) {
       pr[i] = 0.f;
       if (i < nrw) {
-        bool valid = tok < n_tok;
-        if constexpr (MASKED) valid = valid && tok < 32 && ((vis_word[i] >> tok) & 1u);
+        const bool valid = tok < n_tok;
         const float si = valid ? s[i] : kNegInf;
         const float mn = fmaxf(m[i], warp_max(si));
         if (mn != kNegInf) {
@@ -258,8 +248,14 @@ __global__ void __launch_bounds__(128) chunk_attn_fma(const __grid_constant__ Ch
 }
 
 // ---------------------------------------------------------------------------
-// Finish: one warp per query row (b, h, j); merges the state slots that hold
-// data (Eq. 8), then O = a / l (Eq. 9), LSE = (m + log2 l) * ln 2.
+// Finish: one warp per query row (b, h, j).
+//   1. Candidate region (section 4.2, last paragraph): the row attends to the
+//      GPU-resident candidates its visibility word allows - candidates 0..j of a
+//      causal chain, or j and its ancestors in a token tree - with the same
+//      online-softmax update (Eqs. 7-8); lane t holds dimensions [t*D/32, ...).
+//   2. Merge: that state and every history state slot written this round are
+//      combined with Eq. (8).
+//   3. O = a / l (Eq. 9) as bf16, LSE = (m + log2 l) * ln 2 as fp32.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ FinishParams P) {
@@ -269,23 +265,60 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
   const int64_t n_rows = static_cast<int64_t>(P.n_req) * P.n_q_heads * P.n_query;
   if (row >= n_rows) return;
   const int b = static_cast<int>(row / (static_cast<int64_t>(P.n_q_heads) * P.n_query));
-  uint32_t mask = P.slot_mask[b];
+  const int h = static_cast<int>((row / P.n_query) % P.n_q_heads);
+  const int j = static_cast<int>(row % P.n_query);
   float m = kNegInf, l = 0.f, a[VPL];
 #pragma unroll
   for (int c = 0; c < VPL; ++c) a[c] = 0.f;
+
+  if (P.k_cand != nullptr) {
+    uint32_t word;
+    if (!P.tree) {
+      word = (j == 31) ? 0xffffffffu : ((2u << j) - 1u);
+    } else {
+      word = 0u;
+      int node = j;
+      for (int step = 0; step < 32 && node >= 0; ++step) {  // j, then its ancestors up to the root
+        word |= 1u << node;
+        node = P.parent[b * P.n_query + node];
+      }
+    }
+    float q[VPL];
+    const __nv_bfloat16* qp = P.q + row * D + lane * VPL;
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) q[c] = __bfloat162float(qp[c]) * P.q_scale;
+    const int g = h / P.group;
+    while (word) {
+      const int i = __ffs(word) - 1;
+      word &= word - 1u;
+      const int64_t kv = ((static_cast<int64_t>(b) * P.n_cand + i) * P.n_kv_heads + g) * D + lane * VPL;
+      float dot = 0.f;
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) dot = fmaf(q[c], __bfloat162float(P.k_cand[kv + c]), dot);
+      const float sc = warp_sum(dot);
+      const float mn = fmaxf(m, sc);
+      const float al = exp2_approx(m - mn), p = exp2_approx(sc - mn);
+      l = l * al + p;
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) a[c] = fmaf(p, __bfloat162float(P.v_cand[kv + c]), a[c] * al);
+      m = mn;
+    }
+  }
+
+  uint32_t mask = P.slot_mask[b];
   while (mask) {
     const int s = __ffs(mask) - 1;
     mask &= mask - 1;
     const int64_t idx = static_cast<int64_t>(s) * P.slot_stride + row;
-    const RowState h = P.ws_h[idx];
-    if (h.epoch != P.epoch) continue;  // slot not written for this row in this round
-    const float mn = fmaxf(m, h.m);
+    const RowState hs = P.ws_h[idx];
+    if (hs.epoch != P.epoch) continue;  // slot not written for this row in this round
+    const float mn = fmaxf(m, hs.m);
     if (mn == kNegInf) continue;
-    const float al = exp2_approx(m - mn), be = exp2_approx(h.m - mn);
+    const float al = exp2_approx(m - mn), be = exp2_approx(hs.m - mn);
     const float* ap = P.ws_a + idx * D + lane * VPL;
 #pragma unroll
     for (int c = 0; c < VPL; ++c) a[c] = a[c] * al + ap[c] * be;
-    l = l * al + h.l * be;
+    l = l * al + hs.l * be;
     m = mn;
   }
   __nv_bfloat16* op = P.o + row * D + lane * VPL;
@@ -301,26 +334,26 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
   }
 }
 
-template <int D, bool MASKED>
+template <int D>
 cudaError_t launch_chunk_fma(const ChunkParams& p, cudaStream_t stream) {
   constexpr size_t smem = kRowsPerBlock * D * sizeof(float) + 2 * kTile * (D + 8) * 2 + 2 * kTile * D * 2;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_attn_fma<D, MASKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(chunk_attn_fma<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     configured = true;
   }
   dim3 grid(p.splits, p.n_kv_heads, p.n_parts * p.n_rowblk);
-  chunk_attn_fma<D, MASKED><<<grid, 128, smem, stream>>>(p);
+  chunk_attn_fma<D><<<grid, 128, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_chunk_attn(const ChunkParams& p, int head_dim, bool masked, cudaStream_t stream) {
-  if (head_dim == 128) return masked ? launch_chunk_fma<128, true>(p, stream) : launch_chunk_fma<128, false>(p, stream);
-  if (head_dim == 64) return masked ? launch_chunk_fma<64, true>(p, stream) : launch_chunk_fma<64, false>(p, stream);
+cudaError_t launch_chunk_attn(const ChunkParams& p, int head_dim, cudaStream_t stream) {
+  if (head_dim == 128) return launch_chunk_fma<128>(p, stream);
+  if (head_dim == 64) return launch_chunk_fma<64>(p, stream);
   return cudaErrorInvalidValue;
 }
 

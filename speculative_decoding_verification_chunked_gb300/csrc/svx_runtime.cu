@@ -57,8 +57,7 @@ struct svx_ctx_s {
   std::vector<cudaEvent_t> slot_ready, slot_free;
   int next_slot = 0;
 
-  // fp32 state workspace: kHistSlots history slots + 1 candidate-region slot,
-  // rows stamped with the round epoch that wrote them
+  // fp32 state workspace: kHistSlots history slots, rows stamped with the round epoch that wrote them
   svx::RowState* ws_h = nullptr;
   float* ws_a = nullptr;
   int64_t slot_stride = 0;
@@ -66,10 +65,11 @@ struct svx_ctx_s {
   int* d_err = nullptr;   // device error word: a kernel's bounded wait gave up
   bool use_tc = false;    // chunk kernel on the tensor cores (d = 128)
 
-  // candidate visibility words: pinned host staging and device copy
-  uint32_t* h_vis = nullptr;
-  uint32_t* d_vis = nullptr;
-  cudaEvent_t vis_copied = nullptr;
+  // candidate region of the open round: computed by the finish kernel, whose launch parameters
+  // carry the tree parents, so no copy is queued behind the chunk transfers
+  const __nv_bfloat16* cand_k = nullptr;
+  const __nv_bfloat16* cand_v = nullptr;
+  std::vector<int8_t> cand_parent;  // [n_req][n_query], empty for the causal chain
   cudaEvent_t done = nullptr;
 
   // round
@@ -85,8 +85,7 @@ struct svx_ctx_s {
   // timing (SVX_FLAG_TIMING)
   std::vector<PushEvents> ev_push;
   int n_push = 0;
-  cudaEvent_t ev_begin = nullptr, ev_c0 = nullptr, ev_c1 = nullptr, ev_f0 = nullptr, ev_f1 = nullptr;
-  bool cand_timed = false;
+  cudaEvent_t ev_begin = nullptr, ev_f0 = nullptr, ev_f1 = nullptr;
   bool stats_valid = false;
   int64_t h2d_bytes = 0, dev_bytes = 0;
   int n_launch = 0, n_copies = 0;
@@ -132,8 +131,10 @@ int pointer_kind(const void* p) {
   return 0;
 }
 
-svx_status masks_impl(int32_t n_req, int32_t n_query, const int32_t* parent, uint32_t* out, std::string* why) {
-  if (n_req < 0 || n_query < 1 || n_query > 32 || !out) {
+// Visibility words of the candidate region; with validate_only, checks the tree and writes nothing.
+svx_status masks_impl(int32_t n_req, int32_t n_query, const int32_t* parent, uint32_t* out, std::string* why,
+                      bool validate_only = false) {
+  if (n_req < 0 || n_query < 1 || n_query > 32 || (!out && !validate_only)) {
     if (why) *why = "n_req >= 0, 1 <= n_query <= 32 and out != NULL required";
     return SVX_ERR_INVALID_ARG;
   }
@@ -150,6 +151,7 @@ svx_status masks_impl(int32_t n_req, int32_t n_query, const int32_t* parent, uin
           return SVX_ERR_INVALID_ARG;
         }
     }
+    if (validate_only) continue;
     for (int j = 0; j < n_query; ++j) {
       uint32_t w;
       if (!par) {
@@ -210,13 +212,11 @@ void destroy_all(svx_ctx c) {
   for (auto& pe : c->ev_push) {
     cudaEventDestroy(pe.copy0); cudaEventDestroy(pe.copy1); cudaEventDestroy(pe.k0); cudaEventDestroy(pe.k1);
   }
-  for (cudaEvent_t e : {c->ev_begin, c->ev_c0, c->ev_c1, c->ev_f0, c->ev_f1, c->vis_copied, c->done})
+  for (cudaEvent_t e : {c->ev_begin, c->ev_f0, c->ev_f1, c->done})
     if (e) cudaEventDestroy(e);
   if (c->ws_h) cudaFree(c->ws_h);
   if (c->d_err) cudaFree(c->d_err);
   if (c->ws_a) cudaFree(c->ws_a);
-  if (c->d_vis) cudaFree(c->d_vis);
-  if (c->h_vis) cudaFreeHost(c->h_vis);
   if (c->own_cs && c->cs) cudaStreamDestroy(c->cs);
   if (c->own_xs && c->xs) cudaStreamDestroy(c->xs);
   if (prev >= 0) cudaSetDevice(prev);
@@ -298,6 +298,7 @@ svx_status svx_create(const svx_config* cfg, svx_ctx* out) {
     return fail(nullptr, SVX_ERR_INVALID_ARG, "max_query must be in [1, 32]");
   if (k.max_chunk_tokens < 1) return fail(nullptr, SVX_ERR_INVALID_ARG, "max_chunk_tokens must be >= 1");
   if (k.n_slots < 2 || k.n_slots > 3) return fail(nullptr, SVX_ERR_INVALID_ARG, "n_slots must be 2 or 3");
+  if (k.zero_copy_ctas < 0) return fail(nullptr, SVX_ERR_INVALID_ARG, "zero_copy_ctas must be >= 0");
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
     cudaGetLastError();
@@ -344,12 +345,10 @@ svx_status svx_create(const svx_config* cfg, svx_ctx* out) {
   }
   c->use_tc = !(k.flags & SVX_FLAG_NO_TENSOR_CORES) && svx::tc_supported(k.head_dim, c->group * k.max_query);
   c->slot_stride = static_cast<int64_t>(k.max_req) * k.n_q_heads * k.max_query;
-  const int64_t n_state = static_cast<int64_t>(svx::kHistSlots + 1) * c->slot_stride;
+  const int64_t n_state = static_cast<int64_t>(svx::kHistSlots) * c->slot_stride;
   if (cudaMalloc(reinterpret_cast<void**>(&c->ws_h), static_cast<size_t>(n_state) * sizeof(svx::RowState)) !=
           cudaSuccess ||
       cudaMalloc(reinterpret_cast<void**>(&c->ws_a), static_cast<size_t>(n_state) * k.head_dim * sizeof(float)) !=
-          cudaSuccess ||
-      cudaMalloc(reinterpret_cast<void**>(&c->d_vis), static_cast<size_t>(k.max_req) * 32 * sizeof(uint32_t)) !=
           cudaSuccess ||
       cudaMalloc(reinterpret_cast<void**>(&c->d_err), sizeof(int)) != cudaSuccess) {
     cudaGetLastError();
@@ -361,18 +360,12 @@ svx_status svx_create(const svx_config* cfg, svx_ctx* out) {
     cudaGetLastError();
     return bail(SVX_ERR_CUDA, "workspace initialisation failed");
   }
-  if (cudaHostAlloc(reinterpret_cast<void**>(&c->h_vis), static_cast<size_t>(k.max_req) * 32 * sizeof(uint32_t),
-                    cudaHostAllocDefault) != cudaSuccess) {
-    cudaGetLastError();
-    return bail(SVX_ERR_OOM, "pinned mask buffer allocation failed");
-  }
-  c->vis_copied = make_event(false);
   c->done = make_event(false);
-  if (!c->vis_copied || !c->done) return bail(SVX_ERR_CUDA, "event creation failed");
+  if (!c->done) return bail(SVX_ERR_CUDA, "event creation failed");
   if (k.flags & SVX_FLAG_TIMING) {
-    c->ev_begin = make_event(true); c->ev_c0 = make_event(true); c->ev_c1 = make_event(true);
+    c->ev_begin = make_event(true);
     c->ev_f0 = make_event(true); c->ev_f1 = make_event(true);
-    if (!c->ev_begin || !c->ev_c0 || !c->ev_c1 || !c->ev_f0 || !c->ev_f1)
+    if (!c->ev_begin || !c->ev_f0 || !c->ev_f1)
       return bail(SVX_ERR_CUDA, "event creation failed");
   }
   *out = c;
@@ -409,7 +402,6 @@ svx_status svx_round_begin(svx_ctx c, int32_t n_req, int32_t n_query, const void
   c->parts_seen.clear();
   c->cand_done = false;
   c->n_push = 0;
-  c->cand_timed = false;
   c->last_stats_pending = false;
   c->h2d_bytes = c->dev_bytes = 0;
   c->n_launch = c->n_copies = 0;
@@ -424,7 +416,7 @@ namespace {
 // Launches the chunk kernel over `parts` (already resolved to device pointers),
 // in batches of at most kMaxPartsPerLaunch parts, and records which state slots
 // each request may now hold.
-svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, bool masked, int slot_base, int splits_override) {
+svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, int cta_cap) {
   const int R = c->group * c->n_query;
   for (size_t i0 = 0; i0 < parts.size(); i0 += svx::kMaxPartsPerLaunch) {
     const int n = static_cast<int>(std::min<size_t>(svx::kMaxPartsPerLaunch, parts.size() - i0));
@@ -433,7 +425,6 @@ svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, bool masked, in
     p.q = c->q;
     p.ws_h = c->ws_h;
     p.ws_a = c->ws_a;
-    p.vis = masked ? c->d_vis : nullptr;
     p.err = c->d_err;
     p.slot_stride = c->slot_stride;
     p.q_scale = c->q_scale;
@@ -442,10 +433,10 @@ svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, bool masked, in
     p.n_kv_heads = c->cfg.n_kv_heads;
     p.group = c->group;
     p.n_query = c->n_query;
-    p.slot_base = slot_base;
+    p.slot_base = 0;
     p.n_parts = n;
     for (int i = 0; i < n; ++i) p.parts[i] = parts[i0 + i];
-    if (c->use_tc && !masked) {
+    if (c->use_tc) {
       // tensor-core kernel: tiles of all (part, head, row block) pairs split evenly over the CTAs
       const int ncol = svx::tc_ncol(R);
       p.n_rowblk = (R + ncol - 1) / ncol;
@@ -462,21 +453,26 @@ svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, bool masked, in
       }
       p.total_tiles = T;
       int64_t ctas = std::min<int64_t>(svx::tc_max_ctas(c->num_sms), T);
+      if (cta_cap > 0) ctas = std::min<int64_t>(ctas, cta_cap);
       while (ctas > 1 && max_segments(pair_first, pair_tiles, ctas, T) > svx::kHistSlots) --ctas;
       const int64_t segs = max_segments(pair_first, pair_tiles, ctas, T);
       for (int i = 0; i < n; ++i) {
         uint32_t& used = c->slot_mask[static_cast<size_t>(p.parts[i].req)];
-        used |= ((segs >= 32 ? 0xffffffffu : ((1u << segs) - 1u)) << slot_base);
+        used |= (segs >= 32 ? 0xffffffffu : ((1u << segs) - 1u));
       }
       SVX_CUDA(c, svx::launch_chunk_attn_tc(p, ncol, static_cast<int>(ctas), c->cs));
     } else {
       p.n_rowblk = (R + svx::kRowsPerBlock - 1) / svx::kRowsPerBlock;
       int64_t max_tok = 0;
       for (int i = 0; i < n; ++i) max_tok = std::max<int64_t>(max_tok, p.parts[i].n_tok);
-      p.splits = splits_override > 0 ? splits_override : choose_splits(c, n, max_tok, p.n_rowblk);
+      p.splits = choose_splits(c, n, max_tok, p.n_rowblk);
+      if (cta_cap > 0) {
+        const int64_t pairs = static_cast<int64_t>(n) * c->cfg.n_kv_heads * p.n_rowblk;
+        p.splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p.splits, cta_cap / std::max<int64_t>(1, pairs))));
+      }
       for (int i = 0; i < n; ++i)
-        c->slot_mask[static_cast<size_t>(p.parts[i].req)] |= nonempty_splits(p.parts[i].n_tok, p.splits) << slot_base;
-      SVX_CUDA(c, svx::launch_chunk_attn(p, c->cfg.head_dim, masked, c->cs));
+        c->slot_mask[static_cast<size_t>(p.parts[i].req)] |= nonempty_splits(p.parts[i].n_tok, p.splits);
+      SVX_CUDA(c, svx::launch_chunk_attn(p, c->cfg.head_dim, c->cs));
     }
     ++c->n_launch;
   }
@@ -514,7 +510,9 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
                   "part %d: k and v must both be pinned host memory or both device memory (pageable host memory "
                   "cannot be streamed)", i);
     kind[static_cast<size_t>(i)] = kk;
-    if (kk == 1) {
+    if (kk == 1 && (c->cfg.flags & SVX_FLAG_ZERO_COPY)) {
+      kind[static_cast<size_t>(i)] = 3;  // pinned host, read in place by the kernel
+    } else if (kk == 1) {
       if (p.n_tok > c->cfg.max_chunk_tokens)
         return fail(c, SVX_ERR_INVALID_ARG, "part %d: %d tokens exceed max_chunk_tokens %d", i, p.n_tok,
                     c->cfg.max_chunk_tokens);
@@ -531,6 +529,7 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
 
   std::vector<PartDesc> desc(static_cast<size_t>(n_parts));
   int slot = -1;
+  bool zero_copy = false;
   if (n_host > 0) {
     // copy engine: wait until the compute stream released the slot, then stage the host parts
     slot = c->next_slot;
@@ -557,10 +556,12 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
   }
   for (int i = 0; i < n_parts; ++i) {
     const svx_part& p = parts[i];
-    if (kind[static_cast<size_t>(i)] == 2) {
+    const int kd = kind[static_cast<size_t>(i)];
+    if (kd == 2 || kd == 3) {
       desc[static_cast<size_t>(i)] = PartDesc{static_cast<const __nv_bfloat16*>(p.k),
                                               static_cast<const __nv_bfloat16*>(p.v), 0, p.req, p.n_tok};
-      c->dev_bytes += 2 * static_cast<int64_t>(p.n_tok) * row_elems * 2;
+      (kd == 2 ? c->dev_bytes : c->h2d_bytes) += 2 * static_cast<int64_t>(p.n_tok) * row_elems * 2;
+      if (kd == 3) zero_copy = true;
     }
     c->parts_seen.push_back({p.req, p.tok_start, p.n_tok});
   }
@@ -568,7 +569,7 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
     pe->has_copy = n_host > 0;
     SVX_CUDA(c, cudaEventRecord(pe->k0, c->cs));
   }
-  svx_status st = launch_parts(c, desc, false, 0, 0);
+  svx_status st = launch_parts(c, desc, zero_copy ? c->cfg.zero_copy_ctas : 0);
   if (st != SVX_OK) return st;
   if (pe) {
     SVX_CUDA(c, cudaEventRecord(pe->k1, c->cs));
@@ -590,27 +591,15 @@ svx_status svx_candidate_attn(svx_ctx c, const void* k_dev, const void* v_dev, i
   DeviceGuard dg(c->cfg.device);
   if (pointer_kind(k_dev) != 2 || pointer_kind(v_dev) != 2)
     return fail(c, SVX_ERR_INVALID_ARG, "candidate k/v must be device memory (the candidate region is GPU-resident)");
-  // the previous round's mask upload must have left the pinned staging buffer
-  SVX_CUDA(c, cudaEventSynchronize(c->vis_copied));
   std::string why;
-  if (masks_impl(c->n_req, c->n_query, parent_host, c->h_vis, &why) != SVX_OK)
+  if (masks_impl(c->n_req, c->n_query, parent_host, nullptr, &why, true) != SVX_OK)
     return fail(c, SVX_ERR_INVALID_ARG, "%s", why.c_str());
-  SVX_CUDA(c, cudaMemcpyAsync(c->d_vis, c->h_vis, static_cast<size_t>(c->n_req) * c->n_query * sizeof(uint32_t),
-                              cudaMemcpyHostToDevice, c->cs));
-  SVX_CUDA(c, cudaEventRecord(c->vis_copied, c->cs));
-  const int64_t per_req = static_cast<int64_t>(n_cand) * c->cfg.n_kv_heads * c->cfg.head_dim;
-  std::vector<PartDesc> desc(static_cast<size_t>(c->n_req));
-  for (int b = 0; b < c->n_req; ++b)
-    desc[static_cast<size_t>(b)] = PartDesc{static_cast<const __nv_bfloat16*>(k_dev) + b * per_req,
-                                            static_cast<const __nv_bfloat16*>(v_dev) + b * per_req, 0, b, n_cand};
-  const bool timing = (c->cfg.flags & SVX_FLAG_TIMING) != 0;
-  if (timing) SVX_CUDA(c, cudaEventRecord(c->ev_c0, c->cs));
-  svx_status st = launch_parts(c, desc, true, svx::kHistSlots, 1);
-  if (st != SVX_OK) return st;
-  if (timing) {
-    SVX_CUDA(c, cudaEventRecord(c->ev_c1, c->cs));
-    c->cand_timed = true;
-  }
+  // the candidate region is computed by the finish kernel; keep what it needs
+  c->cand_k = static_cast<const __nv_bfloat16*>(k_dev);
+  c->cand_v = static_cast<const __nv_bfloat16*>(v_dev);
+  c->cand_parent.clear();
+  if (parent_host)
+    c->cand_parent.assign(parent_host, parent_host + static_cast<size_t>(c->n_req) * c->n_query);
   c->cand_done = true;
   return SVX_OK;
 }
@@ -637,9 +626,19 @@ svx_status svx_round_finish(svx_ctx c, void* o_dev, float* lse_dev, int32_t time
   p.epoch = c->epoch;
   p.o = static_cast<__nv_bfloat16*>(o_dev);
   p.lse = lse_dev;
+  p.q = c->q;
+  p.k_cand = c->cand_done ? c->cand_k : nullptr;
+  p.v_cand = c->cand_done ? c->cand_v : nullptr;
+  p.q_scale = c->q_scale;
   p.n_req = c->n_req;
   p.n_q_heads = c->cfg.n_q_heads;
+  p.n_kv_heads = c->cfg.n_kv_heads;
+  p.group = c->group;
   p.n_query = c->n_query;
+  p.n_cand = c->n_query;
+  p.tree = c->cand_done && !c->cand_parent.empty() ? 1 : 0;
+  if (p.tree)
+    for (size_t i = 0; i < c->cand_parent.size(); ++i) p.parent[i] = static_cast<int8_t>(c->cand_parent[i]);
   for (int b = 0; b < c->n_req; ++b) p.slot_mask[b] = c->slot_mask[static_cast<size_t>(b)];
   const bool timing = (c->cfg.flags & SVX_FLAG_TIMING) != 0;
   c->state = RoundState::kIdle;
@@ -693,12 +692,30 @@ svx_status svx_round_stats(svx_ctx c, svx_stats* out) {
     SVX_CUDA(c, cudaEventElapsedTime(&ms, pe.k0, pe.k1));
     s.chunk_kernel_ms += ms;
   }
-  if (c->cand_timed) {
-    SVX_CUDA(c, cudaEventElapsedTime(&ms, c->ev_c0, c->ev_c1));
-    s.cand_kernel_ms = ms;
-  }
   SVX_CUDA(c, cudaEventElapsedTime(&ms, c->ev_f0, c->ev_f1));
   s.finish_kernel_ms = ms;
+  // chunk-kernel time not covered by any copy interval of the round (exposed compute)
+  std::vector<std::pair<double, double>> cp, kr;
+  for (int i = 0; i < c->n_push; ++i) {
+    const PushEvents& pe = c->ev_push[static_cast<size_t>(i)];
+    float a = 0.f, b = 0.f;
+    if (pe.has_copy) {
+      SVX_CUDA(c, cudaEventElapsedTime(&a, c->ev_begin, pe.copy0));
+      SVX_CUDA(c, cudaEventElapsedTime(&b, c->ev_begin, pe.copy1));
+      cp.push_back({a, b});
+    }
+    SVX_CUDA(c, cudaEventElapsedTime(&a, c->ev_begin, pe.k0));
+    SVX_CUDA(c, cudaEventElapsedTime(&b, c->ev_begin, pe.k1));
+    kr.push_back({a, b});
+  }
+  std::sort(cp.begin(), cp.end());
+  double exposed = 0.0;
+  for (const auto& k : kr) {
+    double covered = 0.0;
+    for (const auto& x : cp) covered += std::max(0.0, std::min(k.second, x.second) - std::max(k.first, x.first));
+    exposed += std::max(0.0, (k.second - k.first) - covered);
+  }
+  s.chunk_kernel_exposed_ms = exposed;
   *out = s;
   return SVX_OK;
 }

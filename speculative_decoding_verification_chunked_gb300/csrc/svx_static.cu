@@ -1,6 +1,6 @@
 // svx_verify_static: one whole verification round over device-resident KV that
-// allocates no device memory.  Its fp32 state workspace, the candidate
-// visibility words and the device error word live in a file-scope
+// allocates no device memory.  Its fp32 state workspace and the device error
+// word live in a file-scope
 // `static __device__` array of fixed size, which every GPU that loads this
 // library holds until the process exits.
 //
@@ -32,9 +32,8 @@ void set_thread_error(const char* msg);  // svx_runtime.cu: message for svx_last
 namespace {
 
 constexpr size_t kScratchBytes = SVX_STATIC_SCRATCH_BYTES;
-constexpr size_t kVisBytes = static_cast<size_t>(svx::kMaxReq) * 32 * sizeof(uint32_t);
-constexpr size_t kErrOffset = kVisBytes;
-constexpr size_t kStateOffset = kVisBytes + 256;
+constexpr size_t kErrOffset = 0;
+constexpr size_t kStateOffset = 256;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kScratchBytes];
@@ -87,7 +86,7 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
   if ((k_cand_dev == nullptr) != (v_cand_dev == nullptr))
     return fail(SVX_ERR_INVALID_ARG, "give both candidate k and v, or neither");
   const int64_t rows = static_cast<int64_t>(n_req) * n_q_heads * n_query;
-  const size_t need = kStateOffset + static_cast<size_t>(svx::kHistSlots + 1) * static_cast<size_t>(rows) *
+  const size_t need = kStateOffset + static_cast<size_t>(svx::kHistSlots) * static_cast<size_t>(rows) *
                                          (sizeof(svx::RowState) + sizeof(float) * head_dim);
   if (need > kScratchBytes)
     return fail(SVX_ERR_INVALID_ARG,
@@ -103,8 +102,8 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
   }
   if (k_cand_dev && (!aligned16(k_cand_dev) || !aligned16(v_cand_dev)))
     return fail(SVX_ERR_INVALID_ARG, "candidate k/v must be 16-byte aligned");
-  uint32_t vis_host[svx::kMaxReq * 32];
-  if (k_cand_dev && svx_candidate_masks(n_req, n_query, parent_host, vis_host) != SVX_OK)
+  static thread_local uint32_t vis_check[svx::kMaxReq * 32];  // validation only
+  if (k_cand_dev && svx_candidate_masks(n_req, n_query, parent_host, vis_check) != SVX_OK)
     return fail(SVX_ERR_INVALID_ARG, "invalid token-tree parents");
 
   int dev = -1;
@@ -138,11 +137,10 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
   if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return fail(SVX_ERR_CUDA, "cannot read the SM count");
 
-  uint32_t* d_vis = reinterpret_cast<uint32_t*>(sd.ptr);
   int* d_err = reinterpret_cast<int*>(sd.ptr + kErrOffset);
   svx::RowState* ws_h = reinterpret_cast<svx::RowState*>(sd.ptr + kStateOffset);
   float* ws_a = reinterpret_cast<float*>(sd.ptr + kStateOffset +
-                                         static_cast<size_t>(svx::kHistSlots + 1) * rows * sizeof(svx::RowState));
+                                         static_cast<size_t>(svx::kHistSlots) * rows * sizeof(svx::RowState));
   const int G = n_q_heads / n_kv_heads;
   const int R = G * n_query;
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(head_dim));
@@ -169,7 +167,6 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
     if (hist_len_host[b] > 0) reqs[n_hist++] = b;
   for (int i0 = 0; i0 < n_hist; i0 += svx::kMaxPartsPerLaunch) {
     const int n = std::min(svx::kMaxPartsPerLaunch, n_hist - i0);
-    p.vis = nullptr;
     p.slot_base = 0;
     p.n_parts = n;
     for (int i = 0; i < n; ++i) {
@@ -221,36 +218,12 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
           if (svx::split_tile_begin(nt, sp2 + 1, p.splits) > svx::split_tile_begin(nt, sp2, p.splits))
             slot_mask[p.parts[i].req] |= 1u << sp2;
       }
-      e = svx::launch_chunk_attn(p, head_dim, false, s);
+      e = svx::launch_chunk_attn(p, head_dim, s);
     }
     if (e != cudaSuccess) return fail(SVX_ERR_CUDA, "chunk kernel launch failed: %s", cudaGetErrorString(e));
   }
 
-  // ---- candidate region
-  if (k_cand_dev) {
-    cudaError_t e = cudaMemcpyAsync(d_vis, vis_host, static_cast<size_t>(n_req) * n_query * sizeof(uint32_t),
-                                    cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return fail(SVX_ERR_CUDA, "mask upload failed: %s", cudaGetErrorString(e));
-    const int64_t per_req = static_cast<int64_t>(n_query) * n_kv_heads * head_dim;
-    for (int i0 = 0; i0 < n_req; i0 += svx::kMaxPartsPerLaunch) {
-      const int n = std::min(svx::kMaxPartsPerLaunch, n_req - i0);
-      p.vis = d_vis;
-      p.slot_base = svx::kHistSlots;
-      p.splits = 1;
-      p.n_parts = n;
-      p.n_rowblk = (R + svx::kRowsPerBlock - 1) / svx::kRowsPerBlock;
-      for (int i = 0; i < n; ++i) {
-        const int b = i0 + i;
-        p.parts[i] = svx::PartDesc{static_cast<const __nv_bfloat16*>(k_cand_dev) + b * per_req,
-                                   static_cast<const __nv_bfloat16*>(v_cand_dev) + b * per_req, 0, b, n_query};
-        slot_mask[b] |= 1u << svx::kHistSlots;
-      }
-      e = svx::launch_chunk_attn(p, head_dim, true, s);
-      if (e != cudaSuccess) return fail(SVX_ERR_CUDA, "candidate kernel launch failed: %s", cudaGetErrorString(e));
-    }
-  }
-
-  // ---- merge and finalize
+  // ---- candidate region, merge and finalize
   svx::FinishParams f;
   std::memset(&f, 0, sizeof(f));
   f.ws_h = ws_h;
@@ -258,10 +231,20 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
   f.slot_stride = rows;
   f.o = static_cast<__nv_bfloat16*>(o_dev);
   f.lse = lse_dev;
+  f.q = static_cast<const __nv_bfloat16*>(q_dev);
+  f.k_cand = static_cast<const __nv_bfloat16*>(k_cand_dev);
+  f.v_cand = static_cast<const __nv_bfloat16*>(v_cand_dev);
+  f.q_scale = p.q_scale;
   f.epoch = sd.epoch;
   f.n_req = n_req;
   f.n_q_heads = n_q_heads;
+  f.n_kv_heads = n_kv_heads;
+  f.group = G;
   f.n_query = n_query;
+  f.n_cand = n_query;
+  f.tree = (k_cand_dev && parent_host) ? 1 : 0;
+  if (f.tree)
+    for (int i = 0; i < n_req * n_query; ++i) f.parent[i] = static_cast<int8_t>(parent_host[i]);
   for (int b = 0; b < n_req; ++b) f.slot_mask[b] = slot_mask[b];
   cudaError_t e = svx::launch_finish(f, head_dim, s);
   if (e != cudaSuccess) return fail(SVX_ERR_CUDA, "finish kernel launch failed: %s", cudaGetErrorString(e));

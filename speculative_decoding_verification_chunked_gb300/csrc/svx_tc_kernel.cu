@@ -42,6 +42,10 @@ constexpr int NUM_THREADS = 192;
 constexpr int TILE_BYTES = TOK * D * 2;  // one K or V tile, 32 KiB
 constexpr int HALF_BYTES = TOK * 64 * 2; // 64 of the 128 dimensions of a tile, 16 KiB
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// The running maximum of a query row (log2 units) is re-based only when a score
+// exceeds it by more than kTau, so p = 2^(s - m) <= 2^kTau stays exact enough in
+// bf16 and most tiles need no cross-thread maximum at all.
+constexpr float kTau = 8.0f;
 
 template <int NCOL>
 struct TcCfg {
@@ -52,7 +56,7 @@ struct TcCfg {
   static constexpr int OFF_Q = STAGES * 2 * TILE_BYTES;
   static constexpr int OFF_P = OFF_Q + Q_BYTES;
   static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;    // float [4][NCOL]
-  static constexpr int OFF_MNEW = OFF_RED + 4 * NCOL * 4;  // float [NCOL]
+  static constexpr int OFF_MNEW = OFF_RED + 4 * NCOL * 4;  // float [NCOL]: running reference max per row
   static constexpr int OFF_ALPHA = OFF_MNEW + NCOL * 4;  // float [2][NCOL]
   static constexpr int OFF_FIN = OFF_ALPHA + 2 * NCOL * 4;  // float [2][NCOL]: final m, l
   static constexpr int N_BAR = 2 * STAGES + 10 + 2;
@@ -112,6 +116,17 @@ __device__ __forceinline__ bool softmax_all(bool ok) {
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"(static_cast<uint32_t>(ok))
+      : "memory");
+  return r != 0;
+}
+// Barrier among the 128 softmax threads that ORs their flags.
+__device__ __forceinline__ bool softmax_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
       : "memory");
   return r != 0;
 }
@@ -345,16 +360,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
         const int64_t tok0 = (sg.tile0 + t) * TOK;
         const uint32_t kdst = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES;
         const uint32_t vdst = kdst + TILE_BYTES;
+        // lane copies 16-byte piece c = lane % 16 of rows r0 + 2j (j < 64); rows past n_tok read nothing
+        const int c = lane & 15, r0 = lane >> 4;
+        const int64_t valid_rows = (n_tok - tok0 < TOK) ? (n_tok - tok0) : static_cast<int64_t>(TOK);
+        const __nv_bfloat16* ks = kb + (tok0 + r0) * kv_stride + c * 8;
+        const __nv_bfloat16* vs = vb + (tok0 + r0) * kv_stride + c * 8;
+        const int64_t step = 2 * kv_stride;
+        const uint32_t so0 = static_cast<uint32_t>(c >> 3) * HALF_BYTES + static_cast<uint32_t>(r0) * 128u;
 #pragma unroll 8
         for (int j = 0; j < 64; ++j) {
-          const int piece = lane + 32 * j;  // 16 pieces of 16 bytes per token row
-          const int row = piece >> 4, c = piece & 15;
-          const int64_t tok = tok0 + row;
-          const bool in = tok < n_tok;
-          const int64_t off = in ? tok * kv_stride + c * 8 : 0;
-          const uint32_t so = swz_offset(row, c, HALF_BYTES);
-          cp_async16(kdst + so, kb + off, in ? 16 : 0);
-          cp_async16(vdst + so, vb + off, in ? 16 : 0);
+          const int row = r0 + 2 * j;
+          const uint32_t so = so0 + static_cast<uint32_t>(j) * 256u + (static_cast<uint32_t>((c & 7) ^ (row & 7)) << 4);
+          const bool in = row < valid_rows;
+          cp_async16(kdst + so, in ? ks : kb, in ? 16 : 0);
+          cp_async16(vdst + so, in ? vs : vb, in ? 16 : 0);
+          ks += step;
+          vs += step;
         }
         cp_async_arrive_noinc(FULL + 8u * stage);
       }
@@ -436,12 +457,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
     const int tid = threadIdx.x;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     constexpr int NH = NCOL / 32;  // columns per lane after a transpose-reduction
-    float acc[NCOL];
-    float s[NCOL];
-    float m_run[NH], l_w[NH];
+    float acc[NCOL];   // O^T accumulator: output dimension tid, query row c
+    float s[NCOL];     // scores of token tid, then p, then O^T tile values
+    float lsum[NCOL];  // this thread's share of each row's denominator (relative to mref)
+    uint32_t rescaled = 0u;  // bit b: the tile in buffer b re-based the row maxima
+    float* mref = mnew;  // running reference maximum per row, shared by the 128 threads
     int hint = 0;
     int64_t i = 0;
     bool ok = true;
+    int nr = NCOL;
 
     auto accumulate = [&](int64_t j) -> bool {
       if (!softmax_all(W.wait(OFULL + 8u * (j & 1), static_cast<uint32_t>(j >> 1) & 1u))) return false;
@@ -451,14 +475,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
       if constexpr (NCOL == 64) tmem_ld32<32>(ta + 32, s);
       tc_fence_before();
       mbar_arrive(OEMPTY + 8u * (j & 1));
-      const float4* al4 = reinterpret_cast<const float4*>(alpha + (j & 1) * NCOL);
+      if ((rescaled >> (j & 1)) & 1u) {
+        const float4* al4 = reinterpret_cast<const float4*>(alpha + (j & 1) * NCOL);
 #pragma unroll
-      for (int c4 = 0; c4 < NCOL / 4; ++c4) {
-        const float4 a = al4[c4];
-        acc[4 * c4 + 0] = fmaf(acc[4 * c4 + 0], a.x, s[4 * c4 + 0]);
-        acc[4 * c4 + 1] = fmaf(acc[4 * c4 + 1], a.y, s[4 * c4 + 1]);
-        acc[4 * c4 + 2] = fmaf(acc[4 * c4 + 2], a.z, s[4 * c4 + 2]);
-        acc[4 * c4 + 3] = fmaf(acc[4 * c4 + 3], a.w, s[4 * c4 + 3]);
+        for (int c4 = 0; c4 < NCOL / 4; ++c4) {
+          if (4 * c4 < nr) {
+            const float4 a = al4[c4];
+            acc[4 * c4 + 0] = fmaf(acc[4 * c4 + 0], a.x, s[4 * c4 + 0]);
+            acc[4 * c4 + 1] = fmaf(acc[4 * c4 + 1], a.y, s[4 * c4 + 1]);
+            acc[4 * c4 + 2] = fmaf(acc[4 * c4 + 2], a.z, s[4 * c4 + 2]);
+            acc[4 * c4 + 3] = fmaf(acc[4 * c4 + 3], a.w, s[4 * c4 + 3]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < NCOL; ++c)
+          if ((c & ~3) < nr) acc[c] += s[c];
       }
       return true;
     };
@@ -469,7 +501,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
       const int b = pd.req;
       const int R = P.group * P.n_query;
       const int r0 = sg.rb * NCOL;
-      const int nr = min(NCOL, R - r0);
+      nr = min(NCOL, R - r0);
       const int64_t row_base =
           (static_cast<int64_t>(b) * P.n_q_heads + static_cast<int64_t>(sg.g) * P.group) * P.n_query + r0;
 
@@ -480,15 +512,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
         if (c < nr) v = *reinterpret_cast<const uint4*>(P.q + (row_base + c) * D + ch * 8);
         st_shared_v4(base + C::OFF_Q + swz_offset(c, ch, NCOL * 128), v);
       }
+      if (warp == 0) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) mref[lane + 32 * h] = -INFINITY;
+      }
       fence_proxy_async();
       mbar_arrive(QFULL);
 
 #pragma unroll
-      for (int c = 0; c < NCOL; ++c) acc[c] = 0.f;
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        m_run[h] = -INFINITY;
-        l_w[h] = 0.f;
+      for (int c = 0; c < NCOL; ++c) {
+        acc[c] = 0.f;
+        lsum[c] = 0.f;
       }
 
       for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
@@ -503,56 +537,77 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
         if constexpr (NCOL == 64) tmem_ld32<32>(ta + 32, s);
         tc_fence_before();
         mbar_arrive(SEMPTY + 8u * (i & 1));
-#pragma unroll
-        for (int c = 0; c < NCOL; ++c) s[c] = tok_valid ? s[c] * P.q_scale : -INFINITY;
 
-        // tile maximum per row: warp-level transpose-reduction, then across the 4 warps
-        red[warp * NCOL + lane] = xpose_reduce<0, NCOL, true>(s, lane);
-        if constexpr (NCOL == 64) red[warp * NCOL + 32 + lane] = xpose_reduce<32, NCOL, true>(s, lane);
-        named_sync_softmax();
-        if (warp == 0) {
-#pragma unroll
-          for (int h = 0; h < NH; ++h) {
-            const int c = lane + 32 * h;
-            const float tm = fmaxf(fmaxf(red[c], red[NCOL + c]), fmaxf(red[2 * NCOL + c], red[3 * NCOL + c]));
-            const float mn = fmaxf(m_run[h], tm);
-            alpha[(i & 1) * NCOL + c] = (m_run[h] == -INFINITY) ? 0.f : exp2_approx(m_run[h] - mn);
-            mnew[c] = mn;
-            m_run[h] = mn;
-          }
-        }
-        named_sync_softmax();
-
-        // P^T = 2^(s - m_new), bf16, into the K-major swizzled B operand of the PV product
-        const uint32_t pbase = base + C::OFF_P + static_cast<uint32_t>(i & 1) * C::P_BYTES +
-                               static_cast<uint32_t>(tid >> 6) * (NCOL * 128) + static_cast<uint32_t>((tid & 7) << 1);
-        const float4* mn4 = reinterpret_cast<const float4*>(mnew);
+        // scaled scores (log2 units); does any exceed its row's reference by more than kTau?
+        bool up = false;
+        const float4* mr4 = reinterpret_cast<const float4*>(mref);
 #pragma unroll
         for (int c4 = 0; c4 < NCOL / 4; ++c4) {
-          const float4 mm = mn4[c4];
-          s[4 * c4 + 0] = exp2_approx(s[4 * c4 + 0] - mm.x);
-          s[4 * c4 + 1] = exp2_approx(s[4 * c4 + 1] - mm.y);
-          s[4 * c4 + 2] = exp2_approx(s[4 * c4 + 2] - mm.z);
-          s[4 * c4 + 3] = exp2_approx(s[4 * c4 + 3] - mm.w);
-        }
+          if (4 * c4 < nr) {
+            const float4 m4 = mr4[c4];
+            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-        for (int c = 0; c < NCOL; ++c) {
-          const uint32_t off = static_cast<uint32_t>(c) * 128u +
-                               (static_cast<uint32_t>(((tid & 63) >> 3) ^ (c & 7)) << 4);
-          st_shared_b16(pbase + off, __bfloat16_as_ushort(__float2bfloat16_rn(s[c])));
+            for (int e = 0; e < 4; ++e) {
+              const int c = 4 * c4 + e;
+              s[c] = tok_valid ? s[c] * P.q_scale : -INFINITY;
+              up |= s[c] > mm[e] + kTau;
+            }
+          }
+        }
+        up = softmax_any(up);
+        rescaled = (rescaled & ~(1u << (i & 1))) | (static_cast<uint32_t>(up) << (i & 1));
+        if (up) {
+          // exact tile maximum per row: warp transpose-reduction, then across the 4 warps
+          red[warp * NCOL + lane] = xpose_reduce<0, NCOL, true>(s, lane);
+          if constexpr (NCOL == 64) red[warp * NCOL + 32 + lane] = xpose_reduce<32, NCOL, true>(s, lane);
+          named_sync_softmax();
+          if (warp == 0) {
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+              const int c = lane + 32 * h;
+              const float tm = fmaxf(fmaxf(red[c], red[NCOL + c]), fmaxf(red[2 * NCOL + c], red[3 * NCOL + c]));
+              const float mo = mref[c];
+              const float mn = fmaxf(mo, tm);
+              alpha[(i & 1) * NCOL + c] = (mo == -INFINITY) ? 0.f : exp2_approx(mo - mn);
+              mref[c] = mn;
+            }
+          }
+          named_sync_softmax();
+          const float4* al4 = reinterpret_cast<const float4*>(alpha + (i & 1) * NCOL);
+#pragma unroll
+          for (int c4 = 0; c4 < NCOL / 4; ++c4) {
+            if (4 * c4 < nr) {
+              const float4 a = al4[c4];
+              lsum[4 * c4 + 0] *= a.x;
+              lsum[4 * c4 + 1] *= a.y;
+              lsum[4 * c4 + 2] *= a.z;
+              lsum[4 * c4 + 3] *= a.w;
+            }
+          }
+        }
+
+        // P^T = 2^(s - mref), bf16, into the K-major swizzled B operand of the PV product
+        const uint32_t pbase = base + C::OFF_P + static_cast<uint32_t>(i & 1) * C::P_BYTES +
+                               static_cast<uint32_t>(tid >> 6) * (NCOL * 128) + static_cast<uint32_t>((tid & 7) << 1);
+#pragma unroll
+        for (int c4 = 0; c4 < NCOL / 4; ++c4) {
+          if (4 * c4 < nr) {
+            const float4 m4 = mr4[c4];
+            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = 4 * c4 + e;
+              const float pv = exp2_approx(s[c] - mm[e]);
+              lsum[c] += pv;
+              const uint32_t off = static_cast<uint32_t>(c) * 128u +
+                                   (static_cast<uint32_t>(((tid & 63) >> 3) ^ (c & 7)) << 4);
+              st_shared_b16(pbase + off, __bfloat16_as_ushort(__float2bfloat16_rn(pv)));
+            }
+          }
         }
         fence_proxy_async();
         mbar_arrive(PFULL + 8u * (i & 1));
 
-        // per-warp running denominators (lane = row), rescaled like the value sum
-        {
-          const float ts0 = xpose_reduce<0, NCOL, false>(s, lane);
-          l_w[0] = l_w[0] * alpha[(i & 1) * NCOL + lane] + ts0;
-          if constexpr (NCOL == 64) {
-            const float ts1 = xpose_reduce<32, NCOL, false>(s, lane);
-            l_w[NH - 1] = l_w[NH - 1] * alpha[(i & 1) * NCOL + 32 + lane] + ts1;
-          }
-        }
         if (t > 0 && !accumulate(i - 1)) {
           ok = false;
           break;
@@ -560,15 +615,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
       }
       if (!ok || !accumulate(i - 1)) break;
 
-      // segment state: m (warp 0 lanes), l (sum of the per-warp partials), a = acc
-#pragma unroll
-      for (int h = 0; h < NH; ++h) red[warp * NCOL + 32 * h + lane] = l_w[h];
+      // segment state: m = mref, l = sum over threads of lsum, a = acc
+      red[warp * NCOL + lane] = xpose_reduce<0, NCOL, false>(lsum, lane);
+      if constexpr (NCOL == 64) red[warp * NCOL + 32 + lane] = xpose_reduce<32, NCOL, false>(lsum, lane);
       named_sync_softmax();
       if (warp == 0) {
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
           const int c = lane + 32 * h;
-          fin[c] = m_run[h];
+          fin[c] = mref[c];
           fin[NCOL + c] = red[c] + red[NCOL + c] + red[2 * NCOL + c] + red[3 * NCOL + c];
         }
       }
@@ -588,7 +643,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
           *ap = a;
         }
       }
-      named_sync_softmax();  // every thread has read the old headers
+      named_sync_softmax();  // every thread has read the old headers (and fin)
       if (tid < nr) {
         RowState* hp = P.ws_h + srow0 + tid;
         const RowState old = *hp;

@@ -20,6 +20,7 @@ STATUS_NAMES = {0: "SVX_OK", 1: "SVX_ERR_INVALID_ARG", 2: "SVX_ERR_BAD_STATE", 3
                 4: "SVX_ERR_CUDA", 5: "SVX_ERR_TIMEOUT", 6: "SVX_ERR_UNSUPPORTED"}
 FLAG_TIMING = 1
 FLAG_NO_TENSOR_CORES = 2
+FLAG_ZERO_COPY = 4
 
 
 class SvxError(RuntimeError):
@@ -33,7 +34,7 @@ class Config(ctypes.Structure):
     _fields_ = [("max_req", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("max_query", ctypes.c_int32), ("max_chunk_tokens", ctypes.c_int32),
                 ("n_slots", ctypes.c_int32), ("device", ctypes.c_int32), ("compute_stream", ctypes.c_void_p),
-                ("copy_stream", ctypes.c_void_p), ("flags", ctypes.c_uint32)]
+                ("copy_stream", ctypes.c_void_p), ("flags", ctypes.c_uint32), ("zero_copy_ctas", ctypes.c_int32)]
 
 
 class Part(ctypes.Structure):
@@ -46,7 +47,12 @@ class Stats(ctypes.Structure):
                 ("chunk_kernel_ms", ctypes.c_double), ("cand_kernel_ms", ctypes.c_double),
                 ("finish_kernel_ms", ctypes.c_double), ("h2d_bytes", ctypes.c_int64),
                 ("device_bytes", ctypes.c_int64), ("n_chunk_launches", ctypes.c_int32),
-                ("n_copies", ctypes.c_int32)]
+                ("n_copies", ctypes.c_int32), ("chunk_kernel_exposed_ms", ctypes.c_double)]
+
+
+class TierState(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int64), ("C", ctypes.c_int64), ("L", ctypes.c_int64), ("pending", ctypes.c_int64),
+                ("event", ctypes.c_void_p)]
 
 
 class PlanEntry(ctypes.Structure):
@@ -78,6 +84,18 @@ _SIGS = {
                                          ctypes.c_int32, _P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(_P),
                                          ctypes.POINTER(_P), _P, _P, ctypes.POINTER(ctypes.c_int32), ctypes.c_float,
                                          _P, _P, _P]),
+    "svx_migration_endpoint": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                              ctypes.POINTER(ctypes.c_int64)]),
+    "svx_tier_round": (ctypes.c_int, [ctypes.POINTER(TierState), ctypes.c_int64, ctypes.c_int64]),
+    "svx_tier_plan": (ctypes.c_int, [ctypes.POINTER(TierState), ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
+    "svx_tier_complete": (ctypes.c_int, [ctypes.POINTER(TierState)]),
+    "svx_tier_commit": (ctypes.c_int, [ctypes.POINTER(TierState), ctypes.c_int64, ctypes.POINTER(ctypes.c_int64),
+                                       ctypes.POINTER(ctypes.c_int64)]),
+    "svx_tier_migrate": (ctypes.c_int, [ctypes.POINTER(TierState), ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                        _P, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_int64)]),
+    "svx_tier_poll": (ctypes.c_int, [ctypes.POINTER(TierState), ctypes.POINTER(ctypes.c_int32)]),
+    "svx_tier_release": (ctypes.c_int, [ctypes.POINTER(TierState)]),
     "svx_version": (ctypes.c_char_p, []),
 }
 
@@ -146,6 +164,75 @@ def check_coverage(hist_len: Sequence[int], parts: Sequence[tuple]) -> bool:
     return bool(ok.value)
 
 
+# ------------------------------------------------------------ commit-aware tiering
+
+
+def migration_endpoint(H: int, C: int, T: int, g: int) -> int:
+    E = ctypes.c_int64(0)
+    st = lib.svx_migration_endpoint(H, C, T, g, ctypes.byref(E))
+    if st != OK:
+        raise SvxError(st, "svx_migration_endpoint: invalid arguments")
+    return E.value
+
+
+class Tier:
+    """One request's Sealed History / Active Tail / Speculative Frontier boundaries."""
+
+    def __init__(self, H: int = 0, C: int = 0, L: int = 0):
+        self.s = TierState(H, C, L, -1, None)
+
+    def _call(self, fn, *args):
+        st = fn(ctypes.byref(self.s), *args)
+        if st != OK:
+            raise SvxError(st, fn.__name__)
+
+    @property
+    def H(self):
+        return self.s.H
+
+    @property
+    def C(self):
+        return self.s.C
+
+    @property
+    def L(self):
+        return self.s.L
+
+    @property
+    def pending(self):
+        return None if self.s.pending < 0 else self.s.pending
+
+    def round(self, C: int, L: int):
+        self._call(lib.svx_tier_round, C, L)
+
+    def plan(self, T: int, g: int):
+        b, e = ctypes.c_int64(0), ctypes.c_int64(0)
+        self._call(lib.svx_tier_plan, T, g, ctypes.byref(b), ctypes.byref(e))
+        return (b.value, e.value) if e.value > b.value else None
+
+    def complete(self):
+        self._call(lib.svx_tier_complete)
+
+    def commit(self, C_new: int):
+        b, e = ctypes.c_int64(0), ctypes.c_int64(0)
+        self._call(lib.svx_tier_commit, C_new, ctypes.byref(b), ctypes.byref(e))
+        return b.value, e.value
+
+    def migrate(self, T: int, g: int, row_bytes: int, k_dev_at_H, v_dev_at_H, k_host, v_host, stream=None) -> int:
+        E = ctypes.c_int64(0)
+        self._call(lib.svx_tier_migrate, T, g, row_bytes, _ptr(k_dev_at_H), _ptr(v_dev_at_H), _ptr(k_host),
+                   _ptr(v_host), _stream_handle(stream), ctypes.byref(E))
+        return E.value
+
+    def poll(self) -> bool:
+        d = ctypes.c_int32(0)
+        self._call(lib.svx_tier_poll, ctypes.byref(d))
+        return bool(d.value)
+
+    def release(self):
+        self._call(lib.svx_tier_release)
+
+
 # ------------------------------------------------------------ a round that allocates nothing
 
 
@@ -200,11 +287,13 @@ class Verifier:
 
     def __init__(self, max_req: int, n_q_heads: int, n_kv_heads: int, head_dim: int, max_query: int,
                  max_chunk_tokens: int, n_slots: int = 2, device: int = 0, compute_stream=None, copy_stream=None,
-                 timing: bool = False, tensor_cores: bool = True):
+                 timing: bool = False, tensor_cores: bool = True, zero_copy: bool = False,
+                 zero_copy_ctas: int = 0):
         self._keep = (compute_stream, copy_stream)
-        flags = (FLAG_TIMING if timing else 0) | (0 if tensor_cores else FLAG_NO_TENSOR_CORES)
+        flags = ((FLAG_TIMING if timing else 0) | (0 if tensor_cores else FLAG_NO_TENSOR_CORES)
+                 | (FLAG_ZERO_COPY if zero_copy else 0))
         cfg = Config(max_req, n_q_heads, n_kv_heads, head_dim, max_query, max_chunk_tokens, n_slots, device,
-                     _stream_handle(compute_stream), _stream_handle(copy_stream), flags)
+                     _stream_handle(compute_stream), _stream_handle(copy_stream), flags, zero_copy_ctas)
         h = ctypes.c_void_p(None)
         st = lib.svx_create(ctypes.byref(cfg), ctypes.byref(h))
         if st != OK:

@@ -124,3 +124,35 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError):
         spec.loader.exec_module(mod)
+
+
+def test_tiering_matches_oracle(svx):
+    from oracle.tiering import TierState, migration_endpoint
+    rng = np.random.default_rng(5)
+    for _ in range(3000):
+        g = int(rng.choice([1, 16, 128]))
+        T = int(rng.integers(0, 1024))
+        H = g * int(rng.integers(0, 50))
+        C = H + int(rng.integers(0, 3000))
+        assert svx.migration_endpoint(H, C, T, g) == migration_endpoint(H, C, T, g)
+    with pytest.raises(svx.SvxError):
+        svx.migration_endpoint(3, 10, 5, 2)
+    for trial in range(100):
+        T, g = int(rng.integers(0, 600)), int(rng.choice([32, 128]))
+        a, o = svx.Tier(), TierState()
+        for _ in range(50):
+            k = int(rng.integers(1, 9))
+            a.round(a.C, a.C + k)
+            o.round(o.C, o.C + k)
+            assert a.plan(T, g) == o.plan(T, g)
+            if rng.random() < 0.6:
+                a.complete()
+                o.copy_completed()
+            acc = int(rng.integers(0, k + 1))
+            assert a.commit(a.C + acc) == o.commit(o.C + acc)
+            assert (a.H, a.C, a.L, a.pending) == (o.H, o.C, o.L, o.pending)
+    t = svx.Tier()
+    t.round(10, 15)
+    for bad in (lambda: t.round(9, 15), lambda: t.commit(16), lambda: t.commit(9)):
+        with pytest.raises(svx.SvxError):
+            bad()

@@ -194,3 +194,60 @@ def test_full_size_sampled(svx, name):
     rows = sample_rows(w, 24)
     ref = oracle_out(w, x, rows=rows)
     check_parity(o, l, *ref, rows=rows)
+
+
+def test_full_depth_rounds_back_to_back_with_prefetch(svx):
+    """36 layer rounds enqueued without any host wait (finish with timeout 0), so each layer's
+    chunk copies queue behind the previous layer's: cross-layer prefetch through the slot events.
+    Inputs come from the device-side generator and are read back from pinned host memory for the
+    oracle.  Sampled rows of the first, a middle and the last layer are checked."""
+    import torch
+    w = W.named("fulldepth").with_(hist_len=(4096, 3000), chunk_tokens=1024)
+    bf = torch.bfloat16
+    layers = []
+    for l in range(w.n_layers):
+        kh = [torch.empty((C, w.n_kv_heads, w.head_dim), dtype=bf, pin_memory=True) for C in w.hist_len]
+        vh = [torch.empty((C, w.n_kv_heads, w.head_dim), dtype=bf, pin_memory=True) for C in w.hist_len]
+        q, _, _, kc, vc, parent = W.layer_inputs_device(w, l, "cuda", hist_out_k=kh, hist_out_v=vh)
+        o = torch.empty((w.n_req, w.n_q_heads, w.n_query, w.head_dim), dtype=bf, device="cuda")
+        lse = torch.empty((w.n_req, w.n_q_heads, w.n_query), dtype=torch.float32, device="cuda")
+        layers.append((q, kh, vh, kc, vc, o, lse))
+    torch.cuda.synchronize()
+    with make_verifier(svx, w, n_slots=3) as v:
+        for q, kh, vh, kc, vc, o, lse in layers:
+            v.run_round(q, w.hist_len, kh, vh, w.chunk_tokens, o, lse, cand_k=kc, cand_v=vc)
+        torch.cuda.synchronize()
+    u16 = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
+    for l in (0, 17, 35):
+        q, kh, vh, kc, vc, o, lse = layers[l]
+        x = W.LayerInputs(u16(q), [u16(k) for k in kh], [u16(v_) for v_ in vh], u16(kc), u16(vc), None)
+        rows = sample_rows(w, 12, seed=l)
+        o_gpu = o.float().cpu().numpy().astype(np.float64)
+        l_gpu = lse.cpu().numpy().astype(np.float64)
+        check_parity(o_gpu, l_gpu, *oracle_out(w, x, rows=rows), rows=rows)
+
+
+ZC = [SMALL[0], SMALL[1], SMALL[3], SMALL[8]]
+
+
+@pytest.mark.parametrize("w", ZC, ids=[w.name for w in ZC])
+@pytest.mark.parametrize("cap", [0, 8])
+def test_zero_copy_reads_host_history_in_place(svx, w, cap):
+    """SVX_FLAG_ZERO_COPY: pinned host parts go to the chunk kernel without a staging copy, on at
+    most `cap` CTAs (0 = all SMs); whole-history parts exceed max_chunk_tokens on purpose."""
+    x, t = gpu_inputs(w)
+    with make_verifier(svx, w, zero_copy=True, zero_copy_ctas=cap, timing=True) as v:
+        o, l = run_gpu(v, w, t, x, chunk_order=None)
+        st = v.stats()
+        assert st["n_copies"] == 0 and st["h2d_bytes"] == w.hist_bytes
+        # whole histories in one push each
+        import torch
+        o2 = torch.empty((w.n_req, w.n_q_heads, w.n_query, w.head_dim), dtype=torch.bfloat16, device="cuda")
+        l2 = torch.empty((w.n_req, w.n_q_heads, w.n_query), dtype=torch.float32, device="cuda")
+        v.round_begin(t["q"], w.hist_len)
+        v.candidate_attn(t["kc"], t["vc"], x.parent)
+        v.push_chunk([(b, 0, t["kh"][b], t["vh"][b]) for b in range(w.n_req) if w.hist_len[b]])
+        v.round_finish(o2, l2, timeout_ms=60000)
+    ref = oracle_out(w, x)
+    check_parity(o, l, *ref)
+    check_parity(o2.float().cpu().numpy().astype(np.float64), l2.cpu().numpy().astype(np.float64), *ref)

@@ -221,3 +221,46 @@ def layer_inputs(w: Workload, layer: int = 0, hist_alloc: Alloc = _np_alloc,
     k_cand = _normal_bf16(np.random.default_rng([w.seed, layer, _T_KC, 0]), (B, w.n_cand, Hkv, d), scale=ks)
     v_cand = _normal_bf16(np.random.default_rng([w.seed, layer, _T_VC, 0]), (B, w.n_cand, Hkv, d))
     return LayerInputs(q, k_hist, v_hist, k_cand, v_cand, tree_parents(w))
+
+
+# ---------------------------------------------------------------- fast device-side draws
+
+def layer_inputs_device(w: Workload, layer: int, device, hist_out_k=None, hist_out_v=None):
+    """Draw one layer with torch's seeded device generator (Philox) instead of numpy.
+
+    For the multi-GiB full-depth workload, where numpy would take minutes.  Values
+    are float32 standard normals (times the per-KV-head key factor) rounded to
+    bf16 by torch (round-to-nearest-even), the same recipe as ``layer_inputs``
+    with a different random stream.  Returns torch tensors on ``device``; if
+    ``hist_out_k[b]`` / ``hist_out_v[b]`` are given (e.g. pinned host tensors of
+    shape [C_b][H_kv][d], bf16) the history is written there instead and those
+    tensors are returned.  Parents (token trees) come from the numpy recipe.
+    """
+    import torch
+    B, Hq, Hkv, d, nq = w.n_req, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_query
+    g = torch.Generator(device=device)
+    ks = key_head_scale(w)
+    kscale = None if ks is None else torch.from_numpy(ks).to(device).view(1, Hkv, 1)
+
+    def draw(shape, tid, b, scale=None):
+        g.manual_seed(((w.seed * 1000003 + layer) * 16 + tid) * 4099 + b)
+        x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        if scale is not None:
+            x = x * scale
+        return x.to(torch.bfloat16)
+
+    q = draw((B, Hq, nq, d), _T_Q, 0)
+    k_hist, v_hist = [], []
+    for b in range(B):
+        C = w.hist_len[b]
+        kk = draw((C, Hkv, d), _T_KH, b, kscale)
+        vv = draw((C, Hkv, d), _T_VH, b)
+        if hist_out_k is not None:
+            hist_out_k[b].copy_(kk)
+            hist_out_v[b].copy_(vv)
+            kk, vv = hist_out_k[b], hist_out_v[b]
+        k_hist.append(kk)
+        v_hist.append(vv)
+    k_cand = draw((B, w.n_cand, Hkv, d), _T_KC, 0, None if kscale is None else kscale.view(1, 1, Hkv, 1))
+    v_cand = draw((B, w.n_cand, Hkv, d), _T_VC, 0)
+    return q, k_hist, v_hist, k_cand, v_cand, tree_parents(w)
