@@ -267,6 +267,71 @@ svx_status svx_tier_poll(svx_tier_state* s, int32_t* done);
 /* Waits for a migration in flight, advances H and frees its event. */
 svx_status svx_tier_release(svx_tier_state* s);
 
+/* ---- Target-priority admission of Draft steps (host-side decisions) ------------------------ */
+
+/* Section 4.3: a Draft step may start under the selected allocation only if the estimated Target
+ * latency increase is within budget and the estimated Draft step time plus a margin fits the
+ * remaining window; one step per request at a time; instructions expire; ACKs close steps; the
+ * estimates follow observations (x <- x + ema * (observed - x)). */
+typedef struct {
+  double eps_target;    /* acceptable relative Target latency increase, eps_T >= 0 */
+  double delta;         /* time margin for execution variability (same unit as all times) */
+  double ema;           /* weight of the newest observation, (0, 1] */
+  double t_draft;       /* offline Draft single-step time under the allocation, t_D(x, n0) */
+  double delta_target;  /* offline relative Target latency increase under it, Delta_T(x, n0) */
+  int32_t alloc;        /* the allocation n0 (e.g. TPCs or SMs given to the Draft) */
+} svx_sched_config;
+
+typedef struct svx_sched_s* svx_sched;
+
+/* A scheduling instruction: t_latest = t0 + S_hat - t_D_hat - delta. */
+typedef struct {
+  int64_t req;
+  int64_t round;
+  int64_t seq;
+  int32_t alloc;
+  double t_latest;
+} svx_draft_instr;
+
+svx_status svx_sched_create(const svx_sched_config* cfg, svx_sched* out);
+svx_status svx_sched_destroy(svx_sched s);
+/* A new verification round: a pause ends once the latency estimate is back within budget. */
+svx_status svx_sched_new_round(svx_sched s);
+/* At time `now` with remaining window S_hat (`window`): *admitted = 1 and *out filled if a Draft step
+ * for `req` may start, else 0 (paused, a step already unfinished, or a rule fails). */
+svx_status svx_sched_try_admit(svx_sched s, int64_t req, int64_t round, double now, double window,
+                               svx_draft_instr* out, int32_t* admitted);
+/* Draft side, before starting: *ok = 1 iff the instruction matches the current request and round and
+ * t_latest has not passed.  A rejected instruction is dropped (its request may be scheduled again). */
+svx_status svx_sched_check_start(svx_sched s, const svx_draft_instr* ins, int64_t cur_req, int64_t cur_round,
+                                 double now, int32_t* ok);
+/* ACK of a finished step with its observed duration: *accepted = 1 if it closed the request's step. */
+svx_status svx_sched_ack(svx_sched s, int64_t req, int64_t seq, double t_draft_observed, int32_t* accepted);
+/* Observed Target latency with and without co-execution; over budget pauses new submissions. */
+svx_status svx_sched_observe_target(svx_sched s, double t_co, double t_alone);
+/* Current estimates t_D_hat, Delta_T_hat and the pause flag. */
+svx_status svx_sched_estimates(svx_sched s, double* t_draft, double* delta_target, int32_t* paused);
+
+/* ---- I/O-aware dynamic verification width (host-side controller) ---------------------------- */
+
+/* Section 4.2: the next round's width is argmin over the candidate widths of the estimated round time
+ * over the estimated committed tokens.  Round time = Draft generation + max(history transfer, attention)
+ * + rejection correction (overlapped time counted once); every term and the committed count are moving
+ * averages (weight ema on the newest round).  Each width is first tried n_init times, in the given
+ * order; afterwards the width changes only if the best estimate beats the current width's by more than
+ * `threshold` (relative); ties go to the earlier width. */
+typedef struct svx_width_s* svx_width;
+svx_status svx_width_create(const int32_t* widths, int32_t n, double ema, double threshold, int32_t n_init,
+                            svx_width* out);
+svx_status svx_width_destroy(svx_width w);
+/* End-of-round statistics of a round verified at width q (q must be one of the widths). */
+svx_status svx_width_record(svx_width w, int32_t q, double t_draft, double t_h2d, double t_attn, double t_correct,
+                            double committed);
+/* Width for the next round. */
+svx_status svx_width_next(svx_width w, int32_t* q_out);
+/* Current estimate T_round_hat(q) / U_hat(q), or -1 without records. */
+svx_status svx_width_cost(svx_width w, int32_t q, double* cost_out);
+
 /* Library version string. */
 const char* svx_version(void);
 

@@ -17,9 +17,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsvx.so")
 
-SOURCES = ["svx_kernels.cu", "svx_tc_kernel.cu", "svx_runtime.cu", "svx_static.cu", "svx_tier.cu"]
+SOURCES = ["svx_kernels.cu", "svx_tc_kernel.cu", "svx_runtime.cu", "svx_static.cu", "svx_tier.cu", "svx_sched.cu", "svx_width.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
+         "-Xcompiler", "-ffp-contract=off",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 
 

@@ -99,6 +99,7 @@ cudaError_t launch_finish(const FinishParams& p, int head_dim, cudaStream_t stre
 // Tensor-core chunk kernel (d = 128, rows per (part, head) block padded to ncol = 32 or 64).
 bool tc_supported(int head_dim, int rows);
 int tc_ncol(int rows);
+int tc_nwg(int ncol);  // softmax warpgroups; each CTA segment of a pair uses that many state slots
 int tc_max_ctas(int num_sms);
 cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int ncol, int n_ctas, cudaStream_t stream);
 

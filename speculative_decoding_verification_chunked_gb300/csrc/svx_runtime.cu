@@ -454,11 +454,13 @@ svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, int cta_cap) {
       p.total_tiles = T;
       int64_t ctas = std::min<int64_t>(svx::tc_max_ctas(c->num_sms), T);
       if (cta_cap > 0) ctas = std::min<int64_t>(ctas, cta_cap);
-      while (ctas > 1 && max_segments(pair_first, pair_tiles, ctas, T) > svx::kHistSlots) --ctas;
-      const int64_t segs = max_segments(pair_first, pair_tiles, ctas, T);
+      // every CTA segment of a pair writes nwg state slots (one per softmax warpgroup)
+      const int nwg = svx::tc_nwg(ncol);
+      while (ctas > 1 && max_segments(pair_first, pair_tiles, ctas, T) * nwg > svx::kHistSlots) --ctas;
+      const int64_t slots = max_segments(pair_first, pair_tiles, ctas, T) * nwg;
       for (int i = 0; i < n; ++i) {
         uint32_t& used = c->slot_mask[static_cast<size_t>(p.parts[i].req)];
-        used |= (segs >= 32 ? 0xffffffffu : ((1u << segs) - 1u));
+        used |= (slots >= 32 ? 0xffffffffu : ((1u << slots) - 1u));
       }
       SVX_CUDA(c, svx::launch_chunk_attn_tc(p, ncol, static_cast<int>(ctas), c->cs));
     } else {

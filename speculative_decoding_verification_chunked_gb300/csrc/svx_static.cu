@@ -200,9 +200,10 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
         }
         return worst;
       };
-      while (ctas > 1 && segs_for(ctas) > svx::kHistSlots) --ctas;
-      const int64_t segs = segs_for(ctas);
-      for (int i = 0; i < n; ++i) slot_mask[p.parts[i].req] |= (1u << segs) - 1u;
+      const int nwg = svx::tc_nwg(ncol);
+      while (ctas > 1 && segs_for(ctas) * nwg > svx::kHistSlots) --ctas;
+      const int64_t slots = segs_for(ctas) * nwg;
+      for (int i = 0; i < n; ++i) slot_mask[p.parts[i].req] |= (1u << slots) - 1u;
       e = svx::launch_chunk_attn_tc(p, ncol, static_cast<int>(ctas), s);
     } else {
       p.n_rowblk = (R + svx::kRowsPerBlock - 1) / svx::kRowsPerBlock;

@@ -38,7 +38,6 @@ namespace {
 
 constexpr int TOK = kTcTile;  // tokens per tile
 constexpr int D = 128;
-constexpr int NUM_THREADS = 192;
 constexpr int TILE_BYTES = TOK * D * 2;  // one K or V tile, 32 KiB
 constexpr int HALF_BYTES = TOK * 64 * 2; // 64 of the 128 dimensions of a tile, 16 KiB
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -49,18 +48,24 @@ constexpr float kTau = 8.0f;
 
 template <int NCOL>
 struct TcCfg {
+  // Softmax warpgroups.  Two warpgroups taking alternate tiles are supported (each with its own
+  // state slot), but at 320 threads the register cap (168) makes the 32-row form spill and it ran
+  // no faster than one warpgroup (5.64 vs 5.69 TB/s), so one warpgroup is used.
+  static constexpr int NWG = 1;
+  static constexpr int THREADS = 32 * (4 * NWG + 2);
   static constexpr int STAGES = (NCOL == 32) ? 3 : 2;
   static constexpr int Q_BYTES = NCOL * D * 2;
   static constexpr int P_BYTES = NCOL * TOK * 2;
   static constexpr int OFF_KV = 0;
   static constexpr int OFF_Q = STAGES * 2 * TILE_BYTES;
   static constexpr int OFF_P = OFF_Q + Q_BYTES;
-  static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;    // float [4][NCOL]
-  static constexpr int OFF_MNEW = OFF_RED + 4 * NCOL * 4;  // float [NCOL]: running reference max per row
-  static constexpr int OFF_ALPHA = OFF_MNEW + NCOL * 4;  // float [2][NCOL]
-  static constexpr int OFF_FIN = OFF_ALPHA + 2 * NCOL * 4;  // float [2][NCOL]: final m, l
+  // per softmax warpgroup:
+  static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;              // float [NWG][4][NCOL]
+  static constexpr int OFF_MNEW = OFF_RED + NWG * 4 * NCOL * 4;    // float [NWG][NCOL]: reference max per row
+  static constexpr int OFF_ALPHA = OFF_MNEW + NWG * NCOL * 4;      // float [NWG][2][NCOL]
+  static constexpr int OFF_FIN = OFF_ALPHA + NWG * 2 * NCOL * 4;   // float [NWG][2][NCOL]: final m, l
   static constexpr int N_BAR = 2 * STAGES + 10 + 2;
-  static constexpr int OFF_BAR = OFF_FIN + 2 * NCOL * 4;
+  static constexpr int OFF_BAR = OFF_FIN + NWG * 2 * NCOL * 4;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SMEM = BYTES + 1024;  // slack to align the base to 1024 bytes
@@ -106,27 +111,31 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-// Barrier among the 128 softmax threads that also ANDs their flags, so a wait
-// that gave up in one thread makes all of them leave together.
-__device__ __forceinline__ bool softmax_all(bool ok) {
+// Named barriers of the softmax warpgroups: id 1 + wg (its 128 threads), id 3
+// (all softmax threads, at segment starts).
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Barrier that also ANDs the threads' flags, so a wait that gave up in one
+// thread makes all of them leave together.
+__device__ __forceinline__ bool bar_all(uint32_t id, uint32_t n, bool ok) {
   uint32_t r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\t"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(ok))
+      : "r"(static_cast<uint32_t>(ok)), "r"(id), "r"(n)
       : "memory");
   return r != 0;
 }
-// Barrier among the 128 softmax threads that ORs their flags.
-__device__ __forceinline__ bool softmax_any(bool v) {
+// Barrier that ORs the threads' flags.
+__device__ __forceinline__ bool bar_any(uint32_t id, uint32_t n, bool v) {
   uint32_t r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\t"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(v))
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
       : "memory");
   return r != 0;
 }
@@ -291,7 +300,7 @@ struct Waiter {
 };
 
 template <int NCOL>
-__global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_constant__ ChunkParams P) {
+__global__ void __launch_bounds__(TcCfg<NCOL>::THREADS, 1) chunk_attn_tc(const __grid_constant__ ChunkParams P) {
   using C = TcCfg<NCOL>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -321,7 +330,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
       mbar_init(OFULL + 8u * b, 1);
       mbar_init(OEMPTY + 8u * b, 128);
     }
-    mbar_init(QFULL, 128);
+    mbar_init(QFULL, 128 * C::NWG);
     mbar_init(DRAIN, 1);
     misc[1] = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -339,7 +348,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
   const int64_t x_end = cta_tile_begin(blockIdx.x + 1, gridDim.x, T);
   const int64_t kv_stride = static_cast<int64_t>(P.n_kv_heads) * D;
 
-  if (warp == 4) {
+  if (warp == 4 * C::NWG) {
     // ---------------- producer: K/V tiles into the stage ring
     int hint = 0;
     int64_t i = 0;
@@ -382,7 +391,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
       x += sg.n_tiles;
     }
     cp_async_wait_all();
-  } else if (warp == 5) {
+  } else if (warp == 4 * C::NWG + 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc(128, NCOL, false, false);
@@ -415,8 +424,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
         if (!W.wait(QFULL, seg_idx & 1u)) break;
         tc_fence_after();
         if (!issue_s(i)) break;
+        if (C::NWG == 2 && sg.n_tiles > 1 && !issue_s(i + 1)) break;  // each warpgroup's first tile
         for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
-          if (t + 1 < sg.n_tiles && !issue_s(i + 1)) {
+          // one softmax warpgroup: S of the next tile goes out before this tile's PV
+          if (C::NWG == 1 && t + 1 < sg.n_tiles && !issue_s(i + 1)) {
             ok = false;
             break;
           }
@@ -444,6 +455,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
           }
           mma_commit(OFULL + 8u * (i & 1));
           mma_commit(EMPTY + 8u * stage);
+          // two warpgroups: the tile after next uses this tile's S buffer, free since P_i was written
+          if (C::NWG == 2 && t + 2 < sg.n_tiles && !issue_s(i + 2)) {
+            ok = false;
+            break;
+          }
         }
         x += sg.n_tiles;
       }
@@ -453,30 +469,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
     }
     __syncwarp();
   } else {
-    // ---------------- softmax and accumulation (warps 0-3)
-    const int tid = threadIdx.x;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // ---------------- softmax and accumulation (warpgroup wg = warp / 4).  With two warpgroups,
+    // wg takes the tiles i with i % 2 == wg (always TMEM/P buffer wg) and keeps its own online-
+    // softmax state; each writes its own state slot and the finish kernel merges them (Eq. 8).
+    constexpr int NWG = C::NWG;
+    const int wg = warp >> 2;
+    const int tid = threadIdx.x & 127;  // = TMEM lane = token of the S tile = output dimension
+    const uint32_t bar_wg = 1u + static_cast<uint32_t>(wg);
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     constexpr int NH = NCOL / 32;  // columns per lane after a transpose-reduction
     float acc[NCOL];   // O^T accumulator: output dimension tid, query row c
     float s[NCOL];     // scores of token tid, then p, then O^T tile values
     float lsum[NCOL];  // this thread's share of each row's denominator (relative to mref)
-    uint32_t rescaled = 0u;  // bit b: the tile in buffer b re-based the row maxima
-    float* mref = mnew;  // running reference maximum per row, shared by the 128 threads
+    uint32_t rescaled = 0u;  // bit k: the tile with alpha buffer k re-based the row maxima
+    float* red_w = red + wg * 4 * NCOL;
+    float* mref = mnew + wg * NCOL;  // running reference maximum per row, shared by the warpgroup
+    float* alpha_w = alpha + wg * 2 * NCOL;
+    float* fin_w = fin + wg * 2 * NCOL;
     int hint = 0;
     int64_t i = 0;
     bool ok = true;
     int nr = NCOL;
+    auto abuf = [](int64_t j) { return static_cast<int>((NWG == 2 ? (j >> 1) : j) & 1); };
 
     auto accumulate = [&](int64_t j) -> bool {
-      if (!softmax_all(W.wait(OFULL + 8u * (j & 1), static_cast<uint32_t>(j >> 1) & 1u))) return false;
+      if (!bar_all(bar_wg, 128, W.wait(OFULL + 8u * (j & 1), static_cast<uint32_t>(j >> 1) & 1u))) return false;
       tc_fence_after();
       const uint32_t ta = tmem + lane_base + C::O_COL + static_cast<uint32_t>(j & 1) * NCOL;
       tmem_ld32<0>(ta, s);
       if constexpr (NCOL == 64) tmem_ld32<32>(ta + 32, s);
       tc_fence_before();
       mbar_arrive(OEMPTY + 8u * (j & 1));
-      if ((rescaled >> (j & 1)) & 1u) {
-        const float4* al4 = reinterpret_cast<const float4*>(alpha + (j & 1) * NCOL);
+      if ((rescaled >> abuf(j)) & 1u) {
+        const float4* al4 = reinterpret_cast<const float4*>(alpha_w + abuf(j) * NCOL);
 #pragma unroll
         for (int c4 = 0; c4 < NCOL / 4; ++c4) {
           if (4 * c4 < nr) {
@@ -495,7 +520,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
       return true;
     };
 
-    for (int64_t x = x_begin; x < x_end && ok;) {
+    for (int64_t x = x_begin; x < x_end;) {
+      // all softmax threads meet here: nobody is still reading the previous segment's Q through an
+      // MMA, and a wait that gave up anywhere stops both warpgroups together
+      if (!bar_all(3u, 128u * NWG, ok)) break;
       const Seg sg = seg_at(P, x, x_end, hint);
       const PartDesc& pd = P.parts[sg.part];
       const int b = pd.req;
@@ -506,13 +534,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
           (static_cast<int64_t>(b) * P.n_q_heads + static_cast<int64_t>(sg.g) * P.group) * P.n_query + r0;
 
       // Q rows of the pair into shared memory (K-major, swizzled); padding rows are zero
-      for (int idx = tid; idx < NCOL * 16; idx += 128) {
+      for (int idx = threadIdx.x; idx < NCOL * 16; idx += 128 * NWG) {
         const int c = idx >> 4, ch = idx & 15;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (c < nr) v = *reinterpret_cast<const uint4*>(P.q + (row_base + c) * D + ch * 8);
         st_shared_v4(base + C::OFF_Q + swz_offset(c, ch, NCOL * 128), v);
       }
-      if (warp == 0) {
+      if ((warp & 3) == 0) {
 #pragma unroll
         for (int h = 0; h < NH; ++h) mref[lane + 32 * h] = -INFINITY;
       }
@@ -524,10 +552,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
         acc[c] = 0.f;
         lsum[c] = 0.f;
       }
+      int64_t prev = -1;  // this warpgroup's previous tile in the segment
 
       for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
+        if (NWG == 2 && static_cast<int>(i & 1) != wg) continue;
+        // two warpgroups: this warpgroup's previous O first - its PV read the P buffer that P_i
+        // is about to overwrite, so it must have completed (one warpgroup: see below)
+        if (NWG == 2 && prev >= 0 && !accumulate(prev)) {
+          ok = false;
+          break;
+        }
         const bool tok_valid = (sg.tile0 + t) * TOK + tid < pd.n_tok;
-        if (!softmax_all(W.wait(SFULL + 8u * (i & 1), static_cast<uint32_t>(i >> 1) & 1u))) {
+        if (!bar_all(bar_wg, 128, W.wait(SFULL + 8u * (i & 1), static_cast<uint32_t>(i >> 1) & 1u))) {
           ok = false;
           break;
         }
@@ -554,26 +590,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
             }
           }
         }
-        up = softmax_any(up);
-        rescaled = (rescaled & ~(1u << (i & 1))) | (static_cast<uint32_t>(up) << (i & 1));
+        up = bar_any(bar_wg, 128, up);
+        const int ab = abuf(i);
+        rescaled = (rescaled & ~(1u << ab)) | (static_cast<uint32_t>(up) << ab);
         if (up) {
           // exact tile maximum per row: warp transpose-reduction, then across the 4 warps
-          red[warp * NCOL + lane] = xpose_reduce<0, NCOL, true>(s, lane);
-          if constexpr (NCOL == 64) red[warp * NCOL + 32 + lane] = xpose_reduce<32, NCOL, true>(s, lane);
-          named_sync_softmax();
-          if (warp == 0) {
+          red_w[(warp & 3) * NCOL + lane] = xpose_reduce<0, NCOL, true>(s, lane);
+          if constexpr (NCOL == 64) red_w[(warp & 3) * NCOL + 32 + lane] = xpose_reduce<32, NCOL, true>(s, lane);
+          bar_sync(bar_wg, 128);
+          if ((warp & 3) == 0) {
 #pragma unroll
             for (int h = 0; h < NH; ++h) {
               const int c = lane + 32 * h;
-              const float tm = fmaxf(fmaxf(red[c], red[NCOL + c]), fmaxf(red[2 * NCOL + c], red[3 * NCOL + c]));
+              const float tm =
+                  fmaxf(fmaxf(red_w[c], red_w[NCOL + c]), fmaxf(red_w[2 * NCOL + c], red_w[3 * NCOL + c]));
               const float mo = mref[c];
               const float mn = fmaxf(mo, tm);
-              alpha[(i & 1) * NCOL + c] = (mo == -INFINITY) ? 0.f : exp2_approx(mo - mn);
+              alpha_w[ab * NCOL + c] = (mo == -INFINITY) ? 0.f : exp2_approx(mo - mn);
               mref[c] = mn;
             }
           }
-          named_sync_softmax();
-          const float4* al4 = reinterpret_cast<const float4*>(alpha + (i & 1) * NCOL);
+          bar_sync(bar_wg, 128);
+          const float4* al4 = reinterpret_cast<const float4*>(alpha_w + ab * NCOL);
 #pragma unroll
           for (int c4 = 0; c4 < NCOL / 4; ++c4) {
             if (4 * c4 < nr) {
@@ -608,54 +646,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chunk_attn_tc(const __grid_con
         fence_proxy_async();
         mbar_arrive(PFULL + 8u * (i & 1));
 
-        if (t > 0 && !accumulate(i - 1)) {
+        // one warpgroup: the previous tile's O one step behind, so the MMAs of tile i overlap the
+        // accumulation; P_i's buffer was last read by PV_{i-2}, accumulated one iteration ago
+        if (NWG == 1 && prev >= 0 && !accumulate(prev)) {
           ok = false;
           break;
         }
+        prev = i;
       }
-      if (!ok || !accumulate(i - 1)) break;
-
-      // segment state: m = mref, l = sum over threads of lsum, a = acc
-      red[warp * NCOL + lane] = xpose_reduce<0, NCOL, false>(lsum, lane);
-      if constexpr (NCOL == 64) red[warp * NCOL + 32 + lane] = xpose_reduce<32, NCOL, false>(lsum, lane);
-      named_sync_softmax();
-      if (warp == 0) {
+      if (ok && prev >= 0) ok = accumulate(prev);
+      if (ok && prev >= 0) {
+        // this warpgroup's segment state: m = mref, l = sum over threads of lsum, a = acc
+        red_w[(warp & 3) * NCOL + lane] = xpose_reduce<0, NCOL, false>(lsum, lane);
+        if constexpr (NCOL == 64) red_w[(warp & 3) * NCOL + 32 + lane] = xpose_reduce<32, NCOL, false>(lsum, lane);
+        bar_sync(bar_wg, 128);
+        if ((warp & 3) == 0) {
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const int c = lane + 32 * h;
-          fin[c] = mref[c];
-          fin[NCOL + c] = red[c] + red[NCOL + c] + red[2 * NCOL + c] + red[3 * NCOL + c];
+          for (int h = 0; h < NH; ++h) {
+            const int c = lane + 32 * h;
+            fin_w[c] = mref[c];
+            fin_w[NCOL + c] = red_w[c] + red_w[NCOL + c] + red_w[2 * NCOL + c] + red_w[3 * NCOL + c];
+          }
         }
-      }
-      named_sync_softmax();
-      const int64_t srow0 = static_cast<int64_t>(P.slot_base + sg.slot) * P.slot_stride + row_base;
+        bar_sync(bar_wg, 128);
+        const int64_t srow0 =
+            static_cast<int64_t>(P.slot_base + NWG * sg.slot + wg) * P.slot_stride + row_base;
 #pragma unroll
-      for (int c = 0; c < NCOL; ++c) {
-        if (c < nr) {
-          const RowState old = P.ws_h[srow0 + c];
-          const float m = fin[c];
-          float a = acc[c];
-          float* ap = P.ws_a + (srow0 + c) * D + tid;
+        for (int c = 0; c < NCOL; ++c) {
+          if (c < nr) {
+            const RowState old = P.ws_h[srow0 + c];
+            const float m = fin_w[c];
+            float a = acc[c];
+            float* ap = P.ws_a + (srow0 + c) * D + tid;
+            if (old.epoch == P.epoch) {
+              const float mn = fmaxf(old.m, m);
+              if (mn != -INFINITY) a = *ap * exp2_approx(old.m - mn) + a * exp2_approx(m - mn);
+            }
+            *ap = a;
+          }
+        }
+        bar_sync(bar_wg, 128);  // every thread of the warpgroup has read the old headers (and fin)
+        if (tid < nr) {
+          RowState* hp = P.ws_h + srow0 + tid;
+          const RowState old = *hp;
+          float m = fin_w[tid], l = fin_w[NCOL + tid];
           if (old.epoch == P.epoch) {
             const float mn = fmaxf(old.m, m);
-            if (mn != -INFINITY) a = *ap * exp2_approx(old.m - mn) + a * exp2_approx(m - mn);
+            if (mn != -INFINITY) {
+              l = old.l * exp2_approx(old.m - mn) + l * exp2_approx(m - mn);
+              m = mn;
+            }
           }
-          *ap = a;
+          *hp = RowState{m, l, P.epoch, 0u};
         }
-      }
-      named_sync_softmax();  // every thread has read the old headers (and fin)
-      if (tid < nr) {
-        RowState* hp = P.ws_h + srow0 + tid;
-        const RowState old = *hp;
-        float m = fin[tid], l = fin[NCOL + tid];
-        if (old.epoch == P.epoch) {
-          const float mn = fmaxf(old.m, m);
-          if (mn != -INFINITY) {
-            l = old.l * exp2_approx(old.m - mn) + l * exp2_approx(m - mn);
-            m = mn;
-          }
-        }
-        *hp = RowState{m, l, P.epoch, 0u};
       }
       x += sg.n_tiles;
     }
@@ -679,7 +722,7 @@ cudaError_t launch_tc(const ChunkParams& p, int n_ctas, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  chunk_attn_tc<NCOL><<<n_ctas, NUM_THREADS, C::SMEM, stream>>>(p);
+  chunk_attn_tc<NCOL><<<n_ctas, C::THREADS, C::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -687,6 +730,7 @@ cudaError_t launch_tc(const ChunkParams& p, int n_ctas, cudaStream_t stream) {
 
 bool tc_supported(int head_dim, int rows) { return head_dim == 128 && rows >= 1; }
 int tc_ncol(int rows) { return rows <= 32 ? 32 : 64; }
+int tc_nwg(int ncol) { return ncol == 32 ? TcCfg<32>::NWG : TcCfg<64>::NWG; }
 int tc_max_ctas(int num_sms) { return num_sms; }  // one CTA per SM (shared memory)
 
 cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int ncol, int n_ctas, cudaStream_t stream) {

@@ -55,6 +55,16 @@ class TierState(ctypes.Structure):
                 ("event", ctypes.c_void_p)]
 
 
+class SchedConfig(ctypes.Structure):
+    _fields_ = [("eps_target", ctypes.c_double), ("delta", ctypes.c_double), ("ema", ctypes.c_double),
+                ("t_draft", ctypes.c_double), ("delta_target", ctypes.c_double), ("alloc", ctypes.c_int32)]
+
+
+class DraftInstr(ctypes.Structure):
+    _fields_ = [("req", ctypes.c_int64), ("round", ctypes.c_int64), ("seq", ctypes.c_int64),
+                ("alloc", ctypes.c_int32), ("t_latest", ctypes.c_double)]
+
+
 class PlanEntry(ctypes.Structure):
     _fields_ = [("chunk", ctypes.c_int32), ("slot", ctypes.c_int32), ("req", ctypes.c_int32),
                 ("n_tok", ctypes.c_int32), ("tok_start", ctypes.c_int64)]
@@ -96,6 +106,25 @@ _SIGS = {
                                         _P, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_int64)]),
     "svx_tier_poll": (ctypes.c_int, [ctypes.POINTER(TierState), ctypes.POINTER(ctypes.c_int32)]),
     "svx_tier_release": (ctypes.c_int, [ctypes.POINTER(TierState)]),
+    "svx_sched_create": (ctypes.c_int, [ctypes.POINTER(SchedConfig), ctypes.POINTER(_P)]),
+    "svx_sched_destroy": (ctypes.c_int, [_P]),
+    "svx_sched_new_round": (ctypes.c_int, [_P]),
+    "svx_sched_try_admit": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_double, ctypes.c_double,
+                                           ctypes.POINTER(DraftInstr), ctypes.POINTER(ctypes.c_int32)]),
+    "svx_sched_check_start": (ctypes.c_int, [_P, ctypes.POINTER(DraftInstr), ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_double, ctypes.POINTER(ctypes.c_int32)]),
+    "svx_sched_ack": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
+                                     ctypes.POINTER(ctypes.c_int32)]),
+    "svx_sched_observe_target": (ctypes.c_int, [_P, ctypes.c_double, ctypes.c_double]),
+    "svx_sched_estimates": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_int32)]),
+    "svx_width_create": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_double,
+                                        ctypes.c_double, ctypes.c_int32, ctypes.POINTER(_P)]),
+    "svx_width_destroy": (ctypes.c_int, [_P]),
+    "svx_width_record": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                        ctypes.c_double, ctypes.c_double]),
+    "svx_width_next": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32)]),
+    "svx_width_cost": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(ctypes.c_double)]),
     "svx_version": (ctypes.c_char_p, []),
 }
 
@@ -231,6 +260,92 @@ class Tier:
 
     def release(self):
         self._call(lib.svx_tier_release)
+
+
+# ------------------------------------------------------------ Target-priority admission
+
+
+class Scheduler:
+    """Host-side Draft admission (svx_sched_*)."""
+
+    def __init__(self, eps_target: float, delta: float, ema: float, t_draft: float, delta_target: float,
+                 alloc: int = 0):
+        self._h = ctypes.c_void_p(None)
+        st = lib.svx_sched_create(ctypes.byref(SchedConfig(eps_target, delta, ema, t_draft, delta_target, alloc)),
+                                  ctypes.byref(self._h))
+        if st != OK:
+            raise SvxError(st, "svx_sched_create: invalid configuration")
+
+    def __del__(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib.svx_sched_destroy(self._h)
+            self._h = ctypes.c_void_p(None)
+
+    def new_round(self):
+        lib.svx_sched_new_round(self._h)
+
+    def try_admit(self, req: int, rnd: int, now: float, window: float) -> Optional[DraftInstr]:
+        ins, ok = DraftInstr(), ctypes.c_int32(0)
+        st = lib.svx_sched_try_admit(self._h, req, rnd, now, window, ctypes.byref(ins), ctypes.byref(ok))
+        if st != OK:
+            raise SvxError(st, "svx_sched_try_admit")
+        return ins if ok.value else None
+
+    def check_start(self, ins: DraftInstr, cur_req: int, cur_round: int, now: float) -> bool:
+        ok = ctypes.c_int32(0)
+        lib.svx_sched_check_start(self._h, ctypes.byref(ins), cur_req, cur_round, now, ctypes.byref(ok))
+        return bool(ok.value)
+
+    def ack(self, req: int, seq: int, t_obs: float) -> bool:
+        ok = ctypes.c_int32(0)
+        lib.svx_sched_ack(self._h, req, seq, t_obs, ctypes.byref(ok))
+        return bool(ok.value)
+
+    def observe_target(self, t_co: float, t_alone: float):
+        st = lib.svx_sched_observe_target(self._h, t_co, t_alone)
+        if st != OK:
+            raise SvxError(st, "svx_sched_observe_target")
+
+    def estimates(self):
+        a, b, c = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_int32(0)
+        lib.svx_sched_estimates(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+        return a.value, b.value, bool(c.value)
+
+
+# ------------------------------------------------------------ dynamic verification width
+
+
+class WidthController:
+    """svx_width_*: argmin_q T_round_hat(q) / U_hat(q) with initial sampling and a switching threshold."""
+
+    def __init__(self, widths: Sequence[int], ema: float, threshold: float, n_init: int):
+        arr = (ctypes.c_int32 * len(widths))(*widths)
+        self._h = ctypes.c_void_p(None)
+        st = lib.svx_width_create(arr, len(widths), ema, threshold, n_init, ctypes.byref(self._h))
+        if st != OK:
+            raise SvxError(st, "svx_width_create: invalid configuration")
+
+    def __del__(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib.svx_width_destroy(self._h)
+            self._h = ctypes.c_void_p(None)
+
+    def record(self, q: int, t_draft: float, t_h2d: float, t_attn: float, t_correct: float, committed: float):
+        st = lib.svx_width_record(self._h, q, t_draft, t_h2d, t_attn, t_correct, committed)
+        if st != OK:
+            raise SvxError(st, "svx_width_record: unknown width")
+
+    def next_width(self) -> int:
+        q = ctypes.c_int32(0)
+        lib.svx_width_next(self._h, ctypes.byref(q))
+        return q.value
+
+    def cost(self, q: int) -> Optional[float]:
+        c = ctypes.c_double(0)
+        st = lib.svx_width_cost(self._h, q, ctypes.byref(c))
+        if st != OK:
+            raise SvxError(st, "svx_width_cost: unknown width")
+        return None if c.value < 0 else c.value
 
 
 # ------------------------------------------------------------ a round that allocates nothing

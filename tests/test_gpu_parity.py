@@ -251,3 +251,49 @@ def test_zero_copy_reads_host_history_in_place(svx, w, cap):
     ref = oracle_out(w, x)
     check_parity(o, l, *ref)
     check_parity(o2.float().cpu().numpy().astype(np.float64), l2.cpu().numpy().astype(np.float64), *ref)
+
+
+def test_tiering_migration_feeds_the_next_round(svx):
+    """Commit-aware tiering end to end: Eq. (5) picks [H, E), the history rows move device -> pinned
+    host asynchronously, H advances only once the copy is done, and the next round streams the
+    Sealed History [0, H) from host memory while reading the Active Tail [H, C) in place."""
+    import time as _time
+    import torch
+    w = W.Workload("tier", 2, 8, 2, 128, (1500, 700), 256, 5, seed=50)
+    x, t = gpu_inputs(w, resident=True)
+    row_bytes = w.n_kv_heads * w.head_dim * 2
+    T, g = 512, 128
+    host_k = [torch.zeros_like(k, device="cpu").pin_memory() for k in t["kh"]]
+    host_v = [torch.zeros_like(v, device="cpu").pin_memory() for v in t["vh"]]
+    tiers = []
+    stream = torch.cuda.Stream()
+    for b in range(w.n_req):
+        tr = svx.Tier()
+        C = w.hist_len[b]
+        tr.round(C, C + w.n_query)
+        E = tr.migrate(T, g, row_bytes, t["kh"][b], t["vh"][b], host_k[b], host_v[b], stream=stream)
+        assert E == max(0, g * ((C - T) // g)) and tr.H == 0  # nothing confirmed yet
+        deadline = _time.time() + 30
+        while not tr.poll():
+            assert _time.time() < deadline
+            _time.sleep(0.001)
+        assert tr.H == E and tr.pending is None
+        assert torch.equal(host_k[b][:E], t["kh"][b][:E].cpu()) and torch.equal(host_v[b][:E], t["vh"][b][:E].cpu())
+        tiers.append(tr)
+    o = torch.empty((w.n_req, w.n_q_heads, w.n_query, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.n_req, w.n_q_heads, w.n_query), dtype=torch.float32, device="cuda")
+    with make_verifier(svx, w) as v:
+        v.round_begin(t["q"], w.hist_len)
+        v.candidate_attn(t["kc"], t["vc"], x.parent)
+        for b, tr in enumerate(tiers):  # Sealed History from host, chunk by chunk
+            for t0 in range(0, tr.H, w.chunk_tokens):
+                n = min(w.chunk_tokens, tr.H - t0)
+                v.push_chunk([(b, t0, host_k[b][t0:t0 + n], host_v[b][t0:t0 + n])])
+        v.push_chunk([(b, tr.H, t["kh"][b][tr.H:], t["vh"][b][tr.H:]) for b, tr in enumerate(tiers)])
+        v.round_finish(o, lse, timeout_ms=60000)
+    check_parity(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+                 *oracle_out(w, x))
+    for tr in tiers:  # two of five candidates accepted; the rejected suffix never meets [0, H)
+        C0, L0 = tr.C, tr.L
+        rel = tr.commit(C0 + 2)
+        assert rel == (C0 + 2, L0) and rel[0] >= tr.H and tr.C == tr.L == C0 + 2
