@@ -51,8 +51,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="qwen3", choices=["tiny", "qwen3", "internlm", "tree", "fulldepth"])
     ap.add_argument("--zero-copy-ctas", default="0,32",
                     help="comma list of CTA caps for the zero-copy streamed variant (0 = all SMs; empty = skip)")
-    ap.add_argument("--draft-load", action="store_true",
-                    help="also time the streamed round beside a low-priority bf16 GEMM loop (Target priority)")
+    ap.add_argument("--no-draft-load", dest="draft_load", action="store_false",
+                    help="skip timing the streamed round beside a low-priority bf16 GEMM loop (Target priority)")
     ap.add_argument("--slots", type=int, default=3, choices=[2, 3])
     ap.add_argument("--resident-chunk", default="whole", choices=["whole", "plan"],
                     help="device-resident history pushed as one part per request, or in the plan's chunks")
@@ -442,22 +442,25 @@ def main(argv=None):
             kern = [ev[0].elapsed_time(ev[1]) for st in evs for ev in st]
         return ms, kern
 
-    # link bandwidth of this machine (pinned host -> HBM, one large copy, best of 4)
-    probe_h = layers[0]["kh_h"][0]
-    probe_d = torch.empty_like(probe_h, device=dev)
-    best = 0.0
-    for _ in range(4):
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(xs):
-            e0.record(xs)
-            probe_d.copy_(probe_h, non_blocking=True)
-            e1.record(xs)
-        torch.cuda.synchronize(dev)
-        best = max(best, probe_h.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9)
-    link_gbs = best
-    del probe_d
+    def link_probe():
+        """Pinned host -> HBM bandwidth of this machine now (one 256 MiB copy, best of 4).  The host memory
+        of a GB300 node is shared with other GPUs' jobs, so it is sampled before and after the
+        streamed phase."""
+        probe_h = layers[0]["kh_h"][0]
+        probe_d = torch.empty_like(probe_h, device=dev)
+        best = 0.0
+        for _ in range(4):
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(xs):
+                e0.record(xs)
+                probe_d.copy_(probe_h, non_blocking=True)
+                e1.record(xs)
+            torch.cuda.synchronize(dev)
+            best = max(best, probe_h.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9)
+        return best
 
+    link_before = link_probe()
     steps = a.steps if L == 1 else max(3, a.steps // 30)
     warmup = a.warmup if L == 1 else max(3, min(a.warmup, 5))
     # ---- value: resident history (HBM-bound form)
@@ -471,6 +474,8 @@ def main(argv=None):
 
     # ---- e2e: streamed from pinned host, copies in the timed region
     ms_e2e, _ = timed(e2e_step, steps, warmup)
+    link_after = link_probe()
+    link_gbs = max(link_before, link_after)
     clk.__exit__(None, None, None)
     clocks = clk.summary()
     e2e_value, ms_e2e_job = job_throughput(B * nq, ms_e2e, world, dev)
@@ -624,12 +629,13 @@ def main(argv=None):
                 "d2h_bytes_per_step": int(d2h_step), "ms_per_step": ms_e2e_job},
         "gpu_launches": launches_per_step * steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": profiled_traffic(d),
+                     "frac": achieved / hbm_peak, "traffic": profiled_traffic(d, w.name),
                      "kernel": "chunk_attn_tc" if d == 128 else "chunk_attn_fma",
                      "peak_source": f"{hbm_src} hbm_gbs (burst copy)",
                      "algorithmic_bytes_per_launch": int(k1_bytes_per_launch),
                      "ms_per_launch": k1_ms_per_launch},
         "streamed": {"hist_gb_per_s": hist_bytes / (ms_e2e / 1e3) / 1e9, "link_gbs": link_gbs,
+                     "link_gbs_before_after": [link_before, link_after],
                      "link_frac": hist_bytes / (ms_e2e / 1e3) / 1e9 / link_gbs,
                      "layer_copy_busy_ms": s_copy, "layer_round_ms": s_round, "hidden_frac": hidden,
                      "hidden_frac_round_minus_copy": hidden_bound,
@@ -654,20 +660,21 @@ def main(argv=None):
     return 0
 
 
-def profiled_traffic(d: int):
-    """DRAM bytes per launch of the chunk kernel from the committed ncu summary, if that
-    summary was taken on the kernel source as it is now (else None)."""
+def profiled_traffic(d: int, workload: str):
+    """DRAM bytes per launch of the chunk kernel on this workload from the committed ncu
+    summary, if that summary was taken on the kernel source as it is now (else None)."""
     import hashlib
     name = "chunk_attn_tc" if d == 128 else "chunk_attn_fma"
     src = os.path.join(ROOT, "speculative_decoding_verification_chunked_gb300", "csrc",
                        "svx_tc_kernel.cu" if d == 128 else "svx_kernels.cu")
     summ = os.path.join(ROOT, "profiles", f"{name}_traffic.txt")
     try:
-        kv = dict(line.split(":", 1) for line in open(summ) if ":" in line and not line.startswith("#"))
+        kv = {k.strip(): v.strip() for k, v in
+              (line.split(":", 1) for line in open(summ) if ":" in line and not line.startswith("#"))}
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if kv.get("kernel_source_sha256", "").strip() != digest:
+        if kv.get("kernel_source_sha256", "") != digest:
             return None
-        return float(kv["dram_bytes_per_launch"])
+        return float(kv[f"{workload}.dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         return None
 

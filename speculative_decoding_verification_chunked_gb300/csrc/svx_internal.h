@@ -96,11 +96,13 @@ __host__ __device__ inline int64_t cta_of_tile(int64_t x, int64_t n, int64_t T) 
 cudaError_t launch_chunk_attn(const ChunkParams& p, int head_dim, cudaStream_t stream);
 cudaError_t launch_finish(const FinishParams& p, int head_dim, cudaStream_t stream);
 
-// Tensor-core chunk kernel (d = 128, rows per (part, head) block padded to ncol = 32 or 64).
+// Tensor-core chunk kernel (d = 128).  Modes: 0 one softmax warpgroup (<= 32 query rows per pass),
+// 2 two warpgroups on 32 rows each (<= 64 rows per pass), both reading every K/V tile once.
 bool tc_supported(int head_dim, int rows);
-int tc_ncol(int rows);
-int tc_nwg(int ncol);  // softmax warpgroups; each CTA segment of a pair uses that many state slots
+int tc_mode(int rows);
+int tc_rows_per_pass(int mode);
+int tc_slots_per_segment(int mode);
 int tc_max_ctas(int num_sms);
-cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int ncol, int n_ctas, cudaStream_t stream);
+cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int mode, int n_ctas, cudaStream_t stream);
 
 }  // namespace svx

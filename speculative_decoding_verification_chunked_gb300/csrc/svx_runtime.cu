@@ -438,8 +438,9 @@ svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, int cta_cap) {
     for (int i = 0; i < n; ++i) p.parts[i] = parts[i0 + i];
     if (c->use_tc) {
       // tensor-core kernel: tiles of all (part, head, row block) pairs split evenly over the CTAs
-      const int ncol = svx::tc_ncol(R);
-      p.n_rowblk = (R + ncol - 1) / ncol;
+      const int mode = svx::tc_mode(R);
+      const int rpp = svx::tc_rows_per_pass(mode);
+      p.n_rowblk = (R + rpp - 1) / rpp;
       std::vector<int64_t> pair_first, pair_tiles;
       int64_t T = 0;
       for (int i = 0; i < n; ++i) {
@@ -454,15 +455,15 @@ svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, int cta_cap) {
       p.total_tiles = T;
       int64_t ctas = std::min<int64_t>(svx::tc_max_ctas(c->num_sms), T);
       if (cta_cap > 0) ctas = std::min<int64_t>(ctas, cta_cap);
-      // every CTA segment of a pair writes nwg state slots (one per softmax warpgroup)
-      const int nwg = svx::tc_nwg(ncol);
-      while (ctas > 1 && max_segments(pair_first, pair_tiles, ctas, T) * nwg > svx::kHistSlots) --ctas;
-      const int64_t slots = max_segments(pair_first, pair_tiles, ctas, T) * nwg;
+      // every CTA segment of a pair writes tc_slots_per_segment state slots
+      const int sps = svx::tc_slots_per_segment(mode);
+      while (ctas > 1 && max_segments(pair_first, pair_tiles, ctas, T) * sps > svx::kHistSlots) --ctas;
+      const int64_t slots = max_segments(pair_first, pair_tiles, ctas, T) * sps;
       for (int i = 0; i < n; ++i) {
         uint32_t& used = c->slot_mask[static_cast<size_t>(p.parts[i].req)];
         used |= (slots >= 32 ? 0xffffffffu : ((1u << slots) - 1u));
       }
-      SVX_CUDA(c, svx::launch_chunk_attn_tc(p, ncol, static_cast<int>(ctas), c->cs));
+      SVX_CUDA(c, svx::launch_chunk_attn_tc(p, mode, static_cast<int>(ctas), c->cs));
     } else {
       p.n_rowblk = (R + svx::kRowsPerBlock - 1) / svx::kRowsPerBlock;
       int64_t max_tok = 0;

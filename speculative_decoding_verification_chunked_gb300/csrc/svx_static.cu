@@ -177,17 +177,17 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
     }
     cudaError_t e;
     if (head_dim == 128) {
-      const int ncol = svx::tc_ncol(R);
-      p.n_rowblk = (R + ncol - 1) / ncol;
-      int64_t T = 0, max_nt = 0;
+      const int mode = svx::tc_mode(R);
+      const int rpp = svx::tc_rows_per_pass(mode);
+      p.n_rowblk = (R + rpp - 1) / rpp;
+      int64_t T = 0;
       for (int i = 0; i < n; ++i) {
         const int64_t nt = (static_cast<int64_t>(p.parts[i].n_tok) + svx::kTcTile - 1) / svx::kTcTile;
         p.parts[i].tile_base = T;
         T += nt * n_kv_heads * p.n_rowblk;
-        max_nt = std::max(max_nt, nt);
       }
       p.total_tiles = T;
-      // CTAs such that no (part, head, row block) pair spreads over more than kHistSlots of them
+      // CTAs such that no (part, head, row block) pair spreads over more state slots than there are
       int64_t ctas = std::min<int64_t>(svx::tc_max_ctas(num_sms), T);
       auto segs_for = [&](int64_t c) {
         int64_t worst = 0;
@@ -200,11 +200,11 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
         }
         return worst;
       };
-      const int nwg = svx::tc_nwg(ncol);
-      while (ctas > 1 && segs_for(ctas) * nwg > svx::kHistSlots) --ctas;
-      const int64_t slots = segs_for(ctas) * nwg;
+      const int sps = svx::tc_slots_per_segment(mode);
+      while (ctas > 1 && segs_for(ctas) * sps > svx::kHistSlots) --ctas;
+      const int64_t slots = segs_for(ctas) * sps;
       for (int i = 0; i < n; ++i) slot_mask[p.parts[i].req] |= (1u << slots) - 1u;
-      e = svx::launch_chunk_attn_tc(p, ncol, static_cast<int>(ctas), s);
+      e = svx::launch_chunk_attn_tc(p, mode, static_cast<int>(ctas), s);
     } else {
       p.n_rowblk = (R + svx::kRowsPerBlock - 1) / svx::kRowsPerBlock;
       int64_t max_tok = 0;

@@ -46,34 +46,47 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // bf16 and most tiles need no cross-thread maximum at all.
 constexpr float kTau = 8.0f;
 
-template <int NCOL>
+// Work modes of the kernel.  Every softmax warpgroup owns 32 query rows (NCOL).
+//   kSingle    one warpgroup: up to 32 rows of a (request, KV head) pair per pass.
+//   kRowSplit  two warpgroups on 64 rows, 32 each; both consume every K/V tile, so a tile read
+//              from HBM serves all 64 rows (the token-tree shape: G = 4, 16 nodes).
+enum : int { kSingle = 0, kRowSplit = 2 };
+
+template <int MODE>
 struct TcCfg {
-  // Softmax warpgroups.  Two warpgroups taking alternate tiles are supported (each with its own
-  // state slot), but at 320 threads the register cap (168) makes the 32-row form spill and it ran
-  // no faster than one warpgroup (5.64 vs 5.69 TB/s), so one warpgroup is used.
-  static constexpr int NWG = 1;
+  static constexpr int NCOL = 32;                          // query rows per warpgroup (MMA N)
+  static constexpr int NWG = (MODE == kSingle) ? 1 : 2;   // softmax warpgroups
+  static constexpr int ROWS = (MODE == kRowSplit) ? 2 * NCOL : NCOL;  // query rows per pass
+  static constexpr int NBUF = (MODE == kRowSplit) ? 4 : 2;  // S / O / P buffers: (warpgroup, tile parity)
   static constexpr int THREADS = 32 * (4 * NWG + 2);
-  static constexpr int STAGES = (NCOL == 32) ? 3 : 2;
-  static constexpr int Q_BYTES = NCOL * D * 2;
+  static constexpr int STAGES = 3;
+  static constexpr int Q_BYTES = ROWS * D * 2;
+  // P^T of a tile (one per warpgroup) is written into that tile's own K buffer: K is dead once the
+  // tile's S products have completed, and the stage is recycled only after its PV products.
   static constexpr int P_BYTES = NCOL * TOK * 2;
   static constexpr int OFF_KV = 0;
   static constexpr int OFF_Q = STAGES * 2 * TILE_BYTES;
-  static constexpr int OFF_P = OFF_Q + Q_BYTES;
   // per softmax warpgroup:
-  static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;              // float [NWG][4][NCOL]
+  static constexpr int OFF_RED = OFF_Q + Q_BYTES;                  // float [NWG][4][NCOL]
   static constexpr int OFF_MNEW = OFF_RED + NWG * 4 * NCOL * 4;    // float [NWG][NCOL]: reference max per row
   static constexpr int OFF_ALPHA = OFF_MNEW + NWG * NCOL * 4;      // float [NWG][2][NCOL]
   static constexpr int OFF_FIN = OFF_ALPHA + NWG * 2 * NCOL * 4;   // float [NWG][2][NCOL]: final m, l
-  static constexpr int N_BAR = 2 * STAGES + 10 + 2;
+  static constexpr int N_BAR = 2 * STAGES + 5 * NBUF + 2;
   static constexpr int OFF_BAR = OFF_FIN + NWG * 2 * NCOL * 4;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SMEM = BYTES + 1024;  // slack to align the base to 1024 bytes
-  static constexpr uint32_t TMEM_COLS = (4 * NCOL <= 128) ? 128u : 256u;
-  static constexpr uint32_t S_COL = 0;         // S^T buffers at columns [0, 2*NCOL)
-  static constexpr uint32_t O_COL = 2 * NCOL;  // O^T buffers at [2*NCOL, 4*NCOL)
-  static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0 && P_BYTES % 1024 == 0, "swizzle atoms need 1 KiB alignment");
+  static constexpr uint32_t TMEM_COLS = 2 * NBUF * NCOL;  // S and O buffers: 128 or 256 columns
+  static constexpr uint32_t S_COL = 0;
+  static constexpr uint32_t O_COL = NBUF * NCOL;
+  static_assert(OFF_Q % 1024 == 0 && P_BYTES % 1024 == 0 && (NCOL * D * 2) % 1024 == 0 &&
+                    NWG * P_BYTES <= TILE_BYTES,
+                "swizzle atoms need 1 KiB alignment; the P^T buffers must fit in a K tile");
   static_assert(SMEM <= 232448, "shared memory per CTA");
+  // buffer of warpgroup wg for tile j
+  __device__ static constexpr int buf(int64_t j, int wg) {
+    return (MODE == kRowSplit) ? (wg * 2 + static_cast<int>(j & 1)) : static_cast<int>(j & 1);
+  }
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -299,19 +312,23 @@ struct Waiter {
   }
 };
 
-template <int NCOL>
-__global__ void __launch_bounds__(TcCfg<NCOL>::THREADS, 1) chunk_attn_tc(const __grid_constant__ ChunkParams P) {
-  using C = TcCfg<NCOL>;
+template <int MODE>
+__global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const __grid_constant__ ChunkParams P) {
+  using C = TcCfg<MODE>;
+  constexpr int NCOL = C::NCOL;
+  constexpr int NWG = C::NWG;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // mbarriers: FULL/EMPTY per stage; SFULL, SEMPTY, PFULL, OFULL, OEMPTY per buffer; QFULL; DRAIN
   const uint32_t bar0 = base + C::OFF_BAR;
   const uint32_t FULL = bar0, EMPTY = bar0 + 8u * C::STAGES;
-  const uint32_t SFULL = bar0 + 16u * C::STAGES, SEMPTY = SFULL + 16u, PFULL = SEMPTY + 16u, OFULL = PFULL + 16u,
-                 OEMPTY = OFULL + 16u, QFULL = OEMPTY + 16u, DRAIN = QFULL + 8u;
+  const uint32_t SFULL = bar0 + 16u * C::STAGES, SEMPTY = SFULL + 8u * C::NBUF, PFULL = SEMPTY + 8u * C::NBUF,
+                 OFULL = PFULL + 8u * C::NBUF, OEMPTY = OFULL + 8u * C::NBUF, QFULL = OEMPTY + 8u * C::NBUF,
+                 DRAIN = QFULL + 8u;
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_MISC);
   float* red = reinterpret_cast<float*>(gbase + C::OFF_RED);
   float* mnew = reinterpret_cast<float*>(gbase + C::OFF_MNEW);
@@ -323,14 +340,14 @@ __global__ void __launch_bounds__(TcCfg<NCOL>::THREADS, 1) chunk_attn_tc(const _
       mbar_init(FULL + 8u * s, 32);
       mbar_init(EMPTY + 8u * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::NBUF; ++b) {
       mbar_init(SFULL + 8u * b, 1);
       mbar_init(SEMPTY + 8u * b, 128);
       mbar_init(PFULL + 8u * b, 128);
       mbar_init(OFULL + 8u * b, 1);
       mbar_init(OEMPTY + 8u * b, 128);
     }
-    mbar_init(QFULL, 128 * C::NWG);
+    mbar_init(QFULL, 128 * NWG);
     mbar_init(DRAIN, 1);
     misc[1] = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -348,7 +365,7 @@ __global__ void __launch_bounds__(TcCfg<NCOL>::THREADS, 1) chunk_attn_tc(const _
   const int64_t x_end = cta_tile_begin(blockIdx.x + 1, gridDim.x, T);
   const int64_t kv_stride = static_cast<int64_t>(P.n_kv_heads) * D;
 
-  if (warp == 4 * C::NWG) {
+  if (warp == 4 * NWG) {
     // ---------------- producer: K/V tiles into the stage ring
     int hint = 0;
     int64_t i = 0;
@@ -391,28 +408,60 @@ __global__ void __launch_bounds__(TcCfg<NCOL>::THREADS, 1) chunk_attn_tc(const _
       x += sg.n_tiles;
     }
     cp_async_wait_all();
-  } else if (warp == 4 * C::NWG + 1) {
-    // ---------------- MMA issuer
+  } else if (warp == 4 * NWG + 1) {
+    // ---------------- MMA issuer (one thread)
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc(128, NCOL, false, false);
       constexpr uint32_t idesc_o = make_idesc(128, NCOL, true, false);
+      constexpr int SGROUPS = (MODE == kRowSplit) ? 2 : 1;  // warpgroups served by one tile's MMAs
+      // S^T of tile j for every warpgroup that consumes it: K tile (A, K-major) x Q rows (B, K-major)
       auto issue_s = [&](int64_t j) -> bool {
         const int stage = static_cast<int>(j % C::STAGES);
         const uint32_t use = static_cast<uint32_t>(j / C::STAGES);
         if (!W.wait(FULL + 8u * stage, use & 1u)) return false;
-        if (j >= 2 && !W.wait(SEMPTY + 8u * (j & 1), ((static_cast<uint32_t>(j >> 1)) & 1u) ^ 1u)) return false;
         fence_proxy_async();  // cp.async writes (generic proxy) before tensor-core reads (async proxy)
-        tc_fence_after();
         const uint32_t kaddr = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES;
-        const uint32_t qaddr = base + C::OFF_Q;
-        const uint32_t d = tmem + C::S_COL + static_cast<uint32_t>(j & 1) * NCOL;
+        for (int g2 = 0; g2 < SGROUPS; ++g2) {
+          const int wg = g2;
+          const int bf = C::buf(j, wg);
+          if (j >= 2 && !W.wait(SEMPTY + 8u * bf, ((static_cast<uint32_t>(j >> 1)) & 1u) ^ 1u)) return false;
+          tc_fence_after();
+          const uint32_t qaddr = base + C::OFF_Q + static_cast<uint32_t>((MODE == kRowSplit) ? wg : 0) * (NCOL * D * 2);
+          const uint32_t d = tmem + C::S_COL + static_cast<uint32_t>(bf) * NCOL;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = make_sdesc(kaddr + (kk >> 2) * HALF_BYTES + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = make_sdesc(qaddr + (kk >> 2) * (NCOL * 128) + (kk & 3) * 32, 16, 1024);
-          mma_bf16(d, a, b, idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = make_sdesc(kaddr + (kk >> 2) * HALF_BYTES + (kk & 3) * 32, 16, 1024);
+            const uint64_t b = make_sdesc(qaddr + (kk >> 2) * (NCOL * 128) + (kk & 3) * 32, 16, 1024);
+            mma_bf16(d, a, b, idesc_s, kk > 0 ? 1u : 0u);
+          }
         }
-        mma_commit(SFULL + 8u * (j & 1));
+        // commits after every S product of the tile: a warpgroup writes its P^T into this K tile
+        // once its SFULL fires, so no product may still be reading K then
+        for (int g2 = 0; g2 < SGROUPS; ++g2)
+          mma_commit(SFULL + 8u * C::buf(j, g2));
+        return true;
+      };
+      // O^T of tile j for warpgroup wg: V tile (A, dimension-major) x P^T (B, K-major)
+      auto issue_pv = [&](int64_t j, int wg) -> bool {
+        const int bf = C::buf(j, wg);
+        const uint32_t par = static_cast<uint32_t>(j >> 1) & 1u;
+        if (!W.wait(PFULL + 8u * bf, par)) return false;
+        if (j >= 2 && !W.wait(OEMPTY + 8u * bf, par ^ 1u)) return false;
+        fence_proxy_async();  // P^T was written with ordinary stores
+        tc_fence_after();
+        const int stage = static_cast<int>(j % C::STAGES);
+        const uint32_t vaddr = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES + TILE_BYTES;
+        const uint32_t paddr = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES +
+                               static_cast<uint32_t>((MODE == kRowSplit) ? wg : 0) * C::P_BYTES;
+        const uint32_t d = tmem + C::O_COL + static_cast<uint32_t>(bf) * NCOL;
+#pragma unroll
+        for (int kk = 0; kk < TOK / 16; ++kk) {
+          // A = V^T: 64-dimension halves 16 KiB apart (LBO), 8-token groups 1 KiB apart (SBO)
+          const uint64_t a = make_sdesc(vaddr + kk * 2048, HALF_BYTES, 1024);
+          const uint64_t b = make_sdesc(paddr + (kk >> 2) * (NCOL * 128) + (kk & 3) * 32, 16, 1024);
+          mma_bf16(d, a, b, idesc_o, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(OFULL + 8u * bf);
         return true;
       };
       int hint = 0;
@@ -424,42 +473,23 @@ __global__ void __launch_bounds__(TcCfg<NCOL>::THREADS, 1) chunk_attn_tc(const _
         if (!W.wait(QFULL, seg_idx & 1u)) break;
         tc_fence_after();
         if (!issue_s(i)) break;
-        if (C::NWG == 2 && sg.n_tiles > 1 && !issue_s(i + 1)) break;  // each warpgroup's first tile
         for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
-          // one softmax warpgroup: S of the next tile goes out before this tile's PV
-          if (C::NWG == 1 && t + 1 < sg.n_tiles && !issue_s(i + 1)) {
+          // S of the next tile goes out before this tile's PV (one tile ahead)
+          if (t + 1 < sg.n_tiles && !issue_s(i + 1)) {
             ok = false;
             break;
           }
-          const uint32_t par = static_cast<uint32_t>(i >> 1) & 1u;
-          if (!W.wait(PFULL + 8u * (i & 1), par)) {
-            ok = false;
-            break;
-          }
-          if (i >= 2 && !W.wait(OEMPTY + 8u * (i & 1), par ^ 1u)) {
-            ok = false;
-            break;
-          }
-          fence_proxy_async();  // P^T was written with ordinary stores
-          tc_fence_after();
           const int stage = static_cast<int>(i % C::STAGES);
-          const uint32_t vaddr = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES + TILE_BYTES;
-          const uint32_t paddr = base + C::OFF_P + static_cast<uint32_t>(i & 1) * C::P_BYTES;
-          const uint32_t d = tmem + C::O_COL + static_cast<uint32_t>(i & 1) * NCOL;
-#pragma unroll
-          for (int kk = 0; kk < TOK / 16; ++kk) {
-            // A = V^T: dimension-major (MN-major); 64-dimension halves 16 KiB apart, 8-token groups 1 KiB apart
-            const uint64_t a = make_sdesc(vaddr + kk * 2048, HALF_BYTES, 1024);
-            const uint64_t b = make_sdesc(paddr + (kk >> 2) * (NCOL * 128) + (kk & 3) * 32, 16, 1024);
-            mma_bf16(d, a, b, idesc_o, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(OFULL + 8u * (i & 1));
-          mma_commit(EMPTY + 8u * stage);
-          // two warpgroups: the tile after next uses this tile's S buffer, free since P_i was written
-          if (C::NWG == 2 && t + 2 < sg.n_tiles && !issue_s(i + 2)) {
+          if (MODE == kRowSplit) {
+            if (!issue_pv(i, 0) || !issue_pv(i, 1)) {
+              ok = false;
+              break;
+            }
+          } else if (!issue_pv(i, 0)) {
             ok = false;
             break;
           }
+          mma_commit(EMPTY + 8u * stage);  // both products of this stage are done when this fires
         }
         x += sg.n_tiles;
       }
@@ -469,18 +499,20 @@ __global__ void __launch_bounds__(TcCfg<NCOL>::THREADS, 1) chunk_attn_tc(const _
     }
     __syncwarp();
   } else {
-    // ---------------- softmax and accumulation (warpgroup wg = warp / 4).  With two warpgroups,
-    // wg takes the tiles i with i % 2 == wg (always TMEM/P buffer wg) and keeps its own online-
-    // softmax state; each writes its own state slot and the finish kernel merges them (Eq. 8).
-    constexpr int NWG = C::NWG;
+    // ---------------- softmax and accumulation: warpgroup wg = warp / 4, thread tid = TMEM lane
+    // (token tid of an S tile, output dimension tid of an O tile)
     const int wg = warp >> 2;
-    const int tid = threadIdx.x & 127;  // = TMEM lane = token of the S tile = output dimension
+    const int tid = threadIdx.x & 127;
     const uint32_t bar_wg = 1u + static_cast<uint32_t>(wg);
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    constexpr int NH = NCOL / 32;  // columns per lane after a transpose-reduction
-    float acc[NCOL];   // O^T accumulator: output dimension tid, query row c
-    float s[NCOL];     // scores of token tid, then p, then O^T tile values
-    float lsum[NCOL];  // this thread's share of each row's denominator (relative to mref)
+    float acc[NCOL];  // O^T accumulator: output dimension tid, query row c
+    float s[NCOL];    // scores of token tid, then p, then O^T tile values
+    // Row denominators relative to mref.  One warpgroup: each thread keeps its share of every row
+    // (lsum), summed once per segment.  Two warpgroups (fewer registers per thread): each tile's sums
+    // are transpose-reduced at once and lane c of each warp keeps row c's partial (lw).
+    constexpr bool kRowSums = (NWG == 1);
+    float lsum[kRowSums ? NCOL : 1];
+    float lw = 0.f;
     uint32_t rescaled = 0u;  // bit k: the tile with alpha buffer k re-based the row maxima
     float* red_w = red + wg * 4 * NCOL;
     float* mref = mnew + wg * NCOL;  // running reference maximum per row, shared by the warpgroup
@@ -490,16 +522,15 @@ __global__ void __launch_bounds__(TcCfg<NCOL>::THREADS, 1) chunk_attn_tc(const _
     int64_t i = 0;
     bool ok = true;
     int nr = NCOL;
-    auto abuf = [](int64_t j) { return static_cast<int>((NWG == 2 ? (j >> 1) : j) & 1); };
+    auto abuf = [](int64_t j) { return static_cast<int>(j & 1); };
 
     auto accumulate = [&](int64_t j) -> bool {
-      if (!bar_all(bar_wg, 128, W.wait(OFULL + 8u * (j & 1), static_cast<uint32_t>(j >> 1) & 1u))) return false;
+      const int bf = C::buf(j, wg);
+      if (!bar_all(bar_wg, 128, W.wait(OFULL + 8u * bf, static_cast<uint32_t>(j >> 1) & 1u))) return false;
       tc_fence_after();
-      const uint32_t ta = tmem + lane_base + C::O_COL + static_cast<uint32_t>(j & 1) * NCOL;
-      tmem_ld32<0>(ta, s);
-      if constexpr (NCOL == 64) tmem_ld32<32>(ta + 32, s);
+      tmem_ld32<0>(tmem + lane_base + C::O_COL + static_cast<uint32_t>(bf) * NCOL, s);
       tc_fence_before();
-      mbar_arrive(OEMPTY + 8u * (j & 1));
+      mbar_arrive(OEMPTY + 8u * bf);
       if ((rescaled >> abuf(j)) & 1u) {
         const float4* al4 = reinterpret_cast<const float4*>(alpha_w + abuf(j) * NCOL);
 #pragma unroll
@@ -521,58 +552,52 @@ __global__ void __launch_bounds__(TcCfg<NCOL>::THREADS, 1) chunk_attn_tc(const _
     };
 
     for (int64_t x = x_begin; x < x_end;) {
-      // all softmax threads meet here: nobody is still reading the previous segment's Q through an
-      // MMA, and a wait that gave up anywhere stops both warpgroups together
+      // all softmax threads meet here: nobody still needs the previous segment's Q, and a wait that
+      // gave up anywhere stops every warpgroup together
       if (!bar_all(3u, 128u * NWG, ok)) break;
       const Seg sg = seg_at(P, x, x_end, hint);
       const PartDesc& pd = P.parts[sg.part];
       const int b = pd.req;
       const int R = P.group * P.n_query;
-      const int r0 = sg.rb * NCOL;
-      nr = min(NCOL, R - r0);
-      const int64_t row_base =
-          (static_cast<int64_t>(b) * P.n_q_heads + static_cast<int64_t>(sg.g) * P.group) * P.n_query + r0;
+      const int rblk = sg.rb * C::ROWS;                          // first row of this pass
+      const int nrows = min(C::ROWS, R - rblk);                   // valid rows of the pass
+      const int r0 = rblk + ((MODE == kRowSplit) ? wg * NCOL : 0);  // this warpgroup's first row
+      nr = max(0, min(NCOL, R - r0));
+      const int64_t qrow0 =
+          (static_cast<int64_t>(b) * P.n_q_heads + static_cast<int64_t>(sg.g) * P.group) * P.n_query;
 
-      // Q rows of the pair into shared memory (K-major, swizzled); padding rows are zero
-      for (int idx = threadIdx.x; idx < NCOL * 16; idx += 128 * NWG) {
+      // Q rows of the pass into shared memory: 32-row K-major swizzled blocks, padding rows zero
+      for (int idx = threadIdx.x; idx < C::ROWS * 16; idx += 128 * NWG) {
         const int c = idx >> 4, ch = idx & 15;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (c < nr) v = *reinterpret_cast<const uint4*>(P.q + (row_base + c) * D + ch * 8);
-        st_shared_v4(base + C::OFF_Q + swz_offset(c, ch, NCOL * 128), v);
+        if (c < nrows) v = *reinterpret_cast<const uint4*>(P.q + (qrow0 + rblk + c) * D + ch * 8);
+        st_shared_v4(base + C::OFF_Q + static_cast<uint32_t>(c / NCOL) * (NCOL * D * 2) +
+                         swz_offset(c % NCOL, ch, NCOL * 128),
+                     v);
       }
-      if ((warp & 3) == 0) {
-#pragma unroll
-        for (int h = 0; h < NH; ++h) mref[lane + 32 * h] = -INFINITY;
-      }
+      if ((warp & 3) == 0) mref[lane] = -INFINITY;
       fence_proxy_async();
       mbar_arrive(QFULL);
 
 #pragma unroll
       for (int c = 0; c < NCOL; ++c) {
         acc[c] = 0.f;
-        lsum[c] = 0.f;
+        if constexpr (kRowSums) lsum[c] = 0.f;
       }
+      lw = 0.f;
       int64_t prev = -1;  // this warpgroup's previous tile in the segment
 
       for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
-        if (NWG == 2 && static_cast<int>(i & 1) != wg) continue;
-        // two warpgroups: this warpgroup's previous O first - its PV read the P buffer that P_i
-        // is about to overwrite, so it must have completed (one warpgroup: see below)
-        if (NWG == 2 && prev >= 0 && !accumulate(prev)) {
-          ok = false;
-          break;
-        }
+        const int bf = C::buf(i, wg);
         const bool tok_valid = (sg.tile0 + t) * TOK + tid < pd.n_tok;
-        if (!bar_all(bar_wg, 128, W.wait(SFULL + 8u * (i & 1), static_cast<uint32_t>(i >> 1) & 1u))) {
+        if (!bar_all(bar_wg, 128, W.wait(SFULL + 8u * bf, static_cast<uint32_t>(i >> 1) & 1u))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t ta = tmem + lane_base + C::S_COL + static_cast<uint32_t>(i & 1) * NCOL;
-        tmem_ld32<0>(ta, s);
-        if constexpr (NCOL == 64) tmem_ld32<32>(ta + 32, s);
+        tmem_ld32<0>(tmem + lane_base + C::S_COL + static_cast<uint32_t>(bf) * NCOL, s);
         tc_fence_before();
-        mbar_arrive(SEMPTY + 8u * (i & 1));
+        mbar_arrive(SEMPTY + 8u * bf);
 
         // scaled scores (log2 units); does any exceed its row's reference by more than kTau?
         bool up = false;
@@ -596,36 +621,37 @@ __global__ void __launch_bounds__(TcCfg<NCOL>::THREADS, 1) chunk_attn_tc(const _
         if (up) {
           // exact tile maximum per row: warp transpose-reduction, then across the 4 warps
           red_w[(warp & 3) * NCOL + lane] = xpose_reduce<0, NCOL, true>(s, lane);
-          if constexpr (NCOL == 64) red_w[(warp & 3) * NCOL + 32 + lane] = xpose_reduce<32, NCOL, true>(s, lane);
           bar_sync(bar_wg, 128);
           if ((warp & 3) == 0) {
-#pragma unroll
-            for (int h = 0; h < NH; ++h) {
-              const int c = lane + 32 * h;
-              const float tm =
-                  fmaxf(fmaxf(red_w[c], red_w[NCOL + c]), fmaxf(red_w[2 * NCOL + c], red_w[3 * NCOL + c]));
-              const float mo = mref[c];
-              const float mn = fmaxf(mo, tm);
-              alpha_w[ab * NCOL + c] = (mo == -INFINITY) ? 0.f : exp2_approx(mo - mn);
-              mref[c] = mn;
-            }
+            const int c = lane;
+            const float tm = fmaxf(fmaxf(red_w[c], red_w[NCOL + c]), fmaxf(red_w[2 * NCOL + c], red_w[3 * NCOL + c]));
+            const float mo = mref[c];
+            const float mn = fmaxf(mo, tm);
+            alpha_w[ab * NCOL + c] = (mo == -INFINITY) ? 0.f : exp2_approx(mo - mn);
+            mref[c] = mn;
           }
           bar_sync(bar_wg, 128);
-          const float4* al4 = reinterpret_cast<const float4*>(alpha_w + ab * NCOL);
+          if constexpr (kRowSums) {
+            const float4* al4 = reinterpret_cast<const float4*>(alpha_w + ab * NCOL);
 #pragma unroll
-          for (int c4 = 0; c4 < NCOL / 4; ++c4) {
-            if (4 * c4 < nr) {
-              const float4 a = al4[c4];
-              lsum[4 * c4 + 0] *= a.x;
-              lsum[4 * c4 + 1] *= a.y;
-              lsum[4 * c4 + 2] *= a.z;
-              lsum[4 * c4 + 3] *= a.w;
+            for (int c4 = 0; c4 < NCOL / 4; ++c4) {
+              if (4 * c4 < nr) {
+                const float4 a = al4[c4];
+                lsum[4 * c4 + 0] *= a.x;
+                lsum[4 * c4 + 1] *= a.y;
+                lsum[4 * c4 + 2] *= a.z;
+                lsum[4 * c4 + 3] *= a.w;
+              }
             }
+          } else {
+            lw *= alpha_w[ab * NCOL + lane];
           }
         }
 
         // P^T = 2^(s - mref), bf16, into the K-major swizzled B operand of the PV product
-        const uint32_t pbase = base + C::OFF_P + static_cast<uint32_t>(i & 1) * C::P_BYTES +
+        // P^T of this tile goes into the tile's K buffer (dead since the S products completed)
+        const uint32_t pbase = base + C::OFF_KV + static_cast<uint32_t>(i % C::STAGES) * 2u * TILE_BYTES +
+                               static_cast<uint32_t>((MODE == kRowSplit) ? wg : 0) * C::P_BYTES +
                                static_cast<uint32_t>(tid >> 6) * (NCOL * 128) + static_cast<uint32_t>((tid & 7) << 1);
 #pragma unroll
         for (int c4 = 0; c4 < NCOL / 4; ++c4) {
@@ -636,19 +662,23 @@ __global__ void __launch_bounds__(TcCfg<NCOL>::THREADS, 1) chunk_attn_tc(const _
             for (int e = 0; e < 4; ++e) {
               const int c = 4 * c4 + e;
               const float pv = exp2_approx(s[c] - mm[e]);
-              lsum[c] += pv;
+              if constexpr (kRowSums) lsum[c] += pv;
+              s[c] = pv;
               const uint32_t off = static_cast<uint32_t>(c) * 128u +
                                    (static_cast<uint32_t>(((tid & 63) >> 3) ^ (c & 7)) << 4);
               st_shared_b16(pbase + off, __bfloat16_as_ushort(__float2bfloat16_rn(pv)));
             }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[4 * c4 + e] = 0.f;  // rows past nr add nothing to the sums
           }
         }
         fence_proxy_async();
-        mbar_arrive(PFULL + 8u * (i & 1));
+        mbar_arrive(PFULL + 8u * bf);
+        if constexpr (!kRowSums) lw += xpose_reduce<0, NCOL, false>(s, lane);
 
-        // one warpgroup: the previous tile's O one step behind, so the MMAs of tile i overlap the
-        // accumulation; P_i's buffer was last read by PV_{i-2}, accumulated one iteration ago
-        if (NWG == 1 && prev >= 0 && !accumulate(prev)) {
+        // the previous tile's O one step behind, so the MMAs of tile i overlap the accumulation
+        if (prev >= 0 && !accumulate(prev)) {
           ok = false;
           break;
         }
@@ -656,21 +686,21 @@ __global__ void __launch_bounds__(TcCfg<NCOL>::THREADS, 1) chunk_attn_tc(const _
       }
       if (ok && prev >= 0) ok = accumulate(prev);
       if (ok && prev >= 0) {
-        // this warpgroup's segment state: m = mref, l = sum over threads of lsum, a = acc
-        red_w[(warp & 3) * NCOL + lane] = xpose_reduce<0, NCOL, false>(lsum, lane);
-        if constexpr (NCOL == 64) red_w[(warp & 3) * NCOL + 32 + lane] = xpose_reduce<32, NCOL, false>(lsum, lane);
-        bar_sync(bar_wg, 128);
-        if ((warp & 3) == 0) {
-#pragma unroll
-          for (int h = 0; h < NH; ++h) {
-            const int c = lane + 32 * h;
-            fin_w[c] = mref[c];
-            fin_w[NCOL + c] = red_w[c] + red_w[NCOL + c] + red_w[2 * NCOL + c] + red_w[3 * NCOL + c];
-          }
+        // this warpgroup's segment state: m = mref, l = sum over threads, a = acc
+        if constexpr (kRowSums) {
+          red_w[(warp & 3) * NCOL + lane] = xpose_reduce<0, NCOL, false>(lsum, lane);
+        } else {
+          red_w[(warp & 3) * NCOL + lane] = lw;
         }
         bar_sync(bar_wg, 128);
-        const int64_t srow0 =
-            static_cast<int64_t>(P.slot_base + NWG * sg.slot + wg) * P.slot_stride + row_base;
+        if ((warp & 3) == 0) {
+          const int c = lane;
+          fin_w[c] = mref[c];
+          fin_w[NCOL + c] = red_w[c] + red_w[NCOL + c] + red_w[2 * NCOL + c] + red_w[3 * NCOL + c];
+        }
+        bar_sync(bar_wg, 128);
+        const int slot = P.slot_base + sg.slot;
+        const int64_t srow0 = static_cast<int64_t>(slot) * P.slot_stride + qrow0 + r0;
 #pragma unroll
         for (int c = 0; c < NCOL; ++c) {
           if (c < nr) {
@@ -712,31 +742,32 @@ __global__ void __launch_bounds__(TcCfg<NCOL>::THREADS, 1) chunk_attn_tc(const _
   }
 }
 
-template <int NCOL>
+template <int MODE>
 cudaError_t launch_tc(const ChunkParams& p, int n_ctas, cudaStream_t stream) {
-  using C = TcCfg<NCOL>;
+  using C = TcCfg<MODE>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e =
-        cudaFuncSetAttribute(chunk_attn_tc<NCOL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaFuncSetAttribute(chunk_attn_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  chunk_attn_tc<NCOL><<<n_ctas, C::THREADS, C::SMEM, stream>>>(p);
+  chunk_attn_tc<MODE><<<n_ctas, C::THREADS, C::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool tc_supported(int head_dim, int rows) { return head_dim == 128 && rows >= 1; }
-int tc_ncol(int rows) { return rows <= 32 ? 32 : 64; }
-int tc_nwg(int ncol) { return ncol == 32 ? TcCfg<32>::NWG : TcCfg<64>::NWG; }
+int tc_mode(int rows) { return rows <= TcCfg<kSingle>::ROWS ? kSingle : kRowSplit; }
+int tc_rows_per_pass(int mode) { return mode == kRowSplit ? TcCfg<kRowSplit>::ROWS : TcCfg<kSingle>::ROWS; }
+int tc_slots_per_segment(int) { return 1; }
 int tc_max_ctas(int num_sms) { return num_sms; }  // one CTA per SM (shared memory)
 
-cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int ncol, int n_ctas, cudaStream_t stream) {
+cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int mode, int n_ctas, cudaStream_t stream) {
   if (n_ctas < 1) return cudaSuccess;
-  if (ncol == 32) return launch_tc<32>(p, n_ctas, stream);
-  if (ncol == 64) return launch_tc<64>(p, n_ctas, stream);
+  if (mode == kSingle) return launch_tc<kSingle>(p, n_ctas, stream);
+  if (mode == kRowSplit) return launch_tc<kRowSplit>(p, n_ctas, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -39,6 +39,8 @@ SMALL = [
     W.Workload("q32", 2, 8, 4, 128, (90, 257), 64, 32, seed=16),
     W.Workload("tree32", 2, 8, 8, 64, (40, 77), 16, 32, tree=True, tree_max_depth=40, seed=17),
     W.Workload("kscale", 4, 32, 8, 128, (777, 2048, 5, 4000), 512, 7, k_head_scale=True, seed=18),
+    W.Workload("r48", 2, 16, 2, 128, (700, 1300), 256, 6, seed=22),   # 48 rows: row split, 16 idle
+    W.Workload("r96", 2, 16, 4, 128, (500, 901), 128, 24, seed=23),   # 96 rows: two passes, last half empty
 ]
 
 
