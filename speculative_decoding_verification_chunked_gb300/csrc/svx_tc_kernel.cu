@@ -54,16 +54,15 @@ enum : int { kSingle = 0, kRowSplit = 2 };
 
 template <int MODE>
 struct TcCfg {
-  static constexpr int NCOL = 32;                          // query rows per warpgroup (MMA N)
+  static constexpr int NCOL = 32;                          // query rows per softmax warpgroup
   static constexpr int NWG = (MODE == kSingle) ? 1 : 2;   // softmax warpgroups
-  static constexpr int ROWS = (MODE == kRowSplit) ? 2 * NCOL : NCOL;  // query rows per pass
-  static constexpr int NBUF = (MODE == kRowSplit) ? 4 : 2;  // S / O / P buffers: (warpgroup, tile parity)
+  static constexpr int ROWS = NWG * NCOL;                  // query rows per pass: the MMA N of both products
   static constexpr int THREADS = 32 * (4 * NWG + 2);
   static constexpr int STAGES = 3;
   static constexpr int Q_BYTES = ROWS * D * 2;
-  // P^T of a tile (one per warpgroup) is written into that tile's own K buffer: K is dead once the
-  // tile's S products have completed, and the stage is recycled only after its PV products.
-  static constexpr int P_BYTES = NCOL * TOK * 2;
+  // P^T of a tile (all rows of the pass) is written into that tile's own K buffer: K is dead once the
+  // tile's S product has completed, and the stage is recycled only after its PV product.
+  static constexpr int P_BYTES = ROWS * TOK * 2;
   static constexpr int OFF_KV = 0;
   static constexpr int OFF_Q = STAGES * 2 * TILE_BYTES;
   // per softmax warpgroup:
@@ -71,22 +70,19 @@ struct TcCfg {
   static constexpr int OFF_MNEW = OFF_RED + NWG * 4 * NCOL * 4;    // float [NWG][NCOL]: reference max per row
   static constexpr int OFF_ALPHA = OFF_MNEW + NWG * NCOL * 4;      // float [NWG][2][NCOL]
   static constexpr int OFF_FIN = OFF_ALPHA + NWG * 2 * NCOL * 4;   // float [NWG][2][NCOL]: final m, l
-  static constexpr int N_BAR = 2 * STAGES + 5 * NBUF + 2;
+  static constexpr int N_BAR = 2 * STAGES + 5 * 2 + 2;
   static constexpr int OFF_BAR = OFF_FIN + NWG * 2 * NCOL * 4;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SMEM = BYTES + 1024;  // slack to align the base to 1024 bytes
-  static constexpr uint32_t TMEM_COLS = 2 * NBUF * NCOL;  // S and O buffers: 128 or 256 columns
+  // TMEM: S and O accumulators for two tile parities, ROWS columns each (128 or 256 columns); the
+  // columns of warpgroup wg start at wg * NCOL within each
+  static constexpr uint32_t TMEM_COLS = 4 * ROWS;
   static constexpr uint32_t S_COL = 0;
-  static constexpr uint32_t O_COL = NBUF * NCOL;
-  static_assert(OFF_Q % 1024 == 0 && P_BYTES % 1024 == 0 && (NCOL * D * 2) % 1024 == 0 &&
-                    NWG * P_BYTES <= TILE_BYTES,
-                "swizzle atoms need 1 KiB alignment; the P^T buffers must fit in a K tile");
+  static constexpr uint32_t O_COL = 2 * ROWS;
+  static_assert(OFF_Q % 1024 == 0 && P_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0 && P_BYTES <= TILE_BYTES,
+                "swizzle atoms need 1 KiB alignment; P^T must fit in a K tile");
   static_assert(SMEM <= 232448, "shared memory per CTA");
-  // buffer of warpgroup wg for tile j
-  __device__ static constexpr int buf(int64_t j, int wg) {
-    return (MODE == kRowSplit) ? (wg * 2 + static_cast<int>(j & 1)) : static_cast<int>(j & 1);
-  }
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -109,6 +105,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
@@ -152,8 +157,18 @@ __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t n, bool v) {
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void st_shared_b16(uint32_t addr, unsigned short v) {
-  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+// Four 8x8 bf16 matrices, transposed on the way out: register m of thread T holds row T/4, columns
+// 2(T%4) and 2(T%4)+1 (low half first) of matrix m, and row r of matrix m is stored as column r, 16
+// contiguous bytes at the address that thread 8m + r supplies.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
+               "r"(r2), "r"(r3)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
@@ -168,12 +183,15 @@ __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+// One MMA; the shared-memory descriptors are passed as their two 32-bit words (the high word is the
+// same for every operand of this kernel, see desc_lo / kDescHi).
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t d_hi, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(d_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -199,6 +217,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[N]) {
   for (int i = 0; i < 32; ++i) v[OFF + i] = __uint_as_float(r[i]);
 }
 
+// The 128-token x 32-column S tile of this warp's 32 TMEM lanes in the 16x256b shape (two loads of
+// 16 lanes): thread T holds tokens 8z + T/4 (z = 0..3, relative to the warp's first lane) and columns
+// 8k + 2(T%4) + e (k = 0..3, e = 0..1), in register sidx(z, k, e).
+__device__ __forceinline__ constexpr int sidx(int z, int k, int e) { return (z >> 1) * 16 + k * 4 + (z & 1) * 2 + e; }
+__device__ __forceinline__ void tmem_ld_s(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
+      "[%33];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr), "r"(taddr + (16u << 16))
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ float exp2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -216,16 +255,17 @@ __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn_major,
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle (atoms of 8 rows x 128 B).
-__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;  // descriptor version of the tcgen05 family
-  d |= static_cast<uint64_t>(2) << 61;  // swizzle: 128 bytes
-  return d;
+// Shared-memory matrix descriptor, 128-byte swizzle (atoms of 8 rows x 128 B), as two 32-bit words.
+// Low word: start address / 16 (bits 0-13) and the leading-dimension byte offset / 16 (bits 16-29).
+// High word (descriptor bits 32-63): stride byte offset / 16 = 1024 / 16 (8-row groups 1 KiB apart),
+// the tcgen05 descriptor version (bit 46) and the 128-byte swizzle mode (2 in bits 61-63).
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << (46 - 32)) | (2u << (61 - 32));
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }
+// The start-address field advanced by `bytes` (16-byte multiple; shared addresses stay below 256 KiB,
+// so the field never carries into the next one).
+__device__ __forceinline__ constexpr uint32_t desc_adv(uint32_t bytes) { return bytes >> 4; }
 
 // Byte offset of 16-byte piece `chunk` (0..15 along the 128 dimensions) of row
 // `row` in a K-major, 128-byte-swizzled [rows][128] bf16 tile: two atoms
@@ -233,27 +273,6 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo_byte
 __device__ __forceinline__ uint32_t swz_offset(int row, int chunk, uint32_t half_bytes) {
   return static_cast<uint32_t>(chunk >> 3) * half_bytes + static_cast<uint32_t>(row) * 128u +
          (static_cast<uint32_t>((chunk & 7) ^ (row & 7)) << 4);
-}
-
-// Butterfly transpose-reduction: on return, lane L holds the reduction over the
-// warp's 32 lanes of column OFF + L (31 shuffles instead of 32 x 5).
-template <int OFF, int N, bool MAX>
-__device__ __forceinline__ float xpose_reduce(const float (&v)[N], int lane) {
-  float w[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) w[j] = v[OFF + j];
-#pragma unroll
-  for (int step = 16; step >= 1; step >>= 1) {
-    const bool up = (lane & step) != 0;
-#pragma unroll
-    for (int j = 0; j < step; ++j) {
-      const float send = up ? w[j] : w[j + step];
-      const float keep = up ? w[j + step] : w[j];
-      const float got = __shfl_xor_sync(0xffffffffu, send, step);
-      w[j] = MAX ? fmaxf(keep, got) : keep + got;
-    }
-  }
-  return w[0];
 }
 
 struct Seg {
@@ -312,7 +331,9 @@ struct Waiter {
   }
 };
 
-template <int MODE>
+// NK: 8-column blocks of S computed per warpgroup (query rows 0 .. 8*NK-1 of its 32); every pass has
+// at most 8*NK valid rows per warpgroup.
+template <int MODE, int NK>
 __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const __grid_constant__ ChunkParams P) {
   using C = TcCfg<MODE>;
   constexpr int NCOL = C::NCOL;
@@ -326,8 +347,8 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
   // mbarriers: FULL/EMPTY per stage; SFULL, SEMPTY, PFULL, OFULL, OEMPTY per buffer; QFULL; DRAIN
   const uint32_t bar0 = base + C::OFF_BAR;
   const uint32_t FULL = bar0, EMPTY = bar0 + 8u * C::STAGES;
-  const uint32_t SFULL = bar0 + 16u * C::STAGES, SEMPTY = SFULL + 8u * C::NBUF, PFULL = SEMPTY + 8u * C::NBUF,
-                 OFULL = PFULL + 8u * C::NBUF, OEMPTY = OFULL + 8u * C::NBUF, QFULL = OEMPTY + 8u * C::NBUF,
+  const uint32_t SFULL = bar0 + 16u * C::STAGES, SEMPTY = SFULL + 16u, PFULL = SEMPTY + 16u, OFULL = PFULL + 16u,
+                 OEMPTY = OFULL + 16u, QFULL = OEMPTY + 16u,
                  DRAIN = QFULL + 8u;
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_MISC);
   float* red = reinterpret_cast<float*>(gbase + C::OFF_RED);
@@ -340,12 +361,12 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       mbar_init(FULL + 8u * s, 32);
       mbar_init(EMPTY + 8u * s, 1);
     }
-    for (int b = 0; b < C::NBUF; ++b) {
+    for (int b = 0; b < 2; ++b) {  // tile parity
       mbar_init(SFULL + 8u * b, 1);
-      mbar_init(SEMPTY + 8u * b, 128);
-      mbar_init(PFULL + 8u * b, 128);
+      mbar_init(SEMPTY + 8u * b, 128 * NWG);
+      mbar_init(PFULL + 8u * b, 128 * NWG);
       mbar_init(OFULL + 8u * b, 1);
-      mbar_init(OEMPTY + 8u * b, 128);
+      mbar_init(OEMPTY + 8u * b, 128 * NWG);
     }
     mbar_init(QFULL, 128 * NWG);
     mbar_init(DRAIN, 1);
@@ -411,87 +432,84 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
   } else if (warp == 4 * NWG + 1) {
     // ---------------- MMA issuer (one thread)
     if (lane == 0) {
-      constexpr uint32_t idesc_s = make_idesc(128, NCOL, false, false);
-      constexpr uint32_t idesc_o = make_idesc(128, NCOL, true, false);
-      constexpr int SGROUPS = (MODE == kRowSplit) ? 2 : 1;  // warpgroups served by one tile's MMAs
-      // S^T of tile j for every warpgroup that consumes it: K tile (A, K-major) x Q rows (B, K-major)
-      auto issue_s = [&](int64_t j) -> bool {
-        const int stage = static_cast<int>(j % C::STAGES);
-        const uint32_t use = static_cast<uint32_t>(j / C::STAGES);
-        if (!W.wait(FULL + 8u * stage, use & 1u)) return false;
+      constexpr int ROWS = C::ROWS;
+      constexpr uint32_t idesc_s = make_idesc(128, ROWS, false, false);
+      constexpr uint32_t idesc_o = make_idesc(128, ROWS, true, false);
+      const uint32_t qa = desc_lo(base + C::OFF_Q, 16);
+      // S^T of tile j: K tile (A, K-major) x the pass's Q rows (B, K-major)
+      auto issue_s = [&](int64_t j) {
+        const uint32_t kaddr = base + C::OFF_KV + static_cast<uint32_t>(j % C::STAGES) * 2u * TILE_BYTES;
         fence_proxy_async();  // cp.async writes (generic proxy) before tensor-core reads (async proxy)
-        const uint32_t kaddr = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES;
-        for (int g2 = 0; g2 < SGROUPS; ++g2) {
-          const int wg = g2;
-          const int bf = C::buf(j, wg);
-          if (j >= 2 && !W.wait(SEMPTY + 8u * bf, ((static_cast<uint32_t>(j >> 1)) & 1u) ^ 1u)) return false;
-          tc_fence_after();
-          const uint32_t qaddr = base + C::OFF_Q + static_cast<uint32_t>((MODE == kRowSplit) ? wg : 0) * (NCOL * D * 2);
-          const uint32_t d = tmem + C::S_COL + static_cast<uint32_t>(bf) * NCOL;
+        tc_fence_after();
+        const uint32_t d = tmem + C::S_COL + static_cast<uint32_t>(j & 1) * ROWS;
+        const uint32_t ka = desc_lo(kaddr, 16);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = make_sdesc(kaddr + (kk >> 2) * HALF_BYTES + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = make_sdesc(qaddr + (kk >> 2) * (NCOL * 128) + (kk & 3) * 32, 16, 1024);
-            mma_bf16(d, a, b, idesc_s, kk > 0 ? 1u : 0u);
-          }
-        }
-        // commits after every S product of the tile: a warpgroup writes its P^T into this K tile
-        // once its SFULL fires, so no product may still be reading K then
-        for (int g2 = 0; g2 < SGROUPS; ++g2)
-          mma_commit(SFULL + 8u * C::buf(j, g2));
-        return true;
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16(d, ka + desc_adv((kk >> 2) * HALF_BYTES + (kk & 3) * 32),
+                   qa + desc_adv((kk >> 2) * (ROWS * 128) + (kk & 3) * 32), kDescHi, idesc_s, kk > 0 ? 1u : 0u);
+        mma_commit(SFULL + 8u * static_cast<uint32_t>(j & 1));
       };
-      // O^T of tile j for warpgroup wg: V tile (A, dimension-major) x P^T (B, K-major)
-      auto issue_pv = [&](int64_t j, int wg) -> bool {
-        const int bf = C::buf(j, wg);
-        const uint32_t par = static_cast<uint32_t>(j >> 1) & 1u;
-        if (!W.wait(PFULL + 8u * bf, par)) return false;
-        if (j >= 2 && !W.wait(OEMPTY + 8u * bf, par ^ 1u)) return false;
+      // O^T of tile j: V tile (A, dimension-major) x P^T (B, K-major, in the tile's K buffer)
+      auto issue_pv = [&](int64_t j) {
+        const int stage = static_cast<int>(j % C::STAGES);
+        const uint32_t kaddr = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES;
         fence_proxy_async();  // P^T was written with ordinary stores
         tc_fence_after();
-        const int stage = static_cast<int>(j % C::STAGES);
-        const uint32_t vaddr = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES + TILE_BYTES;
-        const uint32_t paddr = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES +
-                               static_cast<uint32_t>((MODE == kRowSplit) ? wg : 0) * C::P_BYTES;
-        const uint32_t d = tmem + C::O_COL + static_cast<uint32_t>(bf) * NCOL;
+        const uint32_t d = tmem + C::O_COL + static_cast<uint32_t>(j & 1) * ROWS;
+        // A = V^T: 64-dimension halves 16 KiB apart (LBO), 8-token groups 1 KiB apart (SBO)
+        const uint32_t va = desc_lo(kaddr + TILE_BYTES, HALF_BYTES), pa = desc_lo(kaddr, 16);
 #pragma unroll
-        for (int kk = 0; kk < TOK / 16; ++kk) {
-          // A = V^T: 64-dimension halves 16 KiB apart (LBO), 8-token groups 1 KiB apart (SBO)
-          const uint64_t a = make_sdesc(vaddr + kk * 2048, HALF_BYTES, 1024);
-          const uint64_t b = make_sdesc(paddr + (kk >> 2) * (NCOL * 128) + (kk & 3) * 32, 16, 1024);
-          mma_bf16(d, a, b, idesc_o, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(OFULL + 8u * bf);
-        return true;
+        for (int kk = 0; kk < TOK / 16; ++kk)
+          mma_bf16(d, va + desc_adv(kk * 2048), pa + desc_adv((kk >> 2) * (ROWS * 128) + (kk & 3) * 32), kDescHi,
+                   idesc_o, kk > 0 ? 1u : 0u);
+        mma_commit(OFULL + 8u * static_cast<uint32_t>(j & 1));
+        mma_commit(EMPTY + 8u * static_cast<uint32_t>(stage));  // the stage's products are done when this fires
       };
-      int hint = 0;
-      int64_t i = 0;
+      // Issue whichever product is ready, so a tile's PV never waits behind the next tile's data.
+      // S(j) needs tile j's data, its segment's Q (first tile of a segment) and S buffer j&1 read by
+      // the softmax (tile j-2); PV(j) needs S(j) issued, P^T(j) written and O buffer j&1 read (tile j-2).
+      const int64_t n_local = x_end - x_begin;
+      int64_t sn = 0, pn = 0;   // next tile (CTA-local) for S and for PV
+      int64_t seg_end = 0;      // end of the segment S is in; sn == seg_end: S waits for the next Q
       uint32_t seg_idx = 0;
-      bool ok = true;
-      for (int64_t x = x_begin; x < x_end && ok; ++seg_idx) {
-        const Seg sg = seg_at(P, x, x_end, hint);
-        if (!W.wait(QFULL, seg_idx & 1u)) break;
-        tc_fence_after();
-        if (!issue_s(i)) break;
-        for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
-          // S of the next tile goes out before this tile's PV (one tile ahead)
-          if (t + 1 < sg.n_tiles && !issue_s(i + 1)) {
-            ok = false;
-            break;
+      int hint = 0;
+      uint32_t spins = 0;
+      uint64_t t_idle = 0;
+      while (pn < n_local) {
+        bool progress = false;
+        if (sn < n_local) {
+          if (sn == seg_end && mbar_test(QFULL, seg_idx & 1u)) {
+            seg_end = sn + seg_at(P, x_begin + sn, x_end, hint).n_tiles;
+            ++seg_idx;
+            tc_fence_after();
           }
-          const int stage = static_cast<int>(i % C::STAGES);
-          if (MODE == kRowSplit) {
-            if (!issue_pv(i, 0) || !issue_pv(i, 1)) {
-              ok = false;
-              break;
-            }
-          } else if (!issue_pv(i, 0)) {
-            ok = false;
-            break;
+          if (sn < seg_end && mbar_test(FULL + 8u * static_cast<uint32_t>(sn % C::STAGES),
+                                        static_cast<uint32_t>(sn / C::STAGES) & 1u) &&
+              (sn < 2 || mbar_test(SEMPTY + 8u * static_cast<uint32_t>(sn & 1),
+                                   (static_cast<uint32_t>(sn >> 1) & 1u) ^ 1u))) {
+            issue_s(sn++);
+            progress = true;
           }
-          mma_commit(EMPTY + 8u * stage);  // both products of this stage are done when this fires
         }
-        x += sg.n_tiles;
+        if (pn < sn && mbar_test(PFULL + 8u * static_cast<uint32_t>(pn & 1), static_cast<uint32_t>(pn >> 1) & 1u) &&
+            (pn < 2 ||
+             mbar_test(OEMPTY + 8u * static_cast<uint32_t>(pn & 1), (static_cast<uint32_t>(pn >> 1) & 1u) ^ 1u))) {
+          issue_pv(pn++);
+          progress = true;
+        }
+        if (progress) {
+          spins = 0;
+        } else if ((++spins & 255u) == 0) {  // bounded: give up after kWaitLimitNs without progress
+          if (*W.abort) break;
+          const uint64_t now = global_ns();
+          if (spins == 256u) {
+            t_idle = now;
+          } else if (now - t_idle > kWaitLimitNs) {
+            *W.abort = 1u;
+            atomicOr(W.err, 1);
+            break;
+          }
+        }
       }
       // drain: every MMA issued by this thread has completed before TMEM is freed
       mma_commit(DRAIN);
@@ -499,25 +517,32 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     }
     __syncwarp();
   } else {
-    // ---------------- softmax and accumulation: warpgroup wg = warp / 4, thread tid = TMEM lane
-    // (token tid of an S tile, output dimension tid of an O tile)
+    // ---------------- softmax and accumulation: warpgroup wg = warp / 4.  For S tiles a thread holds
+    // 4 tokens x 8 columns (16x256b TMEM shape, see tmem_ld_s); for O tiles it holds output
+    // dimension tid, all 32 columns (32x32b shape).
     const int wg = warp >> 2;
+    const int q4 = warp & 3;  // warp within the warpgroup: TMEM lanes / tile tokens 32*q4 .. 32*q4+31
     const int tid = threadIdx.x & 127;
     const uint32_t bar_wg = 1u + static_cast<uint32_t>(wg);
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    float acc[NCOL];  // O^T accumulator: output dimension tid, query row c
-    float s[NCOL];    // scores of token tid, then p, then O^T tile values
-    // Row denominators relative to mref.  One warpgroup: each thread keeps its share of every row
-    // (lsum), summed once per segment.  Two warpgroups (fewer registers per thread): each tile's sums
-    // are transpose-reduced at once and lane c of each warp keeps row c's partial (lw).
-    constexpr bool kRowSums = (NWG == 1);
-    float lsum[kRowSums ? NCOL : 1];
-    float lw = 0.f;
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    constexpr int NC = 8 * NK;  // columns (query rows) computed: the active 8-column blocks
+    float acc[NCOL];   // O^T accumulator: output dimension tid, query row c
+    float s[32];       // S fragment, then the O^T tile values
+    float negm[2 * NK];  // -reference maximum of the thread's columns 8k + 2(lane%4) + e, index 2k + e
+    float thr[2 * NK];   // raw-score threshold of those columns: (reference + kTau) / scale
+    float lsum[2 * NK];  // the thread's share of those columns' denominators (relative to the reference)
+    const float inv_scale = 1.0f / P.q_scale;
     uint32_t rescaled = 0u;  // bit k: the tile with alpha buffer k re-based the row maxima
     float* red_w = red + wg * 4 * NCOL;
     float* mref = mnew + wg * NCOL;  // running reference maximum per row, shared by the warpgroup
     float* alpha_w = alpha + wg * 2 * NCOL;
     float* fin_w = fin + wg * 2 * NCOL;
+    // shared address of row lane%8 of P^T matrix lane/8 (token block 4*q4 + lane/8) for column block 0
+    // (the pass's P^T has C::ROWS rows; this warpgroup's start at row wg * NCOL)
+    const int tb = 4 * q4 + (lane >> 3), pr = lane & 7;
+    const uint32_t p_thread = static_cast<uint32_t>(tb >> 3) * (C::ROWS * 128) +
+                              static_cast<uint32_t>(wg * NCOL + pr) * 128u + (static_cast<uint32_t>((tb & 7) ^ pr) << 4);
+    const uint32_t col_wg = static_cast<uint32_t>(wg * NCOL);  // this warpgroup's columns in S and O
     int hint = 0;
     int64_t i = 0;
     bool ok = true;
@@ -525,28 +550,25 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     auto abuf = [](int64_t j) { return static_cast<int>(j & 1); };
 
     auto accumulate = [&](int64_t j) -> bool {
-      const int bf = C::buf(j, wg);
-      if (!bar_all(bar_wg, 128, W.wait(OFULL + 8u * bf, static_cast<uint32_t>(j >> 1) & 1u))) return false;
+      const uint32_t par = static_cast<uint32_t>(j & 1);
+      if (!bar_all(bar_wg, 128, W.wait(OFULL + 8u * par, static_cast<uint32_t>(j >> 1) & 1u))) return false;
       tc_fence_after();
-      tmem_ld32<0>(tmem + lane_base + C::O_COL + static_cast<uint32_t>(bf) * NCOL, s);
+      tmem_ld32<0>(tmem + lane_base + C::O_COL + par * C::ROWS + col_wg, s);
       tc_fence_before();
-      mbar_arrive(OEMPTY + 8u * bf);
+      mbar_arrive(OEMPTY + 8u * par);
       if ((rescaled >> abuf(j)) & 1u) {
         const float4* al4 = reinterpret_cast<const float4*>(alpha_w + abuf(j) * NCOL);
 #pragma unroll
-        for (int c4 = 0; c4 < NCOL / 4; ++c4) {
-          if (4 * c4 < nr) {
-            const float4 a = al4[c4];
-            acc[4 * c4 + 0] = fmaf(acc[4 * c4 + 0], a.x, s[4 * c4 + 0]);
-            acc[4 * c4 + 1] = fmaf(acc[4 * c4 + 1], a.y, s[4 * c4 + 1]);
-            acc[4 * c4 + 2] = fmaf(acc[4 * c4 + 2], a.z, s[4 * c4 + 2]);
-            acc[4 * c4 + 3] = fmaf(acc[4 * c4 + 3], a.w, s[4 * c4 + 3]);
-          }
+        for (int c4 = 0; c4 < NC / 4; ++c4) {
+          const float4 a = al4[c4];
+          acc[4 * c4 + 0] = fmaf(acc[4 * c4 + 0], a.x, s[4 * c4 + 0]);
+          acc[4 * c4 + 1] = fmaf(acc[4 * c4 + 1], a.y, s[4 * c4 + 1]);
+          acc[4 * c4 + 2] = fmaf(acc[4 * c4 + 2], a.z, s[4 * c4 + 2]);
+          acc[4 * c4 + 3] = fmaf(acc[4 * c4 + 3], a.w, s[4 * c4 + 3]);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < NCOL; ++c)
-          if ((c & ~3) < nr) acc[c] += s[c];
+        for (int c = 0; c < NC; ++c) acc[c] += s[c];
       }
       return true;
     };
@@ -566,116 +588,127 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       const int64_t qrow0 =
           (static_cast<int64_t>(b) * P.n_q_heads + static_cast<int64_t>(sg.g) * P.group) * P.n_query;
 
-      // Q rows of the pass into shared memory: 32-row K-major swizzled blocks, padding rows zero
+      // Q rows of the pass into shared memory: K-major swizzled [ROWS][128], padding rows zero
       for (int idx = threadIdx.x; idx < C::ROWS * 16; idx += 128 * NWG) {
         const int c = idx >> 4, ch = idx & 15;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (c < nrows) v = *reinterpret_cast<const uint4*>(P.q + (qrow0 + rblk + c) * D + ch * 8);
-        st_shared_v4(base + C::OFF_Q + static_cast<uint32_t>(c / NCOL) * (NCOL * D * 2) +
-                         swz_offset(c % NCOL, ch, NCOL * 128),
-                     v);
+        st_shared_v4(base + C::OFF_Q + swz_offset(c, ch, C::ROWS * 128), v);
       }
-      if ((warp & 3) == 0) mref[lane] = -INFINITY;
+      if (q4 == 0) mref[lane] = -INFINITY;
       fence_proxy_async();
       mbar_arrive(QFULL);
 
 #pragma unroll
-      for (int c = 0; c < NCOL; ++c) {
-        acc[c] = 0.f;
-        if constexpr (kRowSums) lsum[c] = 0.f;
+      for (int c = 0; c < NCOL; ++c) acc[c] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 2 * NK; ++j) {
+        negm[j] = 0.f;
+        thr[j] = -INFINITY;  // the first tile always re-bases
+        lsum[j] = 0.f;
       }
-      lw = 0.f;
       int64_t prev = -1;  // this warpgroup's previous tile in the segment
+      const int64_t n_tok = pd.n_tok;
 
       for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
-        const int bf = C::buf(i, wg);
-        const bool tok_valid = (sg.tile0 + t) * TOK + tid < pd.n_tok;
-        if (!bar_all(bar_wg, 128, W.wait(SFULL + 8u * bf, static_cast<uint32_t>(i >> 1) & 1u))) {
+        const uint32_t par = static_cast<uint32_t>(i & 1);
+        if (!bar_all(bar_wg, 128, W.wait(SFULL + 8u * par, static_cast<uint32_t>(i >> 1) & 1u))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        tmem_ld32<0>(tmem + lane_base + C::S_COL + static_cast<uint32_t>(bf) * NCOL, s);
+        tmem_ld_s(tmem + lane_base + C::S_COL + par * C::ROWS + col_wg, s);
         tc_fence_before();
-        mbar_arrive(SEMPTY + 8u * bf);
+        mbar_arrive(SEMPTY + 8u * par);
 
-        // scaled scores (log2 units); does any exceed its row's reference by more than kTau?
-        bool up = false;
-        const float4* mr4 = reinterpret_cast<const float4*>(mref);
+        // tokens past the part's end (last tile only) score -inf: they never vote and p = 0
+        const int64_t tile_tok0 = (sg.tile0 + t) * TOK;
+        if (tile_tok0 + TOK > n_tok) {
+          const int64_t tok = tile_tok0 + 32 * q4 + (lane >> 2);
 #pragma unroll
-        for (int c4 = 0; c4 < NCOL / 4; ++c4) {
-          if (4 * c4 < nr) {
-            const float4 m4 = mr4[c4];
-            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+          for (int z = 0; z < 4; ++z) {
+            const bool valid = tok + 8 * z < n_tok;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = 4 * c4 + e;
-              s[c] = tok_valid ? s[c] * P.q_scale : -INFINITY;
-              up |= s[c] > mm[e] + kTau;
+            for (int k = 0; k < NK; ++k) {
+              s[sidx(z, k, 0)] = valid ? s[sidx(z, k, 0)] : -INFINITY;
+              s[sidx(z, k, 1)] = valid ? s[sidx(z, k, 1)] : -INFINITY;
             }
           }
         }
+        // does any score exceed its row's reference by more than kTau?
+        bool up = false;
+#pragma unroll
+        for (int k = 0; k < NK; ++k)
+#pragma unroll
+          for (int z = 0; z < 4; ++z) {
+            up |= s[sidx(z, k, 0)] > thr[2 * k];
+            up |= s[sidx(z, k, 1)] > thr[2 * k + 1];
+          }
         up = bar_any(bar_wg, 128, up);
         const int ab = abuf(i);
         rescaled = (rescaled & ~(1u << ab)) | (static_cast<uint32_t>(up) << ab);
         if (up) {
-          // exact tile maximum per row: warp transpose-reduction, then across the 4 warps
-          red_w[(warp & 3) * NCOL + lane] = xpose_reduce<0, NCOL, true>(s, lane);
+          // exact tile maximum per row: the thread's 4 tokens, the 8 lanes sharing the columns, the 4 warps
+          float mx[2 * NK];
+#pragma unroll
+          for (int k = 0; k < NK; ++k)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float v = fmaxf(fmaxf(s[sidx(0, k, e)], s[sidx(1, k, e)]), fmaxf(s[sidx(2, k, e)], s[sidx(3, k, e)]));
+              v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+              v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+              v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+              mx[2 * k + e] = v;
+            }
+          if (lane < 4) {
+#pragma unroll
+            for (int k = 0; k < NK; ++k) {
+              red_w[q4 * NCOL + 8 * k + 2 * lane] = mx[2 * k];
+              red_w[q4 * NCOL + 8 * k + 2 * lane + 1] = mx[2 * k + 1];
+            }
+          }
           bar_sync(bar_wg, 128);
-          if ((warp & 3) == 0) {
+          if (q4 == 0 && lane < NC) {
             const int c = lane;
-            const float tm = fmaxf(fmaxf(red_w[c], red_w[NCOL + c]), fmaxf(red_w[2 * NCOL + c], red_w[3 * NCOL + c]));
+            const float tm =
+                fmaxf(fmaxf(red_w[c], red_w[NCOL + c]), fmaxf(red_w[2 * NCOL + c], red_w[3 * NCOL + c])) * P.q_scale;
             const float mo = mref[c];
             const float mn = fmaxf(mo, tm);
             alpha_w[ab * NCOL + c] = (mo == -INFINITY) ? 0.f : exp2_approx(mo - mn);
             mref[c] = mn;
           }
           bar_sync(bar_wg, 128);
-          if constexpr (kRowSums) {
-            const float4* al4 = reinterpret_cast<const float4*>(alpha_w + ab * NCOL);
 #pragma unroll
-            for (int c4 = 0; c4 < NCOL / 4; ++c4) {
-              if (4 * c4 < nr) {
-                const float4 a = al4[c4];
-                lsum[4 * c4 + 0] *= a.x;
-                lsum[4 * c4 + 1] *= a.y;
-                lsum[4 * c4 + 2] *= a.z;
-                lsum[4 * c4 + 3] *= a.w;
-              }
+          for (int k = 0; k < NK; ++k)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c = 8 * k + 2 * (lane & 3) + e;
+              const float m = mref[c];
+              negm[2 * k + e] = -m;
+              thr[2 * k + e] = (m + kTau) * inv_scale;
+              lsum[2 * k + e] *= alpha_w[ab * NCOL + c];
             }
-          } else {
-            lw *= alpha_w[ab * NCOL + lane];
-          }
         }
 
-        // P^T = 2^(s - mref), bf16, into the K-major swizzled B operand of the PV product
-        // P^T of this tile goes into the tile's K buffer (dead since the S products completed)
-        const uint32_t pbase = base + C::OFF_KV + static_cast<uint32_t>(i % C::STAGES) * 2u * TILE_BYTES +
-                               static_cast<uint32_t>((MODE == kRowSplit) ? wg : 0) * C::P_BYTES +
-                               static_cast<uint32_t>(tid >> 6) * (NCOL * 128) + static_cast<uint32_t>((tid & 7) << 1);
+        // P^T = 2^(s*scale - m) in bf16, into the K-major swizzled B operand of the PV product, which
+        // lives in this tile's K buffer (dead since the S products completed): one 8-column block per
+        // stmatrix, its four 8x8 matrices being the thread's four 8-token blocks
+        const uint32_t pbase = base + C::OFF_KV + static_cast<uint32_t>(i % C::STAGES) * 2u * TILE_BYTES + p_thread;
 #pragma unroll
-        for (int c4 = 0; c4 < NCOL / 4; ++c4) {
-          if (4 * c4 < nr) {
-            const float4 m4 = mr4[c4];
-            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+        for (int k = 0; k < NK; ++k) {
+          uint32_t pk[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = 4 * c4 + e;
-              const float pv = exp2_approx(s[c] - mm[e]);
-              if constexpr (kRowSums) lsum[c] += pv;
-              s[c] = pv;
-              const uint32_t off = static_cast<uint32_t>(c) * 128u +
-                                   (static_cast<uint32_t>(((tid & 63) >> 3) ^ (c & 7)) << 4);
-              st_shared_b16(pbase + off, __bfloat16_as_ushort(__float2bfloat16_rn(pv)));
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[4 * c4 + e] = 0.f;  // rows past nr add nothing to the sums
+          for (int z = 0; z < 4; ++z) {
+            const float p0 = exp2_approx(fmaf(s[sidx(z, k, 0)], P.q_scale, negm[2 * k]));
+            const float p1 = exp2_approx(fmaf(s[sidx(z, k, 1)], P.q_scale, negm[2 * k + 1]));
+            lsum[2 * k] += p0;
+            lsum[2 * k + 1] += p1;
+            pk[z] = pack_bf16x2(p0, p1);
           }
+          stmatrix_x4_trans(pbase + static_cast<uint32_t>(k) * 1024u, pk[0], pk[1], pk[2], pk[3]);
         }
         fence_proxy_async();
-        mbar_arrive(PFULL + 8u * bf);
-        if constexpr (!kRowSums) lw += xpose_reduce<0, NCOL, false>(s, lane);
+        mbar_arrive(PFULL + 8u * par);
 
         // the previous tile's O one step behind, so the MMAs of tile i overlap the accumulation
         if (prev >= 0 && !accumulate(prev)) {
@@ -687,13 +720,23 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       if (ok && prev >= 0) ok = accumulate(prev);
       if (ok && prev >= 0) {
         // this warpgroup's segment state: m = mref, l = sum over threads, a = acc
-        if constexpr (kRowSums) {
-          red_w[(warp & 3) * NCOL + lane] = xpose_reduce<0, NCOL, false>(lsum, lane);
-        } else {
-          red_w[(warp & 3) * NCOL + lane] = lw;
+#pragma unroll
+        for (int j = 0; j < 2 * NK; ++j) {
+          float v = lsum[j];
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          v += __shfl_xor_sync(0xffffffffu, v, 8);
+          v += __shfl_xor_sync(0xffffffffu, v, 16);
+          lsum[j] = v;
+        }
+        if (lane < 4) {
+#pragma unroll
+          for (int k = 0; k < NK; ++k) {
+            red_w[q4 * NCOL + 8 * k + 2 * lane] = lsum[2 * k];
+            red_w[q4 * NCOL + 8 * k + 2 * lane + 1] = lsum[2 * k + 1];
+          }
         }
         bar_sync(bar_wg, 128);
-        if ((warp & 3) == 0) {
+        if (q4 == 0 && lane < NC) {
           const int c = lane;
           fin_w[c] = mref[c];
           fin_w[NCOL + c] = red_w[c] + red_w[NCOL + c] + red_w[2 * NCOL + c] + red_w[3 * NCOL + c];
@@ -702,7 +745,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
         const int slot = P.slot_base + sg.slot;
         const int64_t srow0 = static_cast<int64_t>(slot) * P.slot_stride + qrow0 + r0;
 #pragma unroll
-        for (int c = 0; c < NCOL; ++c) {
+        for (int c = 0; c < NC; ++c) {
           if (c < nr) {
             const RowState old = P.ws_h[srow0 + c];
             const float m = fin_w[c];
@@ -742,17 +785,17 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
   }
 }
 
-template <int MODE>
+template <int MODE, int NK>
 cudaError_t launch_tc(const ChunkParams& p, int n_ctas, cudaStream_t stream) {
   using C = TcCfg<MODE>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e =
-        cudaFuncSetAttribute(chunk_attn_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaFuncSetAttribute(chunk_attn_tc<MODE, NK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  chunk_attn_tc<MODE><<<n_ctas, C::THREADS, C::SMEM, stream>>>(p);
+  chunk_attn_tc<MODE, NK><<<n_ctas, C::THREADS, C::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -766,8 +809,17 @@ int tc_max_ctas(int num_sms) { return num_sms; }  // one CTA per SM (shared memo
 
 cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int mode, int n_ctas, cudaStream_t stream) {
   if (n_ctas < 1) return cudaSuccess;
-  if (mode == kSingle) return launch_tc<kSingle>(p, n_ctas, stream);
-  if (mode == kRowSplit) return launch_tc<kRowSplit>(p, n_ctas, stream);
+  const int R = p.group * p.n_query;
+  if (mode == kSingle) {  // one pass of R <= 32 rows: compute ceil(R / 8) column blocks
+    if (R < 1 || R > TcCfg<kSingle>::ROWS) return cudaErrorInvalidValue;
+    switch ((R + 7) / 8) {
+      case 1: return launch_tc<kSingle, 1>(p, n_ctas, stream);
+      case 2: return launch_tc<kSingle, 2>(p, n_ctas, stream);
+      case 3: return launch_tc<kSingle, 3>(p, n_ctas, stream);
+      default: return launch_tc<kSingle, 4>(p, n_ctas, stream);
+    }
+  }
+  if (mode == kRowSplit) return launch_tc<kRowSplit, 4>(p, n_ctas, stream);
   return cudaErrorInvalidValue;
 }
 
