@@ -7,20 +7,22 @@
 // merged into the running state (Eq. 8).
 //
 // Shape of the work.  A KV tile of 128 tokens sits on the MMA M dimension and
-// the (padded) query rows on N, so a small query group (20-64 rows) does not
-// waste a 128-row MMA:
-//   S^T  = K_tile . Q^T      M = 128 tokens, N = NCOL rows, K = d      (TMEM)
+// the (padded) query rows of a pass on N (32 or 64), so a small query group
+// (20-64 rows) does not waste a 128-row MMA:
+//   S^T  = K_tile . Q^T      M = 128 tokens, N = rows, K = d           (TMEM)
 //   P^T  = 2^(S^T*scale - m) per row, written bf16 to shared memory
-//   O^T  = V_tile^T . P^T    M = d = 128,    N = NCOL rows, K = 128 tokens (TMEM)
+//   O^T  = V_tile^T . P^T    M = d = 128,    N = rows, K = 128 tokens  (TMEM)
 // and the fp32 output accumulator lives in registers (thread = one of the 128
 // output dimensions), updated one tile behind the MMAs: acc = acc*alpha + O^T.
 //
-// Warp roles (192 threads, one CTA per SM):
-//   warps 0-3  softmax and accumulation; thread t owns TMEM lane t (token t of
-//              the S tile, output dimension t of the O tile)
-//   warp 4     producer: 16-byte cp.async of K/V tiles into a ring of stages,
-//              written in the 128-byte-swizzled layout the MMA descriptors name
-//   warp 5     one thread issues the MMAs and their commits
+// Warp roles (one CTA per SM; NWG = 1 or 2 softmax warpgroups of 32 rows each):
+//   warps 0 .. 4NWG-1  softmax and accumulation: a thread holds 4 tokens x 8 rows
+//                      of an S tile and one output dimension of an O tile
+//   warp 4NWG          K producer, warp 4NWG+1 V producer: 16-byte cp.async of
+//                      tiles into their rings, written in the 128-byte-swizzled
+//                      layout the MMA descriptors name
+//   warp 4NWG+2        one thread issues the MMAs and their commits, each product
+//                      as soon as its inputs are ready
 // Work split: "stream-K" over the tiles of all (part, KV head, row block)
 // pairs, so every CTA gets the same number of tiles; a CTA that covers part of
 // a pair writes that segment's state into its own state slot, and the finish
@@ -57,21 +59,25 @@ struct TcCfg {
   static constexpr int NCOL = 32;                          // query rows per softmax warpgroup
   static constexpr int NWG = (MODE == kSingle) ? 1 : 2;   // softmax warpgroups
   static constexpr int ROWS = NWG * NCOL;                  // query rows per pass: the MMA N of both products
-  static constexpr int THREADS = 32 * (4 * NWG + 2);
-  static constexpr int STAGES = 3;
+  static constexpr int THREADS = 32 * (4 * NWG + 3);
+  // K and V tiles sit in two rings of their own: a K slot is refilled as soon as its tile's S product
+  // completes, a V slot once the PV product completes.
+  static constexpr int KST = (MODE == kSingle) ? 3 : 2;  // K slots
+  static constexpr int VST = 3;                          // V slots
   static constexpr int Q_BYTES = ROWS * D * 2;
-  // P^T of a tile (all rows of the pass) is written into that tile's own K buffer: K is dead once the
-  // tile's S product has completed, and the stage is recycled only after its PV product.
-  static constexpr int P_BYTES = ROWS * TOK * 2;
-  static constexpr int OFF_KV = 0;
-  static constexpr int OFF_Q = STAGES * 2 * TILE_BYTES;
+  static constexpr int P_BYTES = ROWS * TOK * 2;  // P^T of a tile (all rows of the pass), two buffers
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = KST * TILE_BYTES;
+  static constexpr int OFF_P = OFF_V + VST * TILE_BYTES;
+  static constexpr int OFF_Q = OFF_P + 2 * P_BYTES;
   // per softmax warpgroup:
   static constexpr int OFF_RED = OFF_Q + Q_BYTES;                  // float [NWG][4][NCOL]
   static constexpr int OFF_MNEW = OFF_RED + NWG * 4 * NCOL * 4;    // float [NWG][NCOL]: reference max per row
   static constexpr int OFF_ALPHA = OFF_MNEW + NWG * NCOL * 4;      // float [NWG][2][NCOL]
   static constexpr int OFF_FIN = OFF_ALPHA + NWG * 2 * NCOL * 4;   // float [NWG][2][NCOL]: final m, l
-  static constexpr int N_BAR = 2 * STAGES + 5 * 2 + 2;
-  static constexpr int OFF_BAR = OFF_FIN + NWG * 2 * NCOL * 4;
+  static constexpr int N_BAR = 2 * KST + 2 * VST + 5 * 2 + 2;
+  static constexpr int OFF_HDR = OFF_FIN + NWG * 2 * NCOL * 4;   // RowState [NWG][NCOL]: slot headers read back
+  static constexpr int OFF_BAR = OFF_HDR + NWG * NCOL * 16;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SMEM = BYTES + 1024;  // slack to align the base to 1024 bytes
@@ -80,8 +86,8 @@ struct TcCfg {
   static constexpr uint32_t TMEM_COLS = 4 * ROWS;
   static constexpr uint32_t S_COL = 0;
   static constexpr uint32_t O_COL = 2 * ROWS;
-  static_assert(OFF_Q % 1024 == 0 && P_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0 && P_BYTES <= TILE_BYTES,
-                "swizzle atoms need 1 KiB alignment; P^T must fit in a K tile");
+  static_assert(OFF_Q % 1024 == 0 && P_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0,
+                "swizzle atoms need 1 KiB alignment");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
@@ -169,10 +175,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -346,8 +348,9 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
 
   // mbarriers: FULL/EMPTY per stage; SFULL, SEMPTY, PFULL, OFULL, OEMPTY per buffer; QFULL; DRAIN
   const uint32_t bar0 = base + C::OFF_BAR;
-  const uint32_t FULL = bar0, EMPTY = bar0 + 8u * C::STAGES;
-  const uint32_t SFULL = bar0 + 16u * C::STAGES, SEMPTY = SFULL + 16u, PFULL = SEMPTY + 16u, OFULL = PFULL + 16u,
+  const uint32_t KFULL = bar0, KEMPTY = KFULL + 8u * C::KST, VFULL = KEMPTY + 8u * C::KST,
+                 VEMPTY = VFULL + 8u * C::VST;
+  const uint32_t SFULL = VEMPTY + 8u * C::VST, SEMPTY = SFULL + 16u, PFULL = SEMPTY + 16u, OFULL = PFULL + 16u,
                  OEMPTY = OFULL + 16u, QFULL = OEMPTY + 16u,
                  DRAIN = QFULL + 8u;
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_MISC);
@@ -355,11 +358,16 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
   float* mnew = reinterpret_cast<float*>(gbase + C::OFF_MNEW);
   float* alpha = reinterpret_cast<float*>(gbase + C::OFF_ALPHA);
   float* fin = reinterpret_cast<float*>(gbase + C::OFF_FIN);
+  const RowState* hdr = reinterpret_cast<const RowState*>(gbase + C::OFF_HDR);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(FULL + 8u * s, 32);
-      mbar_init(EMPTY + 8u * s, 1);
+    for (int s = 0; s < C::KST; ++s) {
+      mbar_init(KFULL + 8u * s, 32);
+      mbar_init(KEMPTY + 8u * s, 1);
+    }
+    for (int s = 0; s < C::VST; ++s) {
+      mbar_init(VFULL + 8u * s, 32);
+      mbar_init(VEMPTY + 8u * s, 1);
     }
     for (int b = 0; b < 2; ++b) {  // tile parity
       mbar_init(SFULL + 8u * b, 1);
@@ -386,8 +394,12 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
   const int64_t x_end = cta_tile_begin(blockIdx.x + 1, gridDim.x, T);
   const int64_t kv_stride = static_cast<int64_t>(P.n_kv_heads) * D;
 
-  if (warp == 4 * NWG) {
-    // ---------------- producer: K/V tiles into the stage ring
+  if (warp == 4 * NWG || warp == 4 * NWG + 1) {
+    // ---------------- producers: warp 4*NWG fills the K ring, warp 4*NWG+1 the V ring
+    const bool is_v = warp == 4 * NWG + 1;
+    const int nst = is_v ? C::VST : C::KST;
+    const uint32_t ring = base + (is_v ? C::OFF_V : C::OFF_K);
+    const uint32_t full = is_v ? VFULL : KFULL, empty = is_v ? VEMPTY : KEMPTY;
     int hint = 0;
     int64_t i = 0;
     bool ok = true;
@@ -395,41 +407,46 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       const Seg sg = seg_at(P, x, x_end, hint);
       const PartDesc& pd = P.parts[sg.part];
       const int64_t n_tok = pd.n_tok;
-      const __nv_bfloat16* kb = pd.k + static_cast<int64_t>(sg.g) * D;
-      const __nv_bfloat16* vb = pd.v + static_cast<int64_t>(sg.g) * D;
+      const __nv_bfloat16* src = (is_v ? pd.v : pd.k) + static_cast<int64_t>(sg.g) * D;
       for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
-        const int stage = static_cast<int>(i % C::STAGES);
-        const uint32_t use = static_cast<uint32_t>(i / C::STAGES);
-        if (i >= C::STAGES && !W.wait(EMPTY + 8u * stage, (use - 1u) & 1u)) {
+        const int slot = static_cast<int>(i % nst);
+        const uint32_t use = static_cast<uint32_t>(i / nst);
+        if (i >= nst && !W.wait(empty + 8u * slot, (use - 1u) & 1u)) {
           ok = false;
           break;
         }
         const int64_t tok0 = (sg.tile0 + t) * TOK;
-        const uint32_t kdst = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES;
-        const uint32_t vdst = kdst + TILE_BYTES;
+        const uint32_t dst = ring + static_cast<uint32_t>(slot) * TILE_BYTES;
         // lane copies 16-byte piece c = lane % 16 of rows r0 + 2j (j < 64); rows past n_tok read nothing
         const int c = lane & 15, r0 = lane >> 4;
         const int64_t valid_rows = (n_tok - tok0 < TOK) ? (n_tok - tok0) : static_cast<int64_t>(TOK);
-        const __nv_bfloat16* ks = kb + (tok0 + r0) * kv_stride + c * 8;
-        const __nv_bfloat16* vs = vb + (tok0 + r0) * kv_stride + c * 8;
+        const __nv_bfloat16* ps = src + (tok0 + r0) * kv_stride + c * 8;
         const int64_t step = 2 * kv_stride;
         const uint32_t so0 = static_cast<uint32_t>(c >> 3) * HALF_BYTES + static_cast<uint32_t>(r0) * 128u;
+        if (valid_rows == TOK) {
+#pragma unroll 16
+          for (int j = 0; j < 64; ++j) {
+            const int row = r0 + 2 * j;
+            cp_async16(dst + so0 + static_cast<uint32_t>(j) * 256u + (static_cast<uint32_t>((c & 7) ^ (row & 7)) << 4),
+                       ps, 16);
+            ps += step;
+          }
+        } else {
 #pragma unroll 8
-        for (int j = 0; j < 64; ++j) {
-          const int row = r0 + 2 * j;
-          const uint32_t so = so0 + static_cast<uint32_t>(j) * 256u + (static_cast<uint32_t>((c & 7) ^ (row & 7)) << 4);
-          const bool in = row < valid_rows;
-          cp_async16(kdst + so, in ? ks : kb, in ? 16 : 0);
-          cp_async16(vdst + so, in ? vs : vb, in ? 16 : 0);
-          ks += step;
-          vs += step;
+          for (int j = 0; j < 64; ++j) {
+            const int row = r0 + 2 * j;
+            const bool in = row < valid_rows;
+            cp_async16(dst + so0 + static_cast<uint32_t>(j) * 256u + (static_cast<uint32_t>((c & 7) ^ (row & 7)) << 4),
+                       in ? ps : src, in ? 16 : 0);
+            ps += step;
+          }
         }
-        cp_async_arrive_noinc(FULL + 8u * stage);
+        cp_async_arrive_noinc(full + 8u * slot);
       }
       x += sg.n_tiles;
     }
     cp_async_wait_all();
-  } else if (warp == 4 * NWG + 1) {
+  } else if (warp == 4 * NWG + 2) {
     // ---------------- MMA issuer (one thread)
     if (lane == 0) {
       constexpr int ROWS = C::ROWS;
@@ -438,7 +455,8 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       const uint32_t qa = desc_lo(base + C::OFF_Q, 16);
       // S^T of tile j: K tile (A, K-major) x the pass's Q rows (B, K-major)
       auto issue_s = [&](int64_t j) {
-        const uint32_t kaddr = base + C::OFF_KV + static_cast<uint32_t>(j % C::STAGES) * 2u * TILE_BYTES;
+        const int slot = static_cast<int>(j % C::KST);
+        const uint32_t kaddr = base + C::OFF_K + static_cast<uint32_t>(slot) * TILE_BYTES;
         fence_proxy_async();  // cp.async writes (generic proxy) before tensor-core reads (async proxy)
         tc_fence_after();
         const uint32_t d = tmem + C::S_COL + static_cast<uint32_t>(j & 1) * ROWS;
@@ -448,22 +466,24 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
           mma_bf16(d, ka + desc_adv((kk >> 2) * HALF_BYTES + (kk & 3) * 32),
                    qa + desc_adv((kk >> 2) * (ROWS * 128) + (kk & 3) * 32), kDescHi, idesc_s, kk > 0 ? 1u : 0u);
         mma_commit(SFULL + 8u * static_cast<uint32_t>(j & 1));
+        mma_commit(KEMPTY + 8u * static_cast<uint32_t>(slot));  // the K slot is free when this fires
       };
-      // O^T of tile j: V tile (A, dimension-major) x P^T (B, K-major, in the tile's K buffer)
+      // O^T of tile j: V tile (A, dimension-major) x P^T (B, K-major)
       auto issue_pv = [&](int64_t j) {
-        const int stage = static_cast<int>(j % C::STAGES);
-        const uint32_t kaddr = base + C::OFF_KV + static_cast<uint32_t>(stage) * 2u * TILE_BYTES;
+        const int slot = static_cast<int>(j % C::VST);
+        const uint32_t vaddr = base + C::OFF_V + static_cast<uint32_t>(slot) * TILE_BYTES;
+        const uint32_t paddr = base + C::OFF_P + static_cast<uint32_t>(j & 1) * C::P_BYTES;
         fence_proxy_async();  // P^T was written with ordinary stores
         tc_fence_after();
         const uint32_t d = tmem + C::O_COL + static_cast<uint32_t>(j & 1) * ROWS;
         // A = V^T: 64-dimension halves 16 KiB apart (LBO), 8-token groups 1 KiB apart (SBO)
-        const uint32_t va = desc_lo(kaddr + TILE_BYTES, HALF_BYTES), pa = desc_lo(kaddr, 16);
+        const uint32_t va = desc_lo(vaddr, HALF_BYTES), pa = desc_lo(paddr, 16);
 #pragma unroll
         for (int kk = 0; kk < TOK / 16; ++kk)
           mma_bf16(d, va + desc_adv(kk * 2048), pa + desc_adv((kk >> 2) * (ROWS * 128) + (kk & 3) * 32), kDescHi,
                    idesc_o, kk > 0 ? 1u : 0u);
         mma_commit(OFULL + 8u * static_cast<uint32_t>(j & 1));
-        mma_commit(EMPTY + 8u * static_cast<uint32_t>(stage));  // the stage's products are done when this fires
+        mma_commit(VEMPTY + 8u * static_cast<uint32_t>(slot));  // the V slot (and P^T buffer) is free when this fires
       };
       // Issue whichever product is ready, so a tile's PV never waits behind the next tile's data.
       // S(j) needs tile j's data, its segment's Q (first tile of a segment) and S buffer j&1 read by
@@ -483,8 +503,8 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
             ++seg_idx;
             tc_fence_after();
           }
-          if (sn < seg_end && mbar_test(FULL + 8u * static_cast<uint32_t>(sn % C::STAGES),
-                                        static_cast<uint32_t>(sn / C::STAGES) & 1u) &&
+          if (sn < seg_end && mbar_test(KFULL + 8u * static_cast<uint32_t>(sn % C::KST),
+                                        static_cast<uint32_t>(sn / C::KST) & 1u) &&
               (sn < 2 || mbar_test(SEMPTY + 8u * static_cast<uint32_t>(sn & 1),
                                    (static_cast<uint32_t>(sn >> 1) & 1u) ^ 1u))) {
             issue_s(sn++);
@@ -492,6 +512,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
           }
         }
         if (pn < sn && mbar_test(PFULL + 8u * static_cast<uint32_t>(pn & 1), static_cast<uint32_t>(pn >> 1) & 1u) &&
+            mbar_test(VFULL + 8u * static_cast<uint32_t>(pn % C::VST), static_cast<uint32_t>(pn / C::VST) & 1u) &&
             (pn < 2 ||
              mbar_test(OEMPTY + 8u * static_cast<uint32_t>(pn & 1), (static_cast<uint32_t>(pn >> 1) & 1u) ^ 1u))) {
           issue_pv(pn++);
@@ -537,6 +558,8 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     float* mref = mnew + wg * NCOL;  // running reference maximum per row, shared by the warpgroup
     float* alpha_w = alpha + wg * 2 * NCOL;
     float* fin_w = fin + wg * 2 * NCOL;
+    const RowState* hdr_w = hdr + wg * NCOL;  // the slot's previous headers of this warpgroup's rows
+    const uint32_t hdr_s = base + C::OFF_HDR + static_cast<uint32_t>(wg * NCOL) * 16u;
     // shared address of row lane%8 of P^T matrix lane/8 (token block 4*q4 + lane/8) for column block 0
     // (the pass's P^T has C::ROWS rows; this warpgroup's start at row wg * NCOL)
     const int tb = 4 * q4 + (lane >> 3), pr = lane & 7;
@@ -573,31 +596,42 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       return true;
     };
 
+    // This warpgroup's 32 Q rows of a pass into shared memory (K-major swizzled [ROWS][128], padding
+    // rows zero) with cp.async; QFULL completes when every softmax thread's copies have landed.
+    int hint_q = 0;
+    auto load_q = [&](int64_t xq) {
+      const Seg sq = seg_at(P, xq, x_end, hint_q);
+      const int rblk = sq.rb * C::ROWS;
+      const int nrows = min(C::ROWS, P.group * P.n_query - rblk);
+      const int64_t qrow0 = (static_cast<int64_t>(P.parts[sq.part].req) * P.n_q_heads +
+                             static_cast<int64_t>(sq.g) * P.group) * P.n_query + rblk;
+#pragma unroll
+      for (int idx = tid; idx < NCOL * 16; idx += 128) {
+        const int c = wg * NCOL + (idx >> 4), ch = idx & 15;
+        const bool in = c < nrows;
+        cp_async16(base + C::OFF_Q + swz_offset(c, ch, C::ROWS * 128), in ? P.q + (qrow0 + c) * D + ch * 8 : P.q,
+                   in ? 16 : 0);
+      }
+      cp_async_arrive_noinc(QFULL);
+    };
+    bool q_loaded = false;  // the current segment's Q was fetched during the previous segment
+
     for (int64_t x = x_begin; x < x_end;) {
-      // all softmax threads meet here: nobody still needs the previous segment's Q, and a wait that
-      // gave up anywhere stops every warpgroup together
+      // all softmax threads meet here, so a wait that gave up anywhere stops every warpgroup together
       if (!bar_all(3u, 128u * NWG, ok)) break;
       const Seg sg = seg_at(P, x, x_end, hint);
       const PartDesc& pd = P.parts[sg.part];
       const int b = pd.req;
       const int R = P.group * P.n_query;
       const int rblk = sg.rb * C::ROWS;                          // first row of this pass
-      const int nrows = min(C::ROWS, R - rblk);                   // valid rows of the pass
       const int r0 = rblk + ((MODE == kRowSplit) ? wg * NCOL : 0);  // this warpgroup's first row
       nr = max(0, min(NCOL, R - r0));
       const int64_t qrow0 =
           (static_cast<int64_t>(b) * P.n_q_heads + static_cast<int64_t>(sg.g) * P.group) * P.n_query;
 
-      // Q rows of the pass into shared memory: K-major swizzled [ROWS][128], padding rows zero
-      for (int idx = threadIdx.x; idx < C::ROWS * 16; idx += 128 * NWG) {
-        const int c = idx >> 4, ch = idx & 15;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (c < nrows) v = *reinterpret_cast<const uint4*>(P.q + (qrow0 + rblk + c) * D + ch * 8);
-        st_shared_v4(base + C::OFF_Q + swz_offset(c, ch, C::ROWS * 128), v);
-      }
+      if (!q_loaded) load_q(x);
+      q_loaded = false;
       if (q4 == 0) mref[lane] = -INFINITY;
-      fence_proxy_async();
-      mbar_arrive(QFULL);
 
 #pragma unroll
       for (int c = 0; c < NCOL; ++c) acc[c] = 0.f;
@@ -690,10 +724,10 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
             }
         }
 
-        // P^T = 2^(s*scale - m) in bf16, into the K-major swizzled B operand of the PV product, which
-        // lives in this tile's K buffer (dead since the S products completed): one 8-column block per
+        // P^T = 2^(s*scale - m) in bf16, into the K-major swizzled B operand of the PV product (buffer
+        // i&1, last read by PV(i-2), which completed before accumulate(i-2) ran): one 8-column block per
         // stmatrix, its four 8x8 matrices being the thread's four 8-token blocks
-        const uint32_t pbase = base + C::OFF_KV + static_cast<uint32_t>(i % C::STAGES) * 2u * TILE_BYTES + p_thread;
+        const uint32_t pbase = base + C::OFF_P + static_cast<uint32_t>(i & 1) * C::P_BYTES + p_thread;
 #pragma unroll
         for (int k = 0; k < NK; ++k) {
           uint32_t pk[4];
@@ -709,6 +743,12 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
         }
         fence_proxy_async();
         mbar_arrive(PFULL + 8u * par);
+        // the segment's last S product has completed, so nothing reads Q any more: fetch the next
+        // segment's Q now, and the MMAs can start on it while this segment's state is written
+        if (t + 1 == sg.n_tiles && x + sg.n_tiles < x_end) {
+          load_q(x + sg.n_tiles);
+          q_loaded = true;
+        }
 
         // the previous tile's O one step behind, so the MMAs of tile i overlap the accumulation
         if (prev >= 0 && !accumulate(prev)) {
@@ -719,7 +759,11 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       }
       if (ok && prev >= 0) ok = accumulate(prev);
       if (ok && prev >= 0) {
-        // this warpgroup's segment state: m = mref, l = sum over threads, a = acc
+        // this warpgroup's segment state (m = mref, l = sum over threads, a = acc), merged into the
+        // slot's state when that is from this round (an earlier launch of the round)
+        const int slot = P.slot_base + sg.slot;
+        const int64_t srow0 = static_cast<int64_t>(slot) * P.slot_stride + qrow0 + r0;
+        if (tid < nr) cp_async16(hdr_s + static_cast<uint32_t>(tid) * 16u, P.ws_h + srow0 + tid, 16);
 #pragma unroll
         for (int j = 0; j < 2 * NK; ++j) {
           float v = lsum[j];
@@ -735,6 +779,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
             red_w[q4 * NCOL + 8 * k + 2 * lane + 1] = lsum[2 * k + 1];
           }
         }
+        cp_async_wait_all();
         bar_sync(bar_wg, 128);
         if (q4 == 0 && lane < NC) {
           const int c = lane;
@@ -742,39 +787,46 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
           fin_w[NCOL + c] = red_w[c] + red_w[NCOL + c] + red_w[2 * NCOL + c] + red_w[3 * NCOL + c];
         }
         bar_sync(bar_wg, 128);
-        const int slot = P.slot_base + sg.slot;
-        const int64_t srow0 = static_cast<int64_t>(slot) * P.slot_stride + qrow0 + r0;
+        // per 8-row block: the earlier accumulators first (independent loads), then the merged values
+        float* ap = P.ws_a + srow0 * D + tid;
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          if (c < nr) {
-            const RowState old = P.ws_h[srow0 + c];
-            const float m = fin_w[c];
-            float a = acc[c];
-            float* ap = P.ws_a + (srow0 + c) * D + tid;
-            if (old.epoch == P.epoch) {
-              const float mn = fmaxf(old.m, m);
-              if (mn != -INFINITY) a = *ap * exp2_approx(old.m - mn) + a * exp2_approx(m - mn);
+        for (int k = 0; k < NK; ++k) {
+          float olda[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int c = 8 * k + e;
+            olda[e] = (c < nr && hdr_w[c].epoch == P.epoch) ? ap[c * D] : 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int c = 8 * k + e;
+            if (c < nr) {
+              const float m = fin_w[c], mo = hdr_w[c].m;
+              float a = acc[c];
+              if (hdr_w[c].epoch == P.epoch) {
+                const float mn = fmaxf(mo, m);
+                if (mn != -INFINITY) a = olda[e] * exp2_approx(mo - mn) + a * exp2_approx(m - mn);
+              }
+              ap[c * D] = a;
             }
-            *ap = a;
           }
         }
-        bar_sync(bar_wg, 128);  // every thread of the warpgroup has read the old headers (and fin)
         if (tid < nr) {
-          RowState* hp = P.ws_h + srow0 + tid;
-          const RowState old = *hp;
           float m = fin_w[tid], l = fin_w[NCOL + tid];
-          if (old.epoch == P.epoch) {
-            const float mn = fmaxf(old.m, m);
+          const RowState oldh = hdr_w[tid];
+          if (oldh.epoch == P.epoch) {
+            const float mn = fmaxf(oldh.m, m);
             if (mn != -INFINITY) {
-              l = old.l * exp2_approx(old.m - mn) + l * exp2_approx(m - mn);
+              l = oldh.l * exp2_approx(oldh.m - mn) + l * exp2_approx(m - mn);
               m = mn;
             }
           }
-          *hp = RowState{m, l, P.epoch, 0u};
+          P.ws_h[srow0 + tid] = RowState{m, l, P.epoch, 0u};
         }
       }
       x += sg.n_tiles;
     }
+    cp_async_wait_all();  // a Q prefetch still in flight (a wait gave up) lands before the CTA exits
   }
 
   tc_fence_before();

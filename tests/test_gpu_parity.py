@@ -41,6 +41,8 @@ SMALL = [
     W.Workload("kscale", 4, 32, 8, 128, (777, 2048, 5, 4000), 512, 7, k_head_scale=True, seed=18),
     W.Workload("r48", 2, 16, 2, 128, (700, 1300), 256, 6, seed=22),   # 48 rows: row split, 16 idle
     W.Workload("r96", 2, 16, 4, 128, (500, 901), 128, 24, seed=23),   # 96 rows: two passes, last half empty
+    W.Workload("r12", 2, 8, 4, 128, (600, 1025), 256, 6, seed=24),    # 12 rows: two 8-row column blocks
+    W.Workload("r16", 3, 16, 8, 128, (129, 2000, 64), 512, 8, seed=25),  # 16 rows, exactly two blocks
 ]
 
 
