@@ -283,23 +283,43 @@ struct Seg {
   int64_t n_tiles;
 };
 
+// Even split of the T tiles of a launch over G CTAs in 32-bit arithmetic (the host keeps T below
+// 2^31): CTA k holds tiles [begin(k), begin(k + 1)) with begin(k) = floor(k T / G) = k q + floor(k r / G)
+// for T = q G + r -- the same split as cta_tile_begin.
+struct Split {
+  uint32_t T, G, q, r;
+  __device__ Split(uint32_t t, uint32_t g) : T(t), G(g), q(t / g), r(t % g) {}
+  __device__ uint32_t begin(uint32_t k) const { return k * q + (k * r) / G; }
+  // the CTA holding tile x: the largest k with begin(k) <= x (a float estimate, then exact steps)
+  __device__ uint32_t cta_of(uint32_t x) const {
+    uint32_t k = static_cast<uint32_t>(static_cast<float>(x) * (static_cast<float>(G) / static_cast<float>(T)));
+    if (k >= G) k = G - 1;
+    while (k + 1 < G && begin(k + 1) <= x) ++k;
+    while (k > 0 && begin(k) > x) --k;
+    return k;
+  }
+};
+
 // The segment of this CTA that starts at global tile x: it runs to the end of
 // its (part, head, row block) pair or to the end of the CTA's range.
-__device__ __forceinline__ Seg seg_at(const ChunkParams& P, int64_t x, int64_t x_end, int& hint) {
+__device__ __forceinline__ Seg seg_at(const ChunkParams& P, const Split& sp, int64_t x64, int64_t x_end, int& hint) {
+  const uint32_t x = static_cast<uint32_t>(x64);
   int i = hint;
-  while (i + 1 < P.n_parts && P.parts[i + 1].tile_base <= x) ++i;
+  while (i + 1 < P.n_parts && static_cast<uint32_t>(P.parts[i + 1].tile_base) <= x) ++i;
   hint = i;
-  const int64_t nt = (static_cast<int64_t>(P.parts[i].n_tok) + TOK - 1) / TOK;
-  const int64_t local = x - P.parts[i].tile_base;
-  const int64_t pair = local / nt;
+  const uint32_t nt = (static_cast<uint32_t>(P.parts[i].n_tok) + TOK - 1) / TOK;
+  const uint32_t base_i = static_cast<uint32_t>(P.parts[i].tile_base);
+  const uint32_t local = x - base_i;
+  const uint32_t pair = local / nt;
+  const uint32_t nrb = static_cast<uint32_t>(P.n_rowblk);
   Seg s;
   s.part = i;
-  s.g = static_cast<int>(pair / P.n_rowblk);
-  s.rb = static_cast<int>(pair % P.n_rowblk);
-  s.tile0 = local % nt;
-  const int64_t first = P.parts[i].tile_base + pair * nt;
-  s.n_tiles = min(x_end, first + nt) - x;
-  s.slot = static_cast<int>(static_cast<int64_t>(blockIdx.x) - cta_of_tile(first, gridDim.x, P.total_tiles));
+  s.g = static_cast<int>(pair / nrb);
+  s.rb = static_cast<int>(pair - (pair / nrb) * nrb);
+  s.tile0 = local - pair * nt;
+  const uint32_t first = base_i + pair * nt;
+  s.n_tiles = min(x_end, static_cast<int64_t>(first) + nt) - x64;
+  s.slot = static_cast<int>(blockIdx.x - sp.cta_of(first));
   return s;
 }
 
@@ -390,8 +410,9 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
   Waiter W{misc + 1, P.err};
 
   const int64_t T = P.total_tiles;
-  const int64_t x_begin = cta_tile_begin(blockIdx.x, gridDim.x, T);
-  const int64_t x_end = cta_tile_begin(blockIdx.x + 1, gridDim.x, T);
+  const Split split(static_cast<uint32_t>(T), gridDim.x);
+  const int64_t x_begin = split.begin(blockIdx.x);
+  const int64_t x_end = split.begin(blockIdx.x + 1);
   const int64_t kv_stride = static_cast<int64_t>(P.n_kv_heads) * D;
 
   if (warp == 4 * NWG || warp == 4 * NWG + 1) {
@@ -404,7 +425,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     int64_t i = 0;
     bool ok = true;
     for (int64_t x = x_begin; x < x_end && ok;) {
-      const Seg sg = seg_at(P, x, x_end, hint);
+      const Seg sg = seg_at(P, split, x, x_end, hint);
       const PartDesc& pd = P.parts[sg.part];
       const int64_t n_tok = pd.n_tok;
       const __nv_bfloat16* src = (is_v ? pd.v : pd.k) + static_cast<int64_t>(sg.g) * D;
@@ -499,7 +520,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
         bool progress = false;
         if (sn < n_local) {
           if (sn == seg_end && mbar_test(QFULL, seg_idx & 1u)) {
-            seg_end = sn + seg_at(P, x_begin + sn, x_end, hint).n_tiles;
+            seg_end = sn + seg_at(P, split, x_begin + sn, x_end, hint).n_tiles;
             ++seg_idx;
             tc_fence_after();
           }
@@ -600,7 +621,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     // rows zero) with cp.async; QFULL completes when every softmax thread's copies have landed.
     int hint_q = 0;
     auto load_q = [&](int64_t xq) {
-      const Seg sq = seg_at(P, xq, x_end, hint_q);
+      const Seg sq = seg_at(P, split, xq, x_end, hint_q);
       const int rblk = sq.rb * C::ROWS;
       const int nrows = min(C::ROWS, P.group * P.n_query - rblk);
       const int64_t qrow0 = (static_cast<int64_t>(P.parts[sq.part].req) * P.n_q_heads +
@@ -619,7 +640,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     for (int64_t x = x_begin; x < x_end;) {
       // all softmax threads meet here, so a wait that gave up anywhere stops every warpgroup together
       if (!bar_all(3u, 128u * NWG, ok)) break;
-      const Seg sg = seg_at(P, x, x_end, hint);
+      const Seg sg = seg_at(P, split, x, x_end, hint);
       const PartDesc& pd = P.parts[sg.part];
       const int b = pd.req;
       const int R = P.group * P.n_query;
@@ -862,6 +883,7 @@ int tc_max_ctas(int num_sms) { return num_sms; }  // one CTA per SM (shared memo
 cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int mode, int n_ctas, cudaStream_t stream) {
   if (n_ctas < 1) return cudaSuccess;
   const int R = p.group * p.n_query;
+  if (p.total_tiles > INT32_MAX) return cudaErrorInvalidValue;  // the kernel splits tiles in 32-bit arithmetic
   if (mode == kSingle) {  // one pass of R <= 32 rows: compute ceil(R / 8) column blocks
     if (R < 1 || R > TcCfg<kSingle>::ROWS) return cudaErrorInvalidValue;
     switch ((R + 7) / 8) {
