@@ -34,7 +34,7 @@ struct __align__(16) RowState {
 struct PartDesc {
   const __nv_bfloat16* k;  // [n_tok][Hkv][d]
   const __nv_bfloat16* v;
-  int64_t tile_base;  // tensor-core kernel: first global tile index of this part
+  int64_t tile_base;  // tensor-core kernel: first tile of this part in a CTA group's tile sequence
   int32_t req;
   int32_t n_tok;
 };
@@ -45,7 +45,7 @@ struct ChunkParams {
   float* ws_a;             // [slots][slot_stride][d]
   int* err;                // device error word (bounded waits that gave up)
   int64_t slot_stride;     // state rows per slot (max_req * Hq * max_query)
-  int64_t total_tiles;     // tensor-core kernel: tiles over all (part, head, row block)
+  int64_t total_tiles;     // tensor-core kernel: tiles of one CTA group (all parts, one head and row block)
   float q_scale;           // softmax scale * log2(e)
   uint32_t epoch;          // this round
   int32_t n_q_heads;
@@ -56,6 +56,10 @@ struct ChunkParams {
   int32_t slot_base; // state slot of split / segment 0
   int32_t n_parts;
   int32_t n_rowblk;  // CTAs (FMA) or segments (tensor core) per (part, head) along the query rows
+  // tensor-core kernel: the grid is n_kv_heads * n_rowblk CTA groups of ctas_per_group CTAs; group
+  // (head g, row block rb) = blockIdx / ctas_per_group walks the tiles of every part for that head
+  // and row block, split evenly over its CTAs
+  int32_t ctas_per_group;
   PartDesc parts[kMaxPartsPerLaunch];
 };
 
@@ -103,6 +107,11 @@ int tc_mode(int rows);
 int tc_rows_per_pass(int mode);
 int tc_slots_per_segment(int mode);
 int tc_max_ctas(int num_sms);
+// Work plan of a tensor-core launch over the parts already in p (n_tok set): sets n_rowblk, each
+// part's tile_base, total_tiles and ctas_per_group for at most `cta_budget` CTAs, with no part
+// spreading over more than kHistSlots state slots in its group.  Returns the grid size (CTA groups
+// x CTAs per group) and the number of state slots used in *slots.
+int64_t tc_plan(ChunkParams& p, int mode, int64_t cta_budget, int64_t* slots);
 cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int mode, int n_ctas, cudaStream_t stream);
 
 }  // namespace svx

@@ -256,17 +256,6 @@ int choose_splits(svx_ctx c, int n_parts, int64_t max_tok, int n_rowblk) {
 
 // Largest number of CTAs that one (part, head, row block) pair spreads over
 // when T tiles are split evenly over n CTAs.
-int64_t max_segments(const std::vector<int64_t>& pair_first, const std::vector<int64_t>& pair_tiles, int64_t n,
-                     int64_t T) {
-  int64_t worst = 0;
-  for (size_t i = 0; i < pair_first.size(); ++i) {
-    const int64_t a = svx::cta_of_tile(pair_first[i], n, T);
-    const int64_t b = svx::cta_of_tile(pair_first[i] + pair_tiles[i] - 1, n, T);
-    worst = std::max(worst, b - a + 1);
-  }
-  return worst;
-}
-
 uint32_t nonempty_splits(int64_t n_tok, int splits) {
   const int64_t n_tiles = (n_tok + svx::kTile - 1) / svx::kTile;
   uint32_t m = 0;
@@ -437,28 +426,11 @@ svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, int cta_cap) {
     p.n_parts = n;
     for (int i = 0; i < n; ++i) p.parts[i] = parts[i0 + i];
     if (c->use_tc) {
-      // tensor-core kernel: tiles of all (part, head, row block) pairs split evenly over the CTAs
       const int mode = svx::tc_mode(R);
-      const int rpp = svx::tc_rows_per_pass(mode);
-      p.n_rowblk = (R + rpp - 1) / rpp;
-      std::vector<int64_t> pair_first, pair_tiles;
-      int64_t T = 0;
-      for (int i = 0; i < n; ++i) {
-        const int64_t nt = (static_cast<int64_t>(p.parts[i].n_tok) + svx::kTcTile - 1) / svx::kTcTile;
-        p.parts[i].tile_base = T;
-        for (int pr = 0; pr < c->cfg.n_kv_heads * p.n_rowblk; ++pr) {
-          pair_first.push_back(T + pr * nt);
-          pair_tiles.push_back(nt);
-        }
-        T += nt * c->cfg.n_kv_heads * p.n_rowblk;
-      }
-      p.total_tiles = T;
-      int64_t ctas = std::min<int64_t>(svx::tc_max_ctas(c->num_sms), T);
-      if (cta_cap > 0) ctas = std::min<int64_t>(ctas, cta_cap);
-      // every CTA segment of a pair writes tc_slots_per_segment state slots
-      const int sps = svx::tc_slots_per_segment(mode);
-      while (ctas > 1 && max_segments(pair_first, pair_tiles, ctas, T) * sps > svx::kHistSlots) --ctas;
-      const int64_t slots = max_segments(pair_first, pair_tiles, ctas, T) * sps;
+      int64_t budget = svx::tc_max_ctas(c->num_sms);
+      if (cta_cap > 0) budget = std::min<int64_t>(budget, cta_cap);
+      int64_t slots = 0;
+      const int64_t ctas = svx::tc_plan(p, mode, budget, &slots);
       for (int i = 0; i < n; ++i) {
         uint32_t& used = c->slot_mask[static_cast<size_t>(p.parts[i].req)];
         used |= (slots >= 32 ? 0xffffffffu : ((1u << slots) - 1u));

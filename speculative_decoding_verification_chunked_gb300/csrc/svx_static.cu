@@ -178,31 +178,8 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
     cudaError_t e;
     if (head_dim == 128) {
       const int mode = svx::tc_mode(R);
-      const int rpp = svx::tc_rows_per_pass(mode);
-      p.n_rowblk = (R + rpp - 1) / rpp;
-      int64_t T = 0;
-      for (int i = 0; i < n; ++i) {
-        const int64_t nt = (static_cast<int64_t>(p.parts[i].n_tok) + svx::kTcTile - 1) / svx::kTcTile;
-        p.parts[i].tile_base = T;
-        T += nt * n_kv_heads * p.n_rowblk;
-      }
-      p.total_tiles = T;
-      // CTAs such that no (part, head, row block) pair spreads over more state slots than there are
-      int64_t ctas = std::min<int64_t>(svx::tc_max_ctas(num_sms), T);
-      auto segs_for = [&](int64_t c) {
-        int64_t worst = 0;
-        for (int i = 0; i < n; ++i) {
-          const int64_t nt = (static_cast<int64_t>(p.parts[i].n_tok) + svx::kTcTile - 1) / svx::kTcTile;
-          for (int64_t pr = 0; pr < static_cast<int64_t>(n_kv_heads) * p.n_rowblk; ++pr) {
-            const int64_t first = p.parts[i].tile_base + pr * nt;
-            worst = std::max(worst, svx::cta_of_tile(first + nt - 1, c, T) - svx::cta_of_tile(first, c, T) + 1);
-          }
-        }
-        return worst;
-      };
-      const int sps = svx::tc_slots_per_segment(mode);
-      while (ctas > 1 && segs_for(ctas) * sps > svx::kHistSlots) --ctas;
-      const int64_t slots = segs_for(ctas) * sps;
+      int64_t slots = 0;
+      const int64_t ctas = svx::tc_plan(p, mode, svx::tc_max_ctas(num_sms), &slots);
       for (int i = 0; i < n; ++i) slot_mask[p.parts[i].req] |= (1u << slots) - 1u;
       e = svx::launch_chunk_attn_tc(p, mode, static_cast<int>(ctas), s);
     } else {

@@ -33,6 +33,8 @@
 // copies and MMAs, free TMEM and exit.
 #include <math.h>
 
+#include <algorithm>
+
 #include "svx_internal.h"
 
 namespace svx {
@@ -61,9 +63,11 @@ struct TcCfg {
   static constexpr int ROWS = NWG * NCOL;                  // query rows per pass: the MMA N of both products
   static constexpr int THREADS = 32 * (4 * NWG + 3);
   // K and V tiles sit in two rings of their own: a K slot is refilled as soon as its tile's S product
-  // completes, a V slot once the PV product completes.
-  static constexpr int KST = (MODE == kSingle) ? 3 : 2;  // K slots
-  static constexpr int VST = 3;                          // V slots
+  // completes, a V slot once the PV product completes.  With one CTA per SM, 2 + 3 slots keep ~24 MB
+  // of loads in flight on the whole GPU: enough for the HBM rate at its loaded latency, while a third
+  // K slot (~29 MB) only lengthened DRAM queues and cost 7% (qwen3 shape, one GB300).
+  static constexpr int KST = 2;  // K slots
+  static constexpr int VST = 3;  // V slots
   static constexpr int Q_BYTES = ROWS * D * 2;
   static constexpr int P_BYTES = ROWS * TOK * 2;  // P^T of a tile (all rows of the pass), two buffers
   static constexpr int OFF_K = 0;
@@ -300,26 +304,23 @@ struct Split {
   }
 };
 
-// The segment of this CTA that starts at global tile x: it runs to the end of
-// its (part, head, row block) pair or to the end of the CTA's range.
-__device__ __forceinline__ Seg seg_at(const ChunkParams& P, const Split& sp, int64_t x64, int64_t x_end, int& hint) {
+// The segment of this CTA that starts at tile x of its group's sequence (the tiles of every part
+// for the group's head and row block): it runs to the end of the part or to the end of the CTA's range.
+__device__ __forceinline__ Seg seg_at(const ChunkParams& P, const Split& sp, int grp, int64_t x64, int64_t x_end,
+                                      int& hint) {
   const uint32_t x = static_cast<uint32_t>(x64);
   int i = hint;
   while (i + 1 < P.n_parts && static_cast<uint32_t>(P.parts[i + 1].tile_base) <= x) ++i;
   hint = i;
   const uint32_t nt = (static_cast<uint32_t>(P.parts[i].n_tok) + TOK - 1) / TOK;
-  const uint32_t base_i = static_cast<uint32_t>(P.parts[i].tile_base);
-  const uint32_t local = x - base_i;
-  const uint32_t pair = local / nt;
-  const uint32_t nrb = static_cast<uint32_t>(P.n_rowblk);
+  const uint32_t first = static_cast<uint32_t>(P.parts[i].tile_base);
   Seg s;
   s.part = i;
-  s.g = static_cast<int>(pair / nrb);
-  s.rb = static_cast<int>(pair - (pair / nrb) * nrb);
-  s.tile0 = local - pair * nt;
-  const uint32_t first = base_i + pair * nt;
+  s.g = grp / P.n_rowblk;
+  s.rb = grp - s.g * P.n_rowblk;
+  s.tile0 = x - first;
   s.n_tiles = min(x_end, static_cast<int64_t>(first) + nt) - x64;
-  s.slot = static_cast<int>(blockIdx.x - sp.cta_of(first));
+  s.slot = static_cast<int>(static_cast<uint32_t>(blockIdx.x - grp * P.ctas_per_group) - sp.cta_of(first));
   return s;
 }
 
@@ -410,9 +411,13 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
   Waiter W{misc + 1, P.err};
 
   const int64_t T = P.total_tiles;
-  const Split split(static_cast<uint32_t>(T), gridDim.x);
-  const int64_t x_begin = split.begin(blockIdx.x);
-  const int64_t x_end = split.begin(blockIdx.x + 1);
+  // this CTA's group (KV head, row block) and its share of the group's tiles; CTA j of every group
+  // covers the same token ranges, so the heads of a request are read in step
+  const int grp = static_cast<int>(blockIdx.x) / P.ctas_per_group;
+  const uint32_t jg = blockIdx.x - static_cast<uint32_t>(grp * P.ctas_per_group);
+  const Split split(static_cast<uint32_t>(T), static_cast<uint32_t>(P.ctas_per_group));
+  const int64_t x_begin = split.begin(jg);
+  const int64_t x_end = split.begin(jg + 1);
   const int64_t kv_stride = static_cast<int64_t>(P.n_kv_heads) * D;
 
   if (warp == 4 * NWG || warp == 4 * NWG + 1) {
@@ -425,7 +430,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     int64_t i = 0;
     bool ok = true;
     for (int64_t x = x_begin; x < x_end && ok;) {
-      const Seg sg = seg_at(P, split, x, x_end, hint);
+      const Seg sg = seg_at(P, split, grp, x, x_end, hint);
       const PartDesc& pd = P.parts[sg.part];
       const int64_t n_tok = pd.n_tok;
       const __nv_bfloat16* src = (is_v ? pd.v : pd.k) + static_cast<int64_t>(sg.g) * D;
@@ -520,7 +525,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
         bool progress = false;
         if (sn < n_local) {
           if (sn == seg_end && mbar_test(QFULL, seg_idx & 1u)) {
-            seg_end = sn + seg_at(P, split, x_begin + sn, x_end, hint).n_tiles;
+            seg_end = sn + seg_at(P, split, grp, x_begin + sn, x_end, hint).n_tiles;
             ++seg_idx;
             tc_fence_after();
           }
@@ -621,7 +626,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     // rows zero) with cp.async; QFULL completes when every softmax thread's copies have landed.
     int hint_q = 0;
     auto load_q = [&](int64_t xq) {
-      const Seg sq = seg_at(P, split, xq, x_end, hint_q);
+      const Seg sq = seg_at(P, split, grp, xq, x_end, hint_q);
       const int rblk = sq.rb * C::ROWS;
       const int nrows = min(C::ROWS, P.group * P.n_query - rblk);
       const int64_t qrow0 = (static_cast<int64_t>(P.parts[sq.part].req) * P.n_q_heads +
@@ -640,7 +645,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     for (int64_t x = x_begin; x < x_end;) {
       // all softmax threads meet here, so a wait that gave up anywhere stops every warpgroup together
       if (!bar_all(3u, 128u * NWG, ok)) break;
-      const Seg sg = seg_at(P, split, x, x_end, hint);
+      const Seg sg = seg_at(P, split, grp, x, x_end, hint);
       const PartDesc& pd = P.parts[sg.part];
       const int b = pd.req;
       const int R = P.group * P.n_query;
@@ -879,6 +884,35 @@ int tc_mode(int rows) { return rows <= TcCfg<kSingle>::ROWS ? kSingle : kRowSpli
 int tc_rows_per_pass(int mode) { return mode == kRowSplit ? TcCfg<kRowSplit>::ROWS : TcCfg<kSingle>::ROWS; }
 int tc_slots_per_segment(int) { return 1; }
 int tc_max_ctas(int num_sms) { return num_sms; }  // one CTA per SM (shared memory)
+
+int64_t tc_plan(ChunkParams& p, int mode, int64_t cta_budget, int64_t* slots) {
+  const int R = p.group * p.n_query;
+  const int rpp = tc_rows_per_pass(mode);
+  p.n_rowblk = (R + rpp - 1) / rpp;
+  // one CTA group per (head, row block); each group's tiles (that head and row block of every part,
+  // part after part) are split evenly over its CTAs, so CTA j of every group covers the same tokens
+  const int64_t groups = static_cast<int64_t>(p.n_kv_heads) * p.n_rowblk;
+  int64_t T = 0;
+  for (int i = 0; i < p.n_parts; ++i) {
+    p.parts[i].tile_base = T;
+    T += (static_cast<int64_t>(p.parts[i].n_tok) + TOK - 1) / TOK;
+  }
+  p.total_tiles = T;
+  auto segments = [&](int64_t cpg) {  // the most CTA segments any part spreads over
+    int64_t worst = 0;
+    for (int i = 0; i < p.n_parts; ++i) {
+      const int64_t first = p.parts[i].tile_base, nt = (static_cast<int64_t>(p.parts[i].n_tok) + TOK - 1) / TOK;
+      worst = std::max(worst, cta_of_tile(first + nt - 1, cpg, T) - cta_of_tile(first, cpg, T) + 1);
+    }
+    return worst;
+  };
+  int64_t cpg = std::min<int64_t>(std::max<int64_t>(1, cta_budget / groups), T);
+  const int sps = tc_slots_per_segment(mode);
+  while (cpg > 1 && segments(cpg) * sps > kHistSlots) --cpg;
+  *slots = segments(cpg) * sps;
+  p.ctas_per_group = static_cast<int32_t>(cpg);
+  return groups * cpg;
+}
 
 cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int mode, int n_ctas, cudaStream_t stream) {
   if (n_ctas < 1) return cudaSuccess;
