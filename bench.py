@@ -466,6 +466,12 @@ def main(argv=None):
     # ---- value: resident history (HBM-bound form)
     clk = ClockSampler(local).__enter__()  # sampled over both timed regions
     ms_res, kern_ms = timed(resident_step, steps, warmup, with_events=True)
+    # The streamed phases run without the other layers' device-resident duplicates: a streaming deployment
+    # does not hold its history in HBM twice, and 35 GiB of them slowed the host-to-device copies of the
+    # full-depth round.  Layer 0's copy stays for the overlap comparison.
+    for ly in layers[1:]:
+        ly["kh_d"] = ly["vh_d"] = ly["res_pushes"] = ly["res_plan_pushes"] = None
+    torch.cuda.empty_cache()
     value, ms_res_job = job_throughput(B * nq, ms_res, world, dev)
     toks_per_launch = [sum(n for _, _, n, _, _ in p) for p in layers[0]["res_pushes"]]
     k1_ms_per_launch = statistics.mean(kern_ms)
