@@ -65,7 +65,7 @@ struct ChunkParams {
 
 // Finish kernel: candidate region, merge and finalize.
 struct FinishParams {
-  const RowState* ws_h;
+  RowState* ws_h;  // headers are read, then marked unwritten (epoch 0)
   const float* ws_a;
   int64_t slot_stride;
   __nv_bfloat16* o;              // [B][Hq][nq][d]

@@ -306,12 +306,14 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
   }
 
   uint32_t mask = P.slot_mask[b];
+  uint32_t used = 0u;
   while (mask) {
     const int s = __ffs(mask) - 1;
     mask &= mask - 1;
     const int64_t idx = static_cast<int64_t>(s) * P.slot_stride + row;
     const RowState hs = P.ws_h[idx];
     if (hs.epoch != P.epoch) continue;  // slot not written for this row in this round
+    used |= 1u << s;
     const float mn = fmaxf(m, hs.m);
     if (mn == kNegInf) continue;
     const float al = exp2_approx(m - mn), be = exp2_approx(hs.m - mn);
@@ -320,6 +322,16 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
     for (int c = 0; c < VPL; ++c) a[c] = a[c] * al + ap[c] * be;
     l = l * al + hs.l * be;
     m = mn;
+  }
+  // The row's slot states are consumed: mark them unwritten (epoch 0), so that nothing later takes
+  // them for its own -- in particular a CUDA graph replay of this round, which reuses its epoch.
+  __syncwarp();
+  if (lane == 0) {
+    while (used) {
+      const int s = __ffs(used) - 1;
+      used &= used - 1;
+      P.ws_h[static_cast<int64_t>(s) * P.slot_stride + row].epoch = 0u;
+    }
   }
   __nv_bfloat16* op = P.o + row * D + lane * VPL;
   if (l > 0.f) {

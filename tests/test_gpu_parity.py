@@ -66,6 +66,24 @@ def test_tile_edges_tensor_core_path(svx, hist):
     check_parity(o, l, *oracle_out(w, x))
 
 
+# Tile-split corner cases of the tensor-core kernel: more (KV head, row pass) CTA groups than SMs
+# (160 groups of one CTA, two waves), and one long request that would spread over more state slots
+# than there are (the grid shrinks until it spans at most 8).
+SPLIT_EDGES = [
+    W.Workload("groups160", 1, 320, 40, 128, (300,), 128, 32, seed=26),
+    W.Workload("long1", 1, 32, 8, 128, (60000,), 8192, 5, seed=27),
+]
+
+
+@pytest.mark.parametrize("w", SPLIT_EDGES, ids=[w.name for w in SPLIT_EDGES])
+@pytest.mark.parametrize("resident", [False, True], ids=["streamed", "resident"])
+def test_tile_split_edges(svx, w, resident):
+    x, t = gpu_inputs(w, resident=resident)
+    with make_verifier(svx, w) as v:
+        o, l = run_gpu(v, w, t, x)
+    check_parity(o, l, *oracle_out(w, x))
+
+
 def test_chunk_order_does_not_matter(svx):
     w = SMALL[1]
     x, t = gpu_inputs(w)
