@@ -35,6 +35,13 @@
  * destroyed.
  *
  * Threads: a context is used by one host thread at a time.
+ *
+ * CUDA graphs: a round whose parts are all device memory or zero-copy host memory enqueues work on
+ * the compute stream only, so svx_round_begin .. svx_round_finish (timeout_ms = 0) may be captured
+ * into a CUDA graph on that stream and replayed; each replay computes the round on the captured
+ * buffers' current contents.  Capture after one eager round (kernel set-up happens on first use).
+ * Rounds that stage pinned host parts through the copy engine wait on events recorded by earlier
+ * rounds and cannot be captured.
  */
 #ifndef SVX_H
 #define SVX_H

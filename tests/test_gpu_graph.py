@@ -30,14 +30,15 @@ def _copy_inputs(dst, src):
             a.copy_(b)
 
 
+@pytest.mark.parametrize("zero_copy", [False, True], ids=["device_history", "zero_copy_history"])
 @pytest.mark.parametrize("chunk", [512, 4096], ids=["several_pushes", "one_push"])
-def test_resident_round_replays_from_a_cuda_graph(svx, chunk):
+def test_round_replays_from_a_cuda_graph(svx, chunk, zero_copy):
     import torch
     w = W.Workload("graph", 3, 16, 4, 128, (700, 1500, 129), chunk, 5, seed=41)
-    x0, t0 = gpu_inputs(w, layer=0, resident=True)
-    x1, t1 = gpu_inputs(w, layer=1, resident=True)
+    x0, t0 = gpu_inputs(w, layer=0, resident=not zero_copy)
+    x1, t1 = gpu_inputs(w, layer=1, resident=not zero_copy)
     keep = {k: (v.clone() if not isinstance(v, list) else [None if e is None else e.clone() for e in v])
-            for k, v in t0.items()}
+            for k, v in t0.items()}  # (host history is copied to pageable memory: only a source here)
     B, Hq, nq, d = w.n_req, w.n_q_heads, w.n_query, w.head_dim
     o = torch.empty((B, Hq, nq, d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((B, Hq, nq), dtype=torch.float32, device="cuda")
@@ -52,7 +53,7 @@ def test_resident_round_replays_from_a_cuda_graph(svx, chunk):
         return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
     with svx.Verifier(w.n_req, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_query, w.chunk_tokens, n_slots=2,
-                      compute_stream=cs) as v:
+                      compute_stream=cs, zero_copy=zero_copy) as v:
         round_(v)  # eager round first: kernels configured, reference for the replays
         check_parity(*out(), *oracle_out(w, x0))
         g = torch.cuda.CUDAGraph()
