@@ -49,7 +49,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["svx", "reference"], default="svx")
     ap.add_argument("--workload", default="qwen3", choices=["tiny", "qwen3", "internlm", "tree", "fulldepth"])
-    ap.add_argument("--zero-copy-ctas", default="0,32",
+    ap.add_argument("--zero-copy-ctas", default="0,8,32",
                     help="comma list of CTA caps for the zero-copy streamed variant (0 = all SMs; empty = skip)")
     ap.add_argument("--no-draft-load", dest="draft_load", action="store_false",
                     help="skip timing the streamed round beside a low-priority bf16 GEMM loop (Target priority)")
