@@ -465,7 +465,11 @@ def main(argv=None):
     warmup = a.warmup if L == 1 else max(3, min(a.warmup, 5))
     # ---- value: resident history (HBM-bound form)
     clk = ClockSampler(local).__enter__()  # sampled over both timed regions
-    ms_res, kern_ms = timed(resident_step, steps, warmup, with_events=True)
+    # the value without per-launch events (an event record between two kernels of a round keeps the
+    # second from being launched early); then the same steps with events around every chunk launch for
+    # the roofline
+    ms_res, _ = timed(resident_step, steps, warmup)
+    _, kern_ms = timed(resident_step, steps, 1, with_events=True)
     # The streamed phases run without the other layers' device-resident duplicates: a streaming deployment
     # does not hold its history in HBM twice, and 35 GiB of them slowed the host-to-device copies of the
     # full-depth round.  Layer 0's copy stays for the overlap comparison.

@@ -15,6 +15,30 @@
 
 namespace svx {
 
+// Programmatic dependent launch.  Kernels launched with launch_pdl may start while the kernel before
+// them in the stream is still running; each calls grid_dependency_wait() before its first global
+// memory access (so it sees everything that kernel wrote, and what came before it in the stream) and
+// then allow_dependents(), so the next kernel's CTAs can be scheduled and set up early.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename Params>
+cudaError_t launch_pdl(void (*kernel)(Params), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       const Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+
 constexpr int kMaxReq = 256;
 constexpr int kMaxPartsPerLaunch = 64;  // keeps the kernel parameter block near 2.5 KiB
 constexpr int kHistSlots = 8;           // state slots per query row (history segments)

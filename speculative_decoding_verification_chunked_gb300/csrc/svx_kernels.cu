@@ -257,9 +257,15 @@ __global__ void __launch_bounds__(128) chunk_attn_fma(const __grid_constant__ Ch
 //      combined with Eq. (8).
 //   3. O = a / l (Eq. 9) as bf16, LSE = (m + log2 l) * ln 2 as fp32.
 // ---------------------------------------------------------------------------
+// 128-thread blocks (four rows): with the prefetched states and candidates a thread needs ~165
+// registers, and small blocks let three share an SM, so 1280 rows still fit in one wave.
+constexpr int kFinishThreads = 128;
+
 template <int D>
-__global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ FinishParams P) {
+__global__ void __launch_bounds__(kFinishThreads) finish_kernel(const __grid_constant__ FinishParams P) {
   constexpr int VPL = D / 32;
+  grid_dependency_wait();  // the chunk kernels' states (and every earlier write) are visible from here
+  allow_dependents();
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t n_rows = static_cast<int64_t>(P.n_req) * P.n_q_heads * P.n_query;
@@ -270,6 +276,26 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
   float m = kNegInf, l = 0.f, a[VPL];
 #pragma unroll
   for (int c = 0; c < VPL; ++c) a[c] = 0.f;
+
+  // The row's history states first: every header and accumulator load of the used slots is issued
+  // here, so their latency overlaps the candidate region below (stale slots are loaded and ignored).
+  const uint32_t smask = P.slot_mask[b];
+  RowState hs[kHistSlots];
+  float ha[kHistSlots][VPL];
+#pragma unroll
+  for (int s = 0; s < kHistSlots; ++s) {
+    hs[s] = RowState{kNegInf, 0.f, 0u, 0u};
+    if ((smask >> s) & 1u) {
+      const int64_t idx = static_cast<int64_t>(s) * P.slot_stride + row;
+      hs[s] = P.ws_h[idx];
+      const float* ap = P.ws_a + idx * D + lane * VPL;
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) ha[s][c] = ap[c];
+    } else {
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) ha[s][c] = 0.f;
+    }
+  }
 
   if (P.k_cand != nullptr) {
     uint32_t word;
@@ -288,39 +314,62 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
 #pragma unroll
     for (int c = 0; c < VPL; ++c) q[c] = __bfloat162float(qp[c]) * P.q_scale;
     const int g = h / P.group;
+    // visible candidates in batches of kCandBatch: all their K and V loads are issued first, so a
+    // batch costs one memory round trip instead of one per candidate
+    constexpr int kCandBatch = 8;
     while (word) {
-      const int i = __ffs(word) - 1;
-      word &= word - 1u;
-      const int64_t kv = ((static_cast<int64_t>(b) * P.n_cand + i) * P.n_kv_heads + g) * D + lane * VPL;
-      float dot = 0.f;
+      int idx[kCandBatch];
+      int nb = 0;
 #pragma unroll
-      for (int c = 0; c < VPL; ++c) dot = fmaf(q[c], __bfloat162float(P.k_cand[kv + c]), dot);
-      const float sc = warp_sum(dot);
-      const float mn = fmaxf(m, sc);
-      const float al = exp2_approx(m - mn), p = exp2_approx(sc - mn);
-      l = l * al + p;
+      for (int t = 0; t < kCandBatch; ++t) {
+        idx[t] = -1;
+        if (word) {
+          idx[t] = __ffs(word) - 1;
+          word &= word - 1u;
+          ++nb;
+        }
+      }
+      float kk[kCandBatch][VPL], vv[kCandBatch][VPL];
 #pragma unroll
-      for (int c = 0; c < VPL; ++c) a[c] = fmaf(p, __bfloat162float(P.v_cand[kv + c]), a[c] * al);
-      m = mn;
+      for (int t = 0; t < kCandBatch; ++t) {
+        if (idx[t] >= 0) {
+          const int64_t kv = ((static_cast<int64_t>(b) * P.n_cand + idx[t]) * P.n_kv_heads + g) * D + lane * VPL;
+#pragma unroll
+          for (int c = 0; c < VPL; ++c) {
+            kk[t][c] = __bfloat162float(P.k_cand[kv + c]);
+            vv[t][c] = __bfloat162float(P.v_cand[kv + c]);
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kCandBatch; ++t) {
+        if (t < nb) {
+          float dot = 0.f;
+#pragma unroll
+          for (int c = 0; c < VPL; ++c) dot = fmaf(q[c], kk[t][c], dot);
+          const float sc = warp_sum(dot);
+          const float mn = fmaxf(m, sc);
+          const float al = exp2_approx(m - mn), p = exp2_approx(sc - mn);
+          l = l * al + p;
+#pragma unroll
+          for (int c = 0; c < VPL; ++c) a[c] = fmaf(p, vv[t][c], a[c] * al);
+          m = mn;
+        }
+      }
     }
   }
 
-  uint32_t mask = P.slot_mask[b];
   uint32_t used = 0u;
-  while (mask) {
-    const int s = __ffs(mask) - 1;
-    mask &= mask - 1;
-    const int64_t idx = static_cast<int64_t>(s) * P.slot_stride + row;
-    const RowState hs = P.ws_h[idx];
-    if (hs.epoch != P.epoch) continue;  // slot not written for this row in this round
-    used |= 1u << s;
-    const float mn = fmaxf(m, hs.m);
-    if (mn == kNegInf) continue;
-    const float al = exp2_approx(m - mn), be = exp2_approx(hs.m - mn);
-    const float* ap = P.ws_a + idx * D + lane * VPL;
 #pragma unroll
-    for (int c = 0; c < VPL; ++c) a[c] = a[c] * al + ap[c] * be;
-    l = l * al + hs.l * be;
+  for (int s = 0; s < kHistSlots; ++s) {
+    if (!((smask >> s) & 1u) || hs[s].epoch != P.epoch) continue;  // slot not written for this row this round
+    used |= 1u << s;
+    const float mn = fmaxf(m, hs[s].m);
+    if (mn == kNegInf) continue;
+    const float al = exp2_approx(m - mn), be = exp2_approx(hs[s].m - mn);
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) a[c] = a[c] * al + ha[s][c] * be;
+    l = l * al + hs[s].l * be;
     m = mn;
   }
   // The row's slot states are consumed: mark them unwritten (epoch 0), so that nothing later takes
@@ -371,12 +420,11 @@ cudaError_t launch_chunk_attn(const ChunkParams& p, int head_dim, cudaStream_t s
 
 cudaError_t launch_finish(const FinishParams& p, int head_dim, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(p.n_req) * p.n_q_heads * p.n_query;
-  const int blocks = static_cast<int>((rows * 32 + 255) / 256);
+  const int blocks = static_cast<int>((rows * 32 + kFinishThreads - 1) / kFinishThreads);
   if (blocks == 0) return cudaSuccess;
-  if (head_dim == 128) finish_kernel<128><<<blocks, 256, 0, stream>>>(p);
-  else if (head_dim == 64) finish_kernel<64><<<blocks, 256, 0, stream>>>(p);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (head_dim == 128) return launch_pdl(finish_kernel<128>, dim3(blocks), dim3(kFinishThreads), 0, stream, p);
+  if (head_dim == 64) return launch_pdl(finish_kernel<64>, dim3(blocks), dim3(kFinishThreads), 0, stream, p);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace svx

@@ -408,6 +408,10 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  // everything above touched only shared memory and TMEM; global memory only after the kernel
+  // before this one in the stream has completed
+  grid_dependency_wait();
+  allow_dependents();
   Waiter W{misc + 1, P.err};
 
   const int64_t T = P.total_tiles;
@@ -873,8 +877,7 @@ cudaError_t launch_tc(const ChunkParams& p, int n_ctas, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  chunk_attn_tc<MODE, NK><<<n_ctas, C::THREADS, C::SMEM, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(chunk_attn_tc<MODE, NK>, dim3(n_ctas), dim3(C::THREADS), C::SMEM, stream, p);
 }
 
 }  // namespace

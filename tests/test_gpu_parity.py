@@ -43,6 +43,7 @@ SMALL = [
     W.Workload("r96", 2, 16, 4, 128, (500, 901), 128, 24, seed=23),   # 96 rows: two passes, last half empty
     W.Workload("r12", 2, 8, 4, 128, (600, 1025), 256, 6, seed=24),    # 12 rows: two 8-row column blocks
     W.Workload("r16", 3, 16, 8, 128, (129, 2000, 64), 512, 8, seed=25),  # 16 rows, exactly two blocks
+    W.Workload("g1d128", 2, 8, 8, 128, (300, 129), 128, 3, seed=28),    # one query head per KV head
 ]
 
 
@@ -72,6 +73,8 @@ def test_tile_edges_tensor_core_path(svx, hist):
 SPLIT_EDGES = [
     W.Workload("groups160", 1, 320, 40, 128, (300,), 128, 32, seed=26),
     W.Workload("long1", 1, 32, 8, 128, (60000,), 8192, 5, seed=27),
+    # 70 requests: a push of more than 64 parts is split into several launches
+    W.Workload("req70", 70, 8, 2, 128, tuple(17 + 13 * i for i in range(70)), 256, 3, seed=29),
 ]
 
 
