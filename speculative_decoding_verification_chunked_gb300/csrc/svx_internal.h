@@ -18,7 +18,8 @@ namespace svx {
 // Programmatic dependent launch.  Kernels launched with launch_pdl may start while the kernel before
 // them in the stream is still running; each calls grid_dependency_wait() before its first global
 // memory access (so it sees everything that kernel wrote, and what came before it in the stream) and
-// then allow_dependents(), so the next kernel's CTAs can be scheduled and set up early.
+// allow_dependents() once the next kernel's CTAs may be scheduled: the chunk kernel when its work is
+// done, the short finish kernel at once.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -411,7 +411,6 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
   // everything above touched only shared memory and TMEM; global memory only after the kernel
   // before this one in the stream has completed
   grid_dependency_wait();
-  allow_dependents();
   Waiter W{misc + 1, P.err};
 
   const int64_t T = P.total_tiles;
@@ -859,6 +858,10 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     cp_async_wait_all();  // a Q prefetch still in flight (a wait gave up) lands before the CTA exits
   }
 
+  // The next kernel in the stream may be scheduled once every CTA got here.  Not earlier: a launch can
+  // run for milliseconds (streaming from host memory on a few SMs), and waiting dependents would hold
+  // the other SMs' resources against work on other streams.
+  allow_dependents();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
