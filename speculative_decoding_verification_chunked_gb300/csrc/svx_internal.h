@@ -117,8 +117,8 @@ __host__ __device__ inline int64_t split_tile_begin(int64_t n_tiles, int s, int 
   return (n_tiles * s) / splits;
 }
 
-// Tensor-core kernel work split ("stream-K" over tiles): CTA k of n owns the
-// global tiles [k*T/n, (k+1)*T/n); the CTA holding tile x is cta_of_tile(x).
+// Even split of T tiles over n CTAs (the tensor-core kernel's split inside a CTA group): CTA k owns
+// tiles [k*T/n, (k+1)*T/n); the CTA holding tile x is cta_of_tile(x).
 __host__ __device__ inline int64_t cta_tile_begin(int64_t k, int64_t n, int64_t T) { return (k * T) / n; }
 __host__ __device__ inline int64_t cta_of_tile(int64_t x, int64_t n, int64_t T) { return ((x + 1) * n - 1) / T; }
 

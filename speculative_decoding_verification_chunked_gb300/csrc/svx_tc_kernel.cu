@@ -23,9 +23,11 @@
 //                      layout the MMA descriptors name
 //   warp 4NWG+2        one thread issues the MMAs and their commits, each product
 //                      as soon as its inputs are ready
-// Work split: "stream-K" over the tiles of all (part, KV head, row block)
-// pairs, so every CTA gets the same number of tiles; a CTA that covers part of
-// a pair writes that segment's state into its own state slot, and the finish
+// Work split: one CTA group per (KV head, row block); a group's tiles (that head
+// and row block of every part, part after part) are split evenly over its CTAs
+// ("stream-K" inside the group), so CTA j of every group covers the same tokens
+// and the heads of a request are read in step.  A CTA that covers part of a
+// part writes that segment's state into its own state slot, and the finish
 // kernel merges the slots.
 //
 // Every mbarrier wait is bounded (2 s of global time); a wait that gives up
