@@ -85,8 +85,11 @@ typedef struct {
   void* compute_stream;     /* cudaStream_t for kernels; NULL: library creates one (highest priority) */
   void* copy_stream;        /* cudaStream_t for H2D chunk copies; NULL: library creates one */
   uint32_t flags;           /* SVX_FLAG_* */
-  int32_t zero_copy_ctas;   /* with SVX_FLAG_ZERO_COPY: CTAs (one per SM) of a launch that reads host
-                               parts; 0 = all SMs.  Fewer leave SMs free for co-running work. */
+  int32_t zero_copy_ctas;   /* with SVX_FLAG_ZERO_COPY: CTA budget (one CTA per SM) of a launch that
+                               reads host parts; 0 = all SMs.  A head-dim-128 launch uses
+                               max(1, budget / groups) CTAs for each of its groups (one per KV head
+                               and pass of up to 64 query rows).  Fewer leave SMs free for
+                               co-running work; on GB300, 8 CTAs already fill the host link. */
 } svx_config;
 
 /* One request's contiguous slice of committed history, [tok_start, tok_start + n_tok).
