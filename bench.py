@@ -338,23 +338,32 @@ def main(argv=None):
     bf = torch.bfloat16
 
     # ---- inputs: per layer, history in pinned host memory (streamed) and in device memory (resident)
+    def batched_host(lengths, src=None):
+        """The requests' histories as rows of one pinned [B][C_max][Hkv][d] tensor (views of C_b
+        tokens each), the layout of a batched host KV cache: a chunk's parts are then equally strided
+        and the library stages each chunk with one 2D copy for K and one for V."""
+        big = torch.empty((len(lengths), max(lengths), Hkv, d), dtype=bf, pin_memory=True)
+        views = [big[b_, :C] for b_, C in enumerate(lengths)]
+        if src is not None:
+            for v_, t_ in zip(views, src):
+                v_.copy_(t_)
+        return views
+
     layers = []
     x0 = None
     for l in range(L):
         if L == 1:
-            pinned = lambda s: torch.empty(s, dtype=torch.int16, pin_memory=True).numpy().view(np.uint16)  # noqa
-            x = W.layer_inputs(w, l, hist_alloc=pinned)
+            x = W.layer_inputs(w, l)  # numpy draws; the streamed copies live in batched pinned tensors
             x0 = x
             t16 = lambda arr: torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(bf)  # noqa: E731
             q_h, kc_h, vc_h = (t16(arr).pin_memory() for arr in (x.q, x.k_cand, x.v_cand))
-            kh_h = [t16(k) for k in x.k_hist]
-            vh_h = [t16(v) for v in x.v_hist]
+            kh_h = batched_host(w.hist_len, [t16(k) for k in x.k_hist])
+            vh_h = batched_host(w.hist_len, [t16(v) for v in x.v_hist])
             kh_d = [k.to(dev) for k in kh_h]
             vh_d = [v.to(dev) for v in vh_h]
             parent = x.parent
         else:
-            kh_h = [torch.empty((C, Hkv, d), dtype=bf, pin_memory=True) for C in w.hist_len]
-            vh_h = [torch.empty((C, Hkv, d), dtype=bf, pin_memory=True) for C in w.hist_len]
+            kh_h, vh_h = batched_host(w.hist_len), batched_host(w.hist_len)
             q, kh_d, vh_d, kc, vc, parent = W.layer_inputs_device(w, l, dev)
             for b in range(B):
                 kh_h[b].copy_(kh_d[b])

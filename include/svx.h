@@ -162,7 +162,8 @@ typedef struct {
   int64_t h2d_bytes;      /* history bytes copied from host this round */
   int64_t device_bytes;   /* history bytes read in place from device memory this round */
   int32_t n_chunk_launches;
-  int32_t n_copies;
+  int32_t n_copies;       /* host-to-device copy calls issued: two per host part, or two per chunk when
+                             its host parts are equally strided rows of one batched tensor (2D copies) */
   double chunk_kernel_exposed_ms; /* chunk-kernel time outside every H2D copy interval of the round;
                                      1 - exposed / chunk_kernel_ms is the compute hidden under transfer */
 } svx_stats;

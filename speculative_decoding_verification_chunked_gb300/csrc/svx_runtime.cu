@@ -33,6 +33,7 @@ thread_local std::string g_create_error;
 enum class RoundState { kIdle, kOpen };
 
 constexpr int kCopyStreams = 4;  // the copy stream and three more (see svx_ctx_s::xs_more)
+constexpr ptrdiff_t kMaxCopyPitch = ptrdiff_t(1) << 31;  // larger source strides: one copy per part
 
 struct PushEvents {
   cudaEvent_t copy0, copy1, k0, k1;
@@ -545,19 +546,70 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
     for (auto s : c->xs_more) SVX_CUDA(c, cudaStreamWaitEvent(s, c->fork_ev[si], 0));
     size_t nc = 0;  // copies issued; copy n goes to stream n % kCopyStreams
     auto copy_stream = [&]() { const size_t k = nc++ % kCopyStreams; return k == 0 ? c->xs : c->xs_more[k - 1]; };
-    int hi = 0;
-    for (int i = 0; i < n_parts; ++i) {
-      if (kind[static_cast<size_t>(i)] != 1) continue;
+    // Host part h goes to slot position h: K at 2h * part_elems, V right after it.  When the host parts
+    // have one length and their K (and V) pointers are equally strided in increasing order -- the
+    // requests' rows of one batched [B][C][Hkv][d] tensor -- one 2D copy moves all K parts and one
+    // all V parts (qwen3 chunks: 208 GB/s against 192 GB/s for 4 MiB copies one by one).
+    std::vector<int> host_idx;
+    for (int i = 0; i < n_parts; ++i)
+      if (kind[static_cast<size_t>(i)] == 1) host_idx.push_back(i);
+    const size_t dpitch = static_cast<size_t>(2 * c->part_elems) * 2;
+    const size_t row_bytes = static_cast<size_t>(row_elems) * 2;
+    bool strided = host_idx.size() > 1;
+    ptrdiff_t sk = 0, sv = 0;
+    if (strided) {
+      const svx_part& p0 = parts[host_idx[0]];
+      const char* k0 = static_cast<const char*>(p0.k);
+      const char* v0 = static_cast<const char*>(p0.v);
+      sk = static_cast<const char*>(parts[host_idx[1]].k) - k0;
+      sv = static_cast<const char*>(parts[host_idx[1]].v) - v0;
+      const ptrdiff_t width = static_cast<ptrdiff_t>(p0.n_tok) * static_cast<ptrdiff_t>(row_bytes);
+      strided = sk >= width && sv >= width && sk <= kMaxCopyPitch && sv <= kMaxCopyPitch;
+      for (size_t h = 1; strided && h < host_idx.size(); ++h) {
+        const svx_part& p = parts[host_idx[h]];
+        strided = p.n_tok == p0.n_tok && static_cast<const char*>(p.k) - k0 == static_cast<ptrdiff_t>(h) * sk &&
+                  static_cast<const char*>(p.v) - v0 == static_cast<ptrdiff_t>(h) * sv;
+      }
+    }
+    __nv_bfloat16* const slot_base = c->slot_buf[static_cast<size_t>(slot)];
+    // A 2D copy reads only its rows, each a whole part inside its own pinned allocation.  When the rows
+    // belong to different allocations the driver refuses the call (invalid value, nothing enqueued);
+    // those parts are then copied one by one.
+    auto copy_2d = [&](__nv_bfloat16* dst, const void* src, ptrdiff_t spitch, bool& ok) -> svx_status {
+      if (!ok) return SVX_OK;
+      const size_t width = static_cast<size_t>(parts[host_idx[0]].n_tok) * row_bytes;
+      const cudaError_t e = cudaMemcpy2DAsync(dst, dpitch, src, static_cast<size_t>(spitch), width, host_idx.size(),
+                                              cudaMemcpyHostToDevice, copy_stream());
+      if (e == cudaSuccess) {
+        c->n_copies += 1;
+        return SVX_OK;
+      }
+      if (e != cudaErrorInvalidValue) return fail(c, SVX_ERR_CUDA, "cudaMemcpy2DAsync failed: %s", cudaGetErrorString(e));
+      cudaGetLastError();
+      ok = false;
+      return SVX_OK;
+    };
+    bool k2d = strided, v2d = strided;
+    svx_status cst = copy_2d(slot_base, strided ? parts[host_idx[0]].k : nullptr, sk, k2d);
+    if (cst != SVX_OK) return cst;
+    cst = copy_2d(slot_base + c->part_elems, strided ? parts[host_idx[0]].v : nullptr, sv, v2d);
+    if (cst != SVX_OK) return cst;
+    for (size_t h = 0; h < host_idx.size(); ++h) {
+      const int i = host_idx[h];
       const svx_part& p = parts[i];
-      __nv_bfloat16* dk = c->slot_buf[static_cast<size_t>(slot)] + static_cast<int64_t>(hi) * 2 * c->part_elems;
+      __nv_bfloat16* dk = slot_base + static_cast<int64_t>(h) * 2 * c->part_elems;
       __nv_bfloat16* dv = dk + c->part_elems;
-      const size_t bytes = static_cast<size_t>(p.n_tok) * row_elems * 2;
-      SVX_CUDA(c, cudaMemcpyAsync(dk, p.k, bytes, cudaMemcpyHostToDevice, copy_stream()));
-      SVX_CUDA(c, cudaMemcpyAsync(dv, p.v, bytes, cudaMemcpyHostToDevice, copy_stream()));
+      const size_t bytes = static_cast<size_t>(p.n_tok) * row_bytes;
+      if (!k2d) {
+        SVX_CUDA(c, cudaMemcpyAsync(dk, p.k, bytes, cudaMemcpyHostToDevice, copy_stream()));
+        c->n_copies += 1;
+      }
+      if (!v2d) {
+        SVX_CUDA(c, cudaMemcpyAsync(dv, p.v, bytes, cudaMemcpyHostToDevice, copy_stream()));
+        c->n_copies += 1;
+      }
       desc[static_cast<size_t>(i)] = PartDesc{dk, dv, 0, p.req, p.n_tok};
       c->h2d_bytes += 2 * static_cast<int64_t>(bytes);
-      c->n_copies += 2;
-      ++hi;
     }
     // join: the copy stream waits for the further ones, then marks the slot ready
     for (size_t k = 0; k < c->xs_more.size(); ++k) {
