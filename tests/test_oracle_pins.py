@@ -313,3 +313,37 @@ def test_round_bf16_matches_nearest_representable():
     # ties go to the even mantissa
     assert O.round_bf16(np.array([1 + 2 ** -8]))[0] == 1.0
     assert O.round_bf16(np.array([1 + 3 * 2 ** -8]))[0] == 1 + 2 ** -6
+
+
+def test_parity_bar_allows_only_the_bf16_output_rounding_beyond_the_tolerance():
+    """The GPU parity bar: O error beyond half a bf16 ulp of the exact value (max <= 1e-2, mean <=
+    1e-3), LSE error relative to max(|LSE|, 1).  Pinned on hand-made errors at the boundaries."""
+    import pytest as _pt
+    from helpers import bf16_half_ulp, check_parity
+    o_ref = np.zeros((1, 200))
+    o_ref[0, :4] = [4.075, 0.3, -1.5, 0.0]
+    l_ref = np.array([9.0, 0.001, -np.inf, 2.0])
+    assert np.allclose(bf16_half_ulp(o_ref[0, :4]), [2.0 ** -6, 2.0 ** -10, 2.0 ** -8, 0.0])
+
+    def bump(k, v):
+        o = o_ref.copy()
+        o[0, k] += v
+        return o
+    # 0.0156 of rounding at 4.075 plus 0.009 of error passes; 0.011 beyond it does not
+    check_parity(bump(0, 2.0 ** -6 + 0.009), l_ref, o_ref, l_ref)
+    with _pt.raises(AssertionError):
+        check_parity(bump(0, 2.0 ** -6 + 0.011), l_ref, o_ref, l_ref)
+    with _pt.raises(AssertionError):  # at 0.3 the rounding allowance is only 2^-10
+        check_parity(bump(1, 0.0115), l_ref, o_ref, l_ref)
+    with _pt.raises(AssertionError):  # the mean bar: 0.006 beyond rounding on every element
+        check_parity(o_ref + 0.006 + bf16_half_ulp(o_ref), l_ref, o_ref, l_ref)
+    # an LSE near zero is held to 1e-4 absolute, a large one to 1e-4 relative
+    check_parity(o_ref, l_ref + [8e-4, 9e-5, 0, 1.9e-4], o_ref, l_ref)
+    with _pt.raises(AssertionError):
+        check_parity(o_ref, l_ref + [0, 1.1e-4, 0, 0], o_ref, l_ref)
+    with _pt.raises(AssertionError):
+        check_parity(o_ref, l_ref + [1.0e-3, 0, 0, 0], o_ref, l_ref)
+    l_bad = l_ref.copy()
+    l_bad[2] = 0.0
+    with _pt.raises(AssertionError):  # -inf (nothing visible) must stay -inf
+        check_parity(o_ref, l_bad, o_ref, l_ref)
