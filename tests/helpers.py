@@ -90,3 +90,12 @@ def check_parity(o_gpu, l_gpu, o_ref, l_ref, rows=None):
     if rel.size:
         assert rel.max() <= LSE_REL, f"LSE err {rel.max():.3e} (relative to max(|LSE|, 1))"
     return float(err.max()), float(err.mean()), float(rel.max()) if rel.size else 0.0
+
+
+def sample_rows(w, n, seed=0):
+    """About n random (request, q-head, query) rows, plus the first and the last."""
+    rng = np.random.default_rng(seed)
+    rows = {(int(rng.integers(0, w.n_req)), int(rng.integers(0, w.n_q_heads)), int(rng.integers(0, w.n_query)))
+            for _ in range(n)}
+    rows |= {(w.n_req - 1, w.n_q_heads - 1, w.n_query - 1), (0, 0, 0)}
+    return sorted(rows)

@@ -5,7 +5,7 @@ batched host tensors) or read in place (zero-copy).  Every draw is fixed by its 
 import numpy as np
 import pytest
 
-from helpers import check_parity, gpu_inputs, oracle_out, run_gpu
+from helpers import check_parity, gpu_inputs, oracle_out, run_gpu, sample_rows
 from workloads import synth as W
 
 pytestmark = pytest.mark.gpu
@@ -61,3 +61,44 @@ def test_random_configuration(svx, i):
                       zero_copy=(mode == "zero_copy"), zero_copy_ctas=8 if i % 2 else 0) as v:
         o, l = run_gpu(v, w, t, x)
     check_parity(o, l, *oracle_out(w, x))
+
+
+N_LARGE = 8
+
+
+def draw_large_case(i):
+    """Long ragged histories (up to 60k tokens per request, up to 8 requests): many tiles per CTA
+    group, parts spread over several CTAs (and grids shrunk to the state-slot limit), several pushes."""
+    rng = np.random.default_rng([8, i])
+    B = int(rng.integers(1, 9))
+    hkv = int(rng.choice([2, 4, 8]))
+    G = int(rng.choice([1, 4, 8]))
+    nq = int(rng.integers(1, 17))
+    lens = tuple(int(x) for x in rng.integers(1, 60000, size=B))
+    chunk = int(rng.choice([2048, 8192, 65536]))
+    tree = bool(rng.random() < 0.4)
+    mode = ("resident", "streamed", "batched", "zero_copy")[i % 4]
+    w = W.Workload(f"large{i}", B, hkv * G, hkv, 128, lens, chunk, nq, tree=tree, seed=2000 + i)
+    return w, mode
+
+
+@pytest.mark.parametrize("i", range(N_LARGE))
+def test_random_large_configuration_sampled(svx, i):
+    import torch
+    w, mode = draw_large_case(i)
+    x, t = gpu_inputs(w, resident=(mode == "resident"))
+    if mode == "batched":
+        cmax = max(w.hist_len)
+        kb = torch.zeros((w.n_req, cmax, w.n_kv_heads, w.head_dim), dtype=torch.bfloat16).pin_memory()
+        vb = torch.zeros_like(kb).pin_memory()
+        for b, C in enumerate(w.hist_len):
+            kb[b, :C].copy_(t["kh"][b])
+            vb[b, :C].copy_(t["vh"][b])
+        t["kh"] = [kb[b, :C] for b, C in enumerate(w.hist_len)]
+        t["vh"] = [vb[b, :C] for b, C in enumerate(w.hist_len)]
+    with svx.Verifier(w.n_req, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_query, w.chunk_tokens, n_slots=3,
+                      zero_copy=(mode == "zero_copy"), zero_copy_ctas=8 if i % 2 else 0) as v:
+        o, l = run_gpu(v, w, t, x)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
+    rows = sample_rows(w, 32)
+    check_parity(o, l, *oracle_out(w, x, rows=rows), rows=rows)

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import workloads as W
-from helpers import check_parity, gpu_inputs, oracle_out, run_gpu
+from helpers import check_parity, gpu_inputs, oracle_out, run_gpu, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -228,14 +228,6 @@ def test_state_machine_and_argument_errors(svx):
 
 
 # ---------------------------------------------------------------- full size, sampled rows
-
-
-def sample_rows(w, n, seed=0):
-    rng = np.random.default_rng(seed)
-    rows = {(int(rng.integers(0, w.n_req)), int(rng.integers(0, w.n_q_heads)), int(rng.integers(0, w.n_query)))
-            for _ in range(n)}
-    rows |= {(w.n_req - 1, w.n_q_heads - 1, w.n_query - 1), (0, 0, 0)}
-    return sorted(rows)
 
 
 @pytest.mark.parametrize("name", ["qwen3", "internlm", "tree", "fulldepth"])
