@@ -197,6 +197,20 @@ svx_status svx_candidate_masks(int32_t n_req, int32_t n_query, const int32_t* pa
 svx_status svx_check_coverage(int32_t n_req, const int64_t* hist_len, const int64_t* parts, int64_t n_parts,
                               int32_t* ok_out);
 
+/* Work plan of one tensor-core chunk launch (head_dim 128), as svx_push_chunk makes it; host only.
+ * n_tok[n_parts] (1 <= n_parts <= 64): the parts' token counts; rows = G * n_query, the query rows
+ * per KV head; cta_budget >= 1: CTAs available (the SM count, or zero_copy_ctas).  The grid is
+ * n_groups = n_kv_heads * ceil(rows / rows_per_pass) CTA groups (one per KV head and pass of up to 64
+ * rows) of ctas_per_group CTAs; a group walks the 128-token tiles of every part for its head and
+ * pass, part after part (part i's first tile is tile_base[i] of tiles_per_group), and CTA j of a
+ * group takes tiles [floor(j T / c), floor((j + 1) T / c)) with T = tiles_per_group and c =
+ * ctas_per_group.  The grid shrinks until no part spans more than 8 CTAs (state slots); *slots is
+ * the most it spans.  Out: *grid, *n_groups, *ctas_per_group, *tiles_per_group, *slots,
+ * tile_base[n_parts].  SVX_ERR_INVALID_ARG on bad sizes or more than 2^31 - 1 tiles. */
+svx_status svx_plan_tc(int32_t n_parts, const int32_t* n_tok, int32_t n_kv_heads, int32_t rows, int64_t cta_budget,
+                       int64_t* grid, int32_t* n_groups, int32_t* ctas_per_group, int64_t* tiles_per_group,
+                       int32_t* slots, int64_t* tile_base);
+
 /* ---- a round that allocates nothing ------------------------------------------------------ */
 
 /* Size of the library's static device scratch array (per GPU, held until the process exits). */

@@ -828,4 +828,31 @@ svx_status svx_check_coverage(int32_t n_req, const int64_t* hist_len, const int6
   return SVX_OK;
 }
 
+svx_status svx_plan_tc(int32_t n_parts, const int32_t* n_tok, int32_t n_kv_heads, int32_t rows, int64_t cta_budget,
+                       int64_t* grid, int32_t* n_groups, int32_t* ctas_per_group, int64_t* tiles_per_group,
+                       int32_t* slots, int64_t* tile_base) {
+  if (n_parts < 1 || n_parts > svx::kMaxPartsPerLaunch || !n_tok || n_kv_heads < 1 || rows < 1 || cta_budget < 1 ||
+      !grid || !n_groups || !ctas_per_group || !tiles_per_group || !slots || !tile_base)
+    return SVX_ERR_INVALID_ARG;
+  ChunkParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.n_kv_heads = n_kv_heads;
+  p.group = rows;  // rows per KV head = group * n_query
+  p.n_query = 1;
+  p.n_parts = n_parts;
+  for (int i = 0; i < n_parts; ++i) {
+    if (n_tok[i] < 1) return SVX_ERR_INVALID_ARG;
+    p.parts[i].n_tok = n_tok[i];
+  }
+  int64_t used = 0;
+  *grid = svx::tc_plan(p, svx::tc_mode(rows), cta_budget, &used);
+  if (p.total_tiles > INT32_MAX) return SVX_ERR_INVALID_ARG;
+  *n_groups = static_cast<int32_t>(*grid / p.ctas_per_group);
+  *ctas_per_group = p.ctas_per_group;
+  *tiles_per_group = p.total_tiles;
+  *slots = static_cast<int32_t>(used);
+  for (int i = 0; i < n_parts; ++i) tile_base[i] = p.parts[i].tile_base;
+  return SVX_OK;
+}
+
 }  // extern "C"

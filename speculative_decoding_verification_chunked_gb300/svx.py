@@ -90,6 +90,10 @@ _SIGS = {
     "svx_check_coverage": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_int64),
                                           ctypes.POINTER(ctypes.c_int64), ctypes.c_int64,
                                           ctypes.POINTER(ctypes.c_int32)]),
+    "svx_plan_tc": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
+                                   ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32),
+                                   ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64),
+                                   ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)]),
     "svx_verify_static": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, _P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(_P),
                                          ctypes.POINTER(_P), _P, _P, ctypes.POINTER(ctypes.c_int32), ctypes.c_float,
@@ -180,6 +184,22 @@ def candidate_masks(n_req: int, n_query: int, parent: Optional[np.ndarray] = Non
     if st != OK:
         raise SvxError(st, "svx_candidate_masks: invalid tree or sizes")
     return out
+
+
+def plan_tc(n_tok: Sequence[int], n_kv_heads: int, rows: int, cta_budget: int) -> dict:
+    """Work plan of one tensor-core chunk launch (see svx_plan_tc): grid, n_groups, ctas_per_group,
+    tiles_per_group, slots and tile_base (per part)."""
+    n = len(n_tok)
+    nt = (ctypes.c_int32 * max(1, n))(*[int(x) for x in n_tok])
+    grid, tpg, = ctypes.c_int64(0), ctypes.c_int64(0)
+    ng, cpg, sl = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    tb = (ctypes.c_int64 * max(1, n))()
+    st = lib.svx_plan_tc(n, nt, n_kv_heads, rows, cta_budget, ctypes.byref(grid), ctypes.byref(ng), ctypes.byref(cpg),
+                         ctypes.byref(tpg), ctypes.byref(sl), tb)
+    if st != OK:
+        raise SvxError(st, "svx_plan_tc: invalid arguments")
+    return {"grid": grid.value, "n_groups": ng.value, "ctas_per_group": cpg.value, "tiles_per_group": tpg.value,
+            "slots": sl.value, "tile_base": list(tb[:n])}
 
 
 def check_coverage(hist_len: Sequence[int], parts: Sequence[tuple]) -> bool:

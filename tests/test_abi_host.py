@@ -156,3 +156,66 @@ def test_tiering_matches_oracle(svx):
     for bad in (lambda: t.round(9, 15), lambda: t.commit(16), lambda: t.commit(9)):
         with pytest.raises(svx.SvxError):
             bad()
+
+
+def _begin(k, c, T):
+    return (k * T) // c
+
+
+def _cta_of(x, c, T):
+    return ((x + 1) * c - 1) // T
+
+
+def test_tensor_core_work_plan_invariants(svx):
+    """svx_plan_tc on seeded random launches: the grid is one CTA group per (KV head, pass of <= 64
+    rows); a group's tiles are every part's tiles in order; CTA j of a group takes
+    [floor(jT/c), floor((j+1)T/c)); no part spans more than 8 CTAs, and the grid is the largest
+    that keeps it so within the budget."""
+    rng = np.random.default_rng(5)
+    for _ in range(300):
+        n = int(rng.integers(1, 65))
+        n_tok = [int(x) for x in rng.integers(1, int(rng.choice([300, 5000, 200000])), size=n)]
+        hkv = int(rng.choice([1, 2, 4, 8, 16, 40]))
+        rows = int(rng.integers(1, 257))
+        budget = int(rng.choice([1, 8, 32, 100, 152]))
+        pl = svx.plan_tc(n_tok, hkv, rows, budget)
+        rpp = 32 if rows <= 32 else 64
+        groups = hkv * -(-rows // rpp)
+        nt = [-(-t // 128) for t in n_tok]
+        T = sum(nt)
+        assert pl["n_groups"] == groups and pl["grid"] == groups * pl["ctas_per_group"]
+        assert pl["tiles_per_group"] == T and pl["tile_base"] == list(np.cumsum([0] + nt[:-1]))
+        c = pl["ctas_per_group"]
+
+        def spans(cc):
+            return max(_cta_of(b + t - 1, cc, T) - _cta_of(b, cc, T) + 1 for b, t in zip(pl["tile_base"], nt))
+        top = min(max(1, budget // groups), T)
+        assert 1 <= c <= top and pl["slots"] == spans(c) and (c == 1 or pl["slots"] <= 8)
+        assert all(spans(cc) > 8 for cc in range(c + 1, top + 1))  # the largest grid within the slot limit
+        # the CTA ranges tile [0, T) exactly once, and cta_of inverts them
+        ranges = [(_begin(j, c, T), _begin(j + 1, c, T)) for j in range(c)]
+        assert ranges[0][0] == 0 and ranges[-1][1] == T and all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
+        for j, (lo, hi) in enumerate(ranges):
+            if hi > lo:
+                assert _cta_of(lo, c, T) == j and _cta_of(hi - 1, c, T) == j
+
+
+def test_kernel_split_arithmetic_matches_the_plan():
+    """The kernel splits a group's T tiles over c CTAs in 32-bit arithmetic as begin(k) = k*q +
+    floor(k*r/c) with T = q*c + r, and finds the CTA holding tile x from a float estimate corrected in
+    exact steps; both must equal the host's floor(kT/c) and ((x+1)c - 1) // T."""
+    rng = np.random.default_rng(6)
+    for _ in range(2000):
+        c = int(rng.integers(1, 153))
+        T = int(rng.integers(c, 2 ** 31 - 1)) if rng.random() < 0.5 else int(rng.integers(c, 5000))
+        q, r = divmod(T, c)
+        dev_begin = lambda k: k * q + (k * r) // c  # noqa: E731
+        for k in {0, 1, c // 2, c - 1, c}:
+            assert dev_begin(k) == _begin(k, c, T)
+        for x in {0, T - 1, int(rng.integers(0, T)), dev_begin(c // 2), max(0, dev_begin(c // 2) - 1)}:
+            k = min(int(np.float32(x) * (np.float32(c) / np.float32(T))), c - 1)
+            while k + 1 < c and dev_begin(k + 1) <= x:
+                k += 1
+            while k > 0 and dev_begin(k) > x:
+                k -= 1
+            assert k == _cta_of(x, c, T)
