@@ -143,9 +143,18 @@ svx_status svx_candidate_attn(svx_ctx ctx, const void* k_dev, const void* v_dev,
  * [n_req][Hq][n_query] (natural log of the softmax denominator of the scaled scores) to device
  * memory.  A query with no visible key gets O = 0 and LSE = -inf.  timeout_ms = 0 returns
  * after enqueueing; > 0 waits on the host up to that long and returns SVX_ERR_TIMEOUT if the
- * work has not completed (the work stays enqueued).  The context is ready for the next round
+ * work has not completed (the work stays enqueued), or SVX_ERR_CUDA if a kernel's bounded wait gave
+ * up (2 s; its outputs are then invalid, and the device error word is cleared).  The context is ready for the next round
  * either way; its work is stream-ordered after this round's. */
 svx_status svx_round_finish(svx_ctx ctx, void* o_dev, float* lse_dev, int32_t timeout_ms);
+
+/* Test hook of the failure path (the pages have no counterpart).  Enqueues on the compute stream,
+ * between rounds, a one-thread kernel whose bounded wait on a barrier that nothing completes runs
+ * out after wait_ms (1..2000) and raises the device error word, as a chunk kernel's waits do when
+ * their producer never delivers.  The next svx_round_finish with timeout_ms > 0 then returns
+ * SVX_ERR_CUDA ("a kernel gave up waiting"), clears the word, and the context runs further rounds.
+ * SVX_ERR_BAD_STATE inside a round. */
+svx_status svx_debug_expire_wait(svx_ctx ctx, int32_t wait_ms);
 
 /* Message for the last failing call on ctx (never NULL; "" if none).  NULL ctx: last failure of
  * svx_create or svx_verify_static on this thread. */

@@ -124,6 +124,7 @@ __host__ __device__ inline int64_t cta_of_tile(int64_t x, int64_t n, int64_t T) 
 
 cudaError_t launch_chunk_attn(const ChunkParams& p, int head_dim, cudaStream_t stream);
 cudaError_t launch_finish(const FinishParams& p, int head_dim, cudaStream_t stream);
+cudaError_t launch_expire_wait(int* err, uint64_t limit_ns, cudaStream_t stream);
 
 // Tensor-core chunk kernel (d = 128).  Modes: 0 one softmax warpgroup (<= 32 query rows per pass),
 // 2 two warpgroups on 32 rows each (<= 64 rows per pass), both reading every K/V tile once.

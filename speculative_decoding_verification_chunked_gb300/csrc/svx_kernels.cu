@@ -418,6 +418,40 @@ cudaError_t launch_chunk_attn(const ChunkParams& p, int head_dim, cudaStream_t s
   return cudaErrorInvalidValue;
 }
 
+namespace {
+// A bounded wait on an mbarrier phase that nothing completes: it runs out after limit_ns of global
+// time and raises the device error word (bit 2), the way a chunk kernel's waits end when their
+// producer never delivers.  Test hook of the failure path; one thread, no fault.
+__global__ void expire_wait_kernel(int* err, uint64_t limit_ns) {
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(a) : "memory");
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (;;) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(a)
+        : "memory");
+    if (done) return;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > limit_ns) {
+      atomicOr(err, 2);
+      return;
+    }
+  }
+}
+}  // namespace
+
+cudaError_t launch_expire_wait(int* err, uint64_t limit_ns, cudaStream_t stream) {
+  expire_wait_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_finish(const FinishParams& p, int head_dim, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(p.n_req) * p.n_q_heads * p.n_query;
   const int blocks = static_cast<int>((rows * 32 + kFinishThreads - 1) / kFinishThreads);

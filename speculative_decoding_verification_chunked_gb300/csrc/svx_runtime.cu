@@ -727,7 +727,10 @@ svx_status svx_round_finish(svx_ctx c, void* o_dev, float* lse_dev, int32_t time
       if (e == cudaSuccess) {
         int dev_err = 0;
         SVX_CUDA(c, cudaMemcpy(&dev_err, c->d_err, sizeof(int), cudaMemcpyDeviceToHost));
-        if (dev_err) return fail(c, SVX_ERR_CUDA, "a kernel gave up waiting (device error word %d)", dev_err);
+        if (dev_err) {  // the round's outputs are invalid; the word is cleared, so the context runs on
+          SVX_CUDA(c, cudaMemset(c->d_err, 0, sizeof(int)));
+          return fail(c, SVX_ERR_CUDA, "a kernel gave up waiting (device error word %d)", dev_err);
+        }
         break;
       }
       if (e != cudaErrorNotReady) return fail(c, SVX_ERR_CUDA, "round failed: %s", cudaGetErrorString(e));
@@ -825,6 +828,14 @@ svx_status svx_check_coverage(int32_t n_req, const int64_t* hist_len, const int6
   std::vector<std::array<int64_t, 3>> v(static_cast<size_t>(n_parts));
   for (int64_t i = 0; i < n_parts; ++i) v[static_cast<size_t>(i)] = {parts[3 * i], parts[3 * i + 1], parts[3 * i + 2]};
   *ok_out = coverage_impl(n_req, hist_len, v, nullptr) ? 1 : 0;
+  return SVX_OK;
+}
+
+svx_status svx_debug_expire_wait(svx_ctx c, int32_t wait_ms) {
+  if (!c || wait_ms < 1 || wait_ms > 2000) return SVX_ERR_INVALID_ARG;
+  if (c->state == RoundState::kOpen) return fail(c, SVX_ERR_BAD_STATE, "svx_debug_expire_wait: a round is open");
+  DeviceGuard dg(c->cfg.device);
+  SVX_CUDA(c, svx::launch_expire_wait(c->d_err, static_cast<uint64_t>(wait_ms) * 1000000ull, c->cs));
   return SVX_OK;
 }
 

@@ -90,6 +90,7 @@ _SIGS = {
     "svx_check_coverage": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_int64),
                                           ctypes.POINTER(ctypes.c_int64), ctypes.c_int64,
                                           ctypes.POINTER(ctypes.c_int32)]),
+    "svx_debug_expire_wait": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     "svx_plan_tc": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
                                    ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32),
                                    ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64),
@@ -491,6 +492,10 @@ class Verifier:
     def round_finish(self, o, lse, timeout_ms: int = 0):
         """o: device bf16 [B][Hq][nq][d]; lse: device fp32 [B][Hq][nq]."""
         self._check(lib.svx_round_finish(self._h, _ptr(o), _ptr(lse), timeout_ms))
+
+    def debug_expire_wait(self, wait_ms: int):
+        """Test hook: a kernel whose bounded wait runs out raises the device error word."""
+        self._check(lib.svx_debug_expire_wait(self._h, wait_ms))
 
     def stats(self) -> dict:
         s = Stats()

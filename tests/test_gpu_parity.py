@@ -345,3 +345,23 @@ def test_tiering_migration_feeds_the_next_round(svx):
         C0, L0 = tr.C, tr.L
         rel = tr.commit(C0 + 2)
         assert rel == (C0 + 2, L0) and rel[0] >= tr.H and tr.C == tr.L == C0 + 2
+
+
+def test_a_wait_that_runs_out_is_reported_and_the_context_runs_on(svx):
+    """Failure path without a fault: a kernel whose bounded wait on a barrier that nothing completes
+    runs out (0.2 s) raises the device error word; the next round's finish reports it, clears it, and
+    the round after that is correct again.  Inside an open round the hook is refused."""
+    w = SMALL[2]
+    x, t = gpu_inputs(w)
+    ref = oracle_out(w, x)
+    with make_verifier(svx, w) as v:
+        check_parity(*run_gpu(v, w, t, x, timeout_ms=60000), *ref)
+        v.debug_expire_wait(200)
+        with pytest.raises(svx.SvxError) as ei:
+            run_gpu(v, w, t, x, timeout_ms=60000)
+        assert ei.value.status == svx.ERR_CUDA and "gave up waiting" in ei.value.message
+        check_parity(*run_gpu(v, w, t, x, timeout_ms=60000), *ref)
+        v.round_begin(t["q"], w.hist_len)
+        with pytest.raises(svx.SvxError) as ei:
+            v.debug_expire_wait(200)
+        assert ei.value.status == svx.ERR_BAD_STATE
