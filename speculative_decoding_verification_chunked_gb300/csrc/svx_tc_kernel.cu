@@ -26,9 +26,13 @@
 // Work split: one CTA group per (KV head, row block); a group's tiles (that head
 // and row block of every part, part after part) are split evenly over its CTAs
 // ("stream-K" inside the group), so CTA j of every group covers the same tokens
-// and the heads of a request are read in step.  A CTA that covers part of a
+// and the heads of a request are read in step.  A CTA that covers a piece of a
 // part writes that segment's state into its own state slot, and the finish
 // kernel merges the slots.
+//
+// Launched with programmatic dependent launch: the kernel waits for the work
+// before it in the stream only when it first touches global memory, and lets
+// the next kernel be scheduled once its work is done.
 //
 // Every mbarrier wait is bounded (2 s of global time); a wait that gives up
 // raises the device error word and makes every role of the CTA stop, drain its
