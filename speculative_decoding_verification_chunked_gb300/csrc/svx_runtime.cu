@@ -180,7 +180,7 @@ bool coverage_impl(int32_t n_req, const int64_t* hist_len, const std::vector<std
   std::vector<std::vector<std::pair<int64_t, int64_t>>> per(static_cast<size_t>(std::max(n_req, 0)));
   for (const auto& p : parts) {
     const int64_t b = p[0], t0 = p[1], n = p[2];
-    if (b < 0 || b >= n_req || n <= 0 || t0 < 0 || t0 + n > hist_len[b]) {
+    if (b < 0 || b >= n_req || n <= 0 || t0 < 0 || t0 > hist_len[b] || n > hist_len[b] - t0) {
       if (why) *why = "part (req " + std::to_string(b) + ", start " + std::to_string(t0) + ", n " +
                       std::to_string(n) + ") lies outside the request's history";
       return false;
@@ -502,10 +502,10 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
     if (seen[static_cast<size_t>(p.req)])
       return fail(c, SVX_ERR_INVALID_ARG, "part %d: request %d appears twice in one chunk", i, p.req);
     seen[static_cast<size_t>(p.req)] = 1;
-    if (p.n_tok < 1 || p.tok_start < 0 || p.tok_start + p.n_tok > c->hist_len[static_cast<size_t>(p.req)])
-      return fail(c, SVX_ERR_INVALID_ARG, "part %d: tokens [%lld, %lld) outside history [0, %lld) of request %d", i,
-                  static_cast<long long>(p.tok_start), static_cast<long long>(p.tok_start + p.n_tok),
-                  static_cast<long long>(c->hist_len[static_cast<size_t>(p.req)]), p.req);
+    const int64_t C = c->hist_len[static_cast<size_t>(p.req)];
+    if (p.n_tok < 1 || p.tok_start < 0 || p.tok_start > C || p.n_tok > C - p.tok_start)
+      return fail(c, SVX_ERR_INVALID_ARG, "part %d: %d tokens from %lld outside history [0, %lld) of request %d", i,
+                  p.n_tok, static_cast<long long>(p.tok_start), static_cast<long long>(C), p.req);
     if (!p.k || !p.v || !aligned16(p.k) || !aligned16(p.v))
       return fail(c, SVX_ERR_INVALID_ARG, "part %d: k and v must be non-NULL and 16-byte aligned", i);
     const int kk = pointer_kind(p.k), kv = pointer_kind(p.v);

@@ -104,6 +104,15 @@ def test_coverage_matches_oracle(svx):
         assert svx.check_coverage(hist, parts) == O.covers_exactly_once(hist, parts), (hist, parts)
 
 
+def test_coverage_rejects_parts_whose_end_does_not_fit_64_bits(svx):
+    """A part's end (start + length) past the int64 range lies outside every history."""
+    big = (1 << 63) - 1
+    for parts in ([(0, big, 1)], [(0, big - 5, 10)], [(0, 0, 10), (0, 10, big)], [(0, 10, big), (0, 0, 10)]):
+        assert not svx.check_coverage([10], parts), parts
+        assert not O.covers_exactly_once([10], parts), parts
+    assert svx.check_coverage([big], [(0, 0, big)])
+
+
 def test_create_rejects_bad_config_without_touching_a_device(svx):
     bad = [dict(head_dim=96), dict(max_query=33), dict(n_q_heads=12, n_kv_heads=8), dict(n_slots=4),
            dict(max_req=0), dict(max_chunk_tokens=0)]
