@@ -75,6 +75,10 @@ SPLIT_EDGES = [
     W.Workload("long1", 1, 32, 8, 128, (60000,), 8192, 5, seed=27),
     # 70 requests: a push of more than 64 parts is split into several launches
     W.Workload("req70", 70, 8, 2, 128, tuple(17 + 13 * i for i in range(70)), 256, 3, seed=29),
+    # the API's limits: 256 requests (a full staging slot, four launches per chunk), 32-node trees of any
+    # depth (a full parent block in the finish launch), empty and ragged histories, 64 rows per KV head
+    W.Workload("max256", 256, 4, 2, 128, tuple((37 * i) % 301 for i in range(256)), 64, 32, tree=True,
+               tree_max_depth=31, seed=33),
 ]
 
 
@@ -177,6 +181,31 @@ def test_user_streams_and_timing_stats(svx):
     n_chunks = max(-(-C // w.chunk_tokens) for C in w.hist_len)
     assert 2 * n_chunks <= st["n_copies"] <= 2 * n_parts  # equally strided parts of a chunk share 2D copies
     assert st["round_ms"] > 0 and st["chunk_kernel_ms"] > 0 and st["copy_busy_ms"] > 0
+
+
+@pytest.mark.parametrize("tc", [True, False], ids=["tc", "fma"])
+def test_part_past_32_bit_element_offsets(svx, tc):
+    """One resident part of 2,131,480 tokens (8 KV heads, d = 128: element offsets up to 2.18e9, past
+    2^31).  Its history is a 4099-token block repeated 520 times and no candidate region is attended,
+    so every key's weight is the block key's, counted 520 times: O equals the block's O and LSE the
+    block's LSE + ln 520 (Eq. 9's normaliser).  The oracle computes the block alone."""
+    import torch
+    n, m = 4099, 520
+    w = W.Workload("block", 1, 32, 8, 128, (n,), n, 5, seed=34)
+    x, t = gpu_inputs(w, resident=True)
+    kb = t["kh"][0].repeat(m, 1, 1)
+    vb = t["vh"][0].repeat(m, 1, 1)
+    assert kb.shape[0] * w.n_kv_heads * w.head_dim > 2 ** 31
+    o = torch.empty((1, 32, 5, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, 32, 5), dtype=torch.float32, device="cuda")
+    with svx.Verifier(1, 32, 8, 128, 5, 64, n_slots=2, tensor_cores=tc) as v:
+        v.run_round(t["q"], (n * m,), [kb], [vb], n * m, o, lse, timeout_ms=60000)
+        torch.cuda.synchronize()
+    og, lg = o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+    del kb, vb, t
+    torch.cuda.empty_cache()
+    o_ref, l_ref = oracle_out(w, x, with_candidates=False)
+    check_parity(og, lg, o_ref, l_ref + np.log(m))
 
 
 # ---------------------------------------------------------------- errors
