@@ -71,7 +71,7 @@ def bf16_half_ulp(x):
 
 
 def check_parity(o_gpu, l_gpu, o_ref, l_ref, rows=None):
-    """The bar (BASELINE tolerances, read for a bf16 output and an LSE that may sit near zero):
+    """The bar (the stated tolerances, read for a bf16 output and an LSE that may sit near zero):
     - O: the error beyond the output format's own rounding, max(0, |O - O_ref| - half a bf16 ulp at
       |O_ref|), has max <= 1e-2 and mean <= 1e-3.  No bf16 output can meet an absolute 1e-2 on
       |O| >= 4 (the rounding alone can be 0.0156), and rows with few visible keys reach it;
