@@ -573,7 +573,7 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
     }
     __nv_bfloat16* const slot_base = c->slot_buf[static_cast<size_t>(slot)];
     // A 2D copy reads only its rows, each a whole part inside its own pinned allocation.  When the rows
-    // belong to different allocations the driver refuses the call (invalid value, nothing enqueued);
+    // belong to different allocations cudaMemcpy2DAsync refuses the call (invalid value, nothing enqueued);
     // those parts are then copied one by one.
     auto copy_2d = [&](__nv_bfloat16* dst, const void* src, ptrdiff_t spitch, bool& ok) -> svx_status {
       if (!ok) return SVX_OK;
