@@ -49,6 +49,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["svx", "reference"], default="svx")
     ap.add_argument("--workload", default="qwen3", choices=["tiny", "qwen3", "internlm", "tree", "fulldepth"])
+    ap.add_argument("--head-dim", type=int, choices=[64, 128], default=None,
+                    help="the workload with another head dimension (same tokens, heads and queries)")
     ap.add_argument("--zero-copy-ctas", default="0,8,32",
                     help="comma list of CTA caps for the zero-copy streamed variant (0 = all SMs; empty = skip)")
     ap.add_argument("--no-draft-load", dest="draft_load", action="store_false",
@@ -206,7 +208,7 @@ def run_reference(a, rank, world):
     if rank != 0:
         return 0
     import multiprocessing as mp
-    w = W.named(a.workload)
+    w = workload_of(a)
     cores = os.cpu_count() or 1
     n_pairs = a.cpu_sample_pairs or min(cores, w.n_req * w.n_kv_heads)
     pairs, total = cpu_sample_pairs(w, n_pairs)
@@ -236,14 +238,23 @@ def run_reference(a, rank, world):
     return 0
 
 
+def workload_of(a) -> W.Workload:
+    w = W.named(a.workload)
+    return w.with_(head_dim=a.head_dim) if a.head_dim else w
+
+
 def workload_config(w: W.Workload, a) -> dict:
+    l2_bytes = 129e6
+    per_round = 4 * w.n_kv_heads * w.head_dim * sum(w.hist_len)
     return {"workload": f"{w.name}: {w.n_req} requests, {w.n_q_heads}/{w.n_kv_heads} heads, d={w.head_dim}, "
                         f"history {min(w.hist_len)}..{max(w.hist_len)} tokens, chunk {w.chunk_tokens}, "
                         f"{w.n_query} verify queries ({'token tree' if w.tree else 'causal chain'})",
             "n_req": w.n_req, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
             "hist_tokens": int(sum(w.hist_len)), "chunk_tokens": w.chunk_tokens, "n_query": w.n_query,
             "slots": a.slots, "resident_chunk": a.resident_chunk,
-            "l2": "no flush: 1 round reads >= 1 GiB of history, larger than the 129 MB L2",
+            "l2": (f"no flush: one round reads {per_round / 2**20:.0f} MiB of history, more than the 129 MB L2"
+                   if per_round > l2_bytes else
+                   f"no flush: one round reads {per_round / 2**10:.0f} KiB of history, which stays in the 129 MB L2"),
             "seed": w.seed}
 
 
@@ -313,7 +324,7 @@ def main(argv=None):
         return run_reference(a, rank, world)
 
     import multiprocessing as mp
-    w = W.named(a.workload)
+    w = workload_of(a)
     w = w.with_(seed=w.seed + 1000 * rank)
     L = w.n_layers
     do_cpu = rank == 0 and world == 1 and not a.no_cpu_baseline
@@ -649,7 +660,7 @@ def main(argv=None):
         "gpu_launches": launches_per_step * steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": profiled_traffic(d, w.name),
-                     "kernel": "chunk_attn_tc" if d == 128 else "chunk_attn_fma",
+                     "kernel": "chunk_attn_tc",
                      "peak_source": f"{hbm_src} hbm_gbs (burst copy)",
                      "algorithmic_bytes_per_launch": int(k1_bytes_per_launch),
                      "ms_per_launch": k1_ms_per_launch},
@@ -693,20 +704,17 @@ def code_digest(path: str) -> str:
 
 
 def profiled_traffic(d: int, workload: str):
-    """DRAM bytes per launch of the chunk kernel on this workload from the committed ncu
-    summary, if that summary was taken on the kernel source as it is now (else None)."""
-    import hashlib
-    name = "chunk_attn_tc" if d == 128 else "chunk_attn_fma"
-    src = os.path.join(ROOT, "speculative_decoding_verification_chunked_gb300", "csrc",
-                       "svx_tc_kernel.cu" if d == 128 else "svx_kernels.cu")
-    summ = os.path.join(ROOT, "profiles", f"{name}_traffic.txt")
+    """DRAM bytes per launch of the tensor-core chunk kernel on this workload (head dimension d) from
+    the committed ncu summary, if that summary was taken on the kernel source as it is now (else None)."""
+    src = os.path.join(ROOT, "speculative_decoding_verification_chunked_gb300", "csrc", "svx_tc_kernel.cu")
+    summ = os.path.join(ROOT, "profiles", "chunk_attn_tc_traffic.txt")
     try:
         kv = {k.strip(): v.strip() for k, v in
               (line.split(":", 1) for line in open(summ) if ":" in line and not line.startswith("#"))}
         digest = code_digest(src)
         if kv.get("kernel_code_sha256", "") != digest:
             return None
-        return float(kv[f"{workload}.dram_bytes_per_launch"])
+        return float(kv[f"{workload}.dram_bytes_per_launch" if d == 128 else f"{workload}_d{d}.dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         return None
 

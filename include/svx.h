@@ -66,7 +66,7 @@ typedef struct svx_ctx_s* svx_ctx;
 
 /* svx_config.flags */
 #define SVX_FLAG_TIMING 1u           /* record CUDA events around copies and kernels (svx_round_stats) */
-#define SVX_FLAG_NO_TENSOR_CORES 2u  /* run the history chunk kernel on FP32 FMA even where d = 128 */
+#define SVX_FLAG_NO_TENSOR_CORES 2u  /* run the history chunk kernel on FP32 FMA instead of tcgen05 */
 #define SVX_FLAG_ZERO_COPY 4u        /* read pinned host parts in place over the host link (no staging copy);
                                         the chunk kernel then runs at link speed on zero_copy_ctas SMs */
 

@@ -126,7 +126,7 @@ cudaError_t launch_chunk_attn(const ChunkParams& p, int head_dim, cudaStream_t s
 cudaError_t launch_finish(const FinishParams& p, int head_dim, cudaStream_t stream);
 cudaError_t launch_expire_wait(int* err, uint64_t limit_ns, cudaStream_t stream);
 
-// Tensor-core chunk kernel (d = 128).  Modes: 0 one softmax warpgroup (<= 32 query rows per pass),
+// Tensor-core chunk kernel (d = 64 or 128).  Modes: 0 one softmax warpgroup (<= 32 query rows per pass),
 // 2 two warpgroups on 32 rows each (<= 64 rows per pass), both reading every K/V tile once.
 bool tc_supported(int head_dim, int rows);
 int tc_mode(int rows);
@@ -138,6 +138,6 @@ int tc_max_ctas(int num_sms);
 // spreading over more than kHistSlots state slots in its group.  Returns the grid size (CTA groups
 // x CTAs per group) and the number of state slots used in *slots.
 int64_t tc_plan(ChunkParams& p, int mode, int64_t cta_budget, int64_t* slots);
-cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int mode, int n_ctas, cudaStream_t stream);
+cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int head_dim, int mode, int n_ctas, cudaStream_t stream);
 
 }  // namespace svx

@@ -6,7 +6,8 @@
 //                             every token of the chunk (the chunk is shared by
 //                             the whole query group, section 4.2), chunk-local
 //                             state (Eq. 7) merged into the running state (Eq. 8).
-//                             (FP32-FMA form; d = 128 runs on the tensor cores.)
+//                             (FP32-FMA form, run only with SVX_FLAG_NO_TENSOR_CORES;
+//                             by default the tensor-core kernel takes every chunk.)
 //   finish_kernel<D>          the candidate region under its causal / token-tree
 //                             mask (section 4.2, last paragraph), then the merge
 //                             of all states (Eq. 8), O = a / l (Eq. 9) in bf16

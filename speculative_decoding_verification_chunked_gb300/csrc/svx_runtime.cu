@@ -72,7 +72,7 @@ struct svx_ctx_s {
   int64_t slot_stride = 0;
   uint32_t epoch = 0;
   int* d_err = nullptr;   // device error word: a kernel's bounded wait gave up
-  bool use_tc = false;    // chunk kernel on the tensor cores (d = 128)
+  bool use_tc = false;    // chunk kernel on the tensor cores
 
   // candidate region of the open round: computed by the finish kernel, whose launch parameters
   // carry the tree parents, so no copy is queued behind the chunk transfers
@@ -464,7 +464,7 @@ svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, int cta_cap) {
         uint32_t& used = c->slot_mask[static_cast<size_t>(p.parts[i].req)];
         used |= (slots >= 32 ? 0xffffffffu : ((1u << slots) - 1u));
       }
-      SVX_CUDA(c, svx::launch_chunk_attn_tc(p, mode, static_cast<int>(ctas), c->cs));
+      SVX_CUDA(c, svx::launch_chunk_attn_tc(p, c->cfg.head_dim, mode, static_cast<int>(ctas), c->cs));
     } else {
       p.n_rowblk = (R + svx::kRowsPerBlock - 1) / svx::kRowsPerBlock;
       int64_t max_tok = 0;

@@ -176,12 +176,12 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
                                  static_cast<int32_t>(hist_len_host[b])};
     }
     cudaError_t e;
-    if (head_dim == 128) {
+    if (svx::tc_supported(head_dim, R)) {
       const int mode = svx::tc_mode(R);
       int64_t slots = 0;
       const int64_t ctas = svx::tc_plan(p, mode, svx::tc_max_ctas(num_sms), &slots);
       for (int i = 0; i < n; ++i) slot_mask[p.parts[i].req] |= (1u << slots) - 1u;
-      e = svx::launch_chunk_attn_tc(p, mode, static_cast<int>(ctas), s);
+      e = svx::launch_chunk_attn_tc(p, head_dim, mode, static_cast<int>(ctas), s);
     } else {
       p.n_rowblk = (R + svx::kRowsPerBlock - 1) / svx::kRowsPerBlock;
       int64_t max_tok = 0;

@@ -1,4 +1,4 @@
-// Chunk attention on the 5th-generation tensor cores (tcgen05, TMEM), d = 128.
+// Chunk attention on the 5th-generation tensor cores (tcgen05, TMEM), d = 64 or 128.
 //
 // One history chunk of "Resource-Efficient Speculative Decoding for
 // Long-Context LLM Serving", section 4.2, is shared by every verification query
@@ -11,9 +11,12 @@
 // (20-64 rows) does not waste a 128-row MMA:
 //   S^T  = K_tile . Q^T      M = 128 tokens, N = rows, K = d           (TMEM)
 //   P^T  = 2^(S^T*scale - m) per row, written bf16 to shared memory
-//   O^T  = V_tile^T . P^T    M = d = 128,    N = rows, K = 128 tokens  (TMEM)
+//   O^T  = V_tile^T . P^T    M = 128 dims,   N = rows, K = 128 tokens  (TMEM)
 // and the fp32 output accumulator lives in registers (thread = one of the 128
 // output dimensions), updated one tile behind the MMAs: acc = acc*alpha + O^T.
+// Tiles always span 128 dimensions.  With d = 64 only their lower 64 are loaded:
+// S takes d/16 MMAs over them, and the upper half of every V slot is zeroed once,
+// so O^T rows 64..127 are zero and no thread keeps them.
 //
 // Warp roles (one CTA per SM; NWG = 1 or 2 softmax warpgroups of 32 rows each):
 //   warps 0 .. 4NWG-1  softmax and accumulation: a thread holds 4 tokens x 8 rows
@@ -47,8 +50,8 @@ namespace svx {
 namespace {
 
 constexpr int TOK = kTcTile;  // tokens per tile
-constexpr int D = 128;
-constexpr int TILE_BYTES = TOK * D * 2;  // one K or V tile, 32 KiB
+constexpr int TILE_D = 128;                   // dimensions of a shared-memory tile (two swizzle atoms)
+constexpr int TILE_BYTES = TOK * TILE_D * 2;  // one K or V tile, 32 KiB
 constexpr int HALF_BYTES = TOK * 64 * 2; // 64 of the 128 dimensions of a tile, 16 KiB
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // The running maximum of a query row (log2 units) is re-based only when a score
@@ -74,7 +77,7 @@ struct TcCfg {
   // K slot (~29 MB) only lengthened DRAM queues and cost 7% (qwen3 shape, one GB300).
   static constexpr int KST = 2;  // K slots
   static constexpr int VST = 3;  // V slots
-  static constexpr int Q_BYTES = ROWS * D * 2;
+  static constexpr int Q_BYTES = ROWS * TILE_D * 2;
   static constexpr int P_BYTES = ROWS * TOK * 2;  // P^T of a tile (all rows of the pass), two buffers
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KST * TILE_BYTES;
@@ -137,6 +140,9 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void st_shared_zero16(uint32_t dst) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
 }
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
@@ -361,9 +367,10 @@ struct Waiter {
 };
 
 // NK: 8-column blocks of S computed per warpgroup (query rows 0 .. 8*NK-1 of its 32); every pass has
-// at most 8*NK valid rows per warpgroup.
-template <int MODE, int NK>
+// at most 8*NK valid rows per warpgroup.  DH: the head dimension, 64 or 128.
+template <int MODE, int NK, int DH>
 __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const __grid_constant__ ChunkParams P) {
+  static_assert(DH == 64 || DH == TILE_D, "head dimension");
   using C = TcCfg<MODE>;
   constexpr int NCOL = C::NCOL;
   constexpr int NWG = C::NWG;
@@ -409,6 +416,13 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async();
   }
+  if constexpr (DH < TILE_D) {
+    // the upper 64 dimensions of every V slot stay zero for the whole launch (the producers write only
+    // the lower half), so the PV product's rows 64..127 are zero
+    for (uint32_t o = threadIdx.x * 16u; o < static_cast<uint32_t>(C::VST * HALF_BYTES); o += C::THREADS * 16u)
+      st_shared_zero16(base + C::OFF_V + (o / HALF_BYTES) * TILE_BYTES + HALF_BYTES + o % HALF_BYTES);
+    fence_proxy_async();  // generic-proxy stores, later read by the tensor cores
+  }
   if (warp == 0) tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -427,7 +441,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
   const Split split(static_cast<uint32_t>(T), static_cast<uint32_t>(P.ctas_per_group));
   const int64_t x_begin = split.begin(jg);
   const int64_t x_end = split.begin(jg + 1);
-  const int64_t kv_stride = static_cast<int64_t>(P.n_kv_heads) * D;
+  const int64_t kv_stride = static_cast<int64_t>(P.n_kv_heads) * DH;
 
   if (warp == 4 * NWG || warp == 4 * NWG + 1) {
     // ---------------- producers: warp 4*NWG fills the K ring, warp 4*NWG+1 the V ring
@@ -442,7 +456,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       const Seg sg = seg_at(P, split, grp, x, x_end, hint);
       const PartDesc& pd = P.parts[sg.part];
       const int64_t n_tok = pd.n_tok;
-      const __nv_bfloat16* src = (is_v ? pd.v : pd.k) + static_cast<int64_t>(sg.g) * D;
+      const __nv_bfloat16* src = (is_v ? pd.v : pd.k) + static_cast<int64_t>(sg.g) * DH;
       for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
         const int slot = static_cast<int>(i % nst);
         const uint32_t use = static_cast<uint32_t>(i / nst);
@@ -452,26 +466,30 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
         }
         const int64_t tok0 = (sg.tile0 + t) * TOK;
         const uint32_t dst = ring + static_cast<uint32_t>(slot) * TILE_BYTES;
-        // lane copies 16-byte piece c = lane % 16 of rows r0 + 2j (j < 64); rows past n_tok read nothing
-        const int c = lane & 15, r0 = lane >> 4;
+        // a token row of one head is PC 16-byte pieces; lane copies piece c = lane % PC of rows
+        // r0 + RPI*j (j < TOK/RPI); rows past n_tok read nothing
+        constexpr int PC = DH / 8, RPI = 32 / PC;
+        const int c = lane % PC, r0 = lane / PC;
         const int64_t valid_rows = (n_tok - tok0 < TOK) ? (n_tok - tok0) : static_cast<int64_t>(TOK);
         const __nv_bfloat16* ps = src + (tok0 + r0) * kv_stride + c * 8;
-        const int64_t step = 2 * kv_stride;
+        const int64_t step = RPI * kv_stride;
         const uint32_t so0 = static_cast<uint32_t>(c >> 3) * HALF_BYTES + static_cast<uint32_t>(r0) * 128u;
         if (valid_rows == TOK) {
 #pragma unroll 16
-          for (int j = 0; j < 64; ++j) {
-            const int row = r0 + 2 * j;
-            cp_async16(dst + so0 + static_cast<uint32_t>(j) * 256u + (static_cast<uint32_t>((c & 7) ^ (row & 7)) << 4),
+          for (int j = 0; j < TOK / RPI; ++j) {
+            const int row = r0 + RPI * j;
+            cp_async16(dst + so0 + static_cast<uint32_t>(j) * (RPI * 128u) +
+                           (static_cast<uint32_t>((c & 7) ^ (row & 7)) << 4),
                        ps, 16);
             ps += step;
           }
         } else {
 #pragma unroll 8
-          for (int j = 0; j < 64; ++j) {
-            const int row = r0 + 2 * j;
+          for (int j = 0; j < TOK / RPI; ++j) {
+            const int row = r0 + RPI * j;
             const bool in = row < valid_rows;
-            cp_async16(dst + so0 + static_cast<uint32_t>(j) * 256u + (static_cast<uint32_t>((c & 7) ^ (row & 7)) << 4),
+            cp_async16(dst + so0 + static_cast<uint32_t>(j) * (RPI * 128u) +
+                           (static_cast<uint32_t>((c & 7) ^ (row & 7)) << 4),
                        in ? ps : src, in ? 16 : 0);
             ps += step;
           }
@@ -497,7 +515,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
         const uint32_t d = tmem + C::S_COL + static_cast<uint32_t>(j & 1) * ROWS;
         const uint32_t ka = desc_lo(kaddr, 16);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
+        for (int kk = 0; kk < DH / 16; ++kk)
           mma_bf16(d, ka + desc_adv((kk >> 2) * HALF_BYTES + (kk & 3) * 32),
                    qa + desc_adv((kk >> 2) * (ROWS * 128) + (kk & 3) * 32), kDescHi, idesc_s, kk > 0 ? 1u : 0u);
         mma_commit(SFULL + 8u * static_cast<uint32_t>(j & 1));
@@ -632,7 +650,8 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     };
 
     // This warpgroup's 32 Q rows of a pass into shared memory (K-major swizzled [ROWS][128], padding
-    // rows zero) with cp.async; QFULL completes when every softmax thread's copies have landed.
+    // rows zero; with d = 64 the upper half is never read) with cp.async; QFULL completes when every
+    // softmax thread's copies have landed.
     int hint_q = 0;
     auto load_q = [&](int64_t xq) {
       const Seg sq = seg_at(P, split, grp, xq, x_end, hint_q);
@@ -641,10 +660,10 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       const int64_t qrow0 = (static_cast<int64_t>(P.parts[sq.part].req) * P.n_q_heads +
                              static_cast<int64_t>(sq.g) * P.group) * P.n_query + rblk;
 #pragma unroll
-      for (int idx = tid; idx < NCOL * 16; idx += 128) {
-        const int c = wg * NCOL + (idx >> 4), ch = idx & 15;
+      for (int idx = tid; idx < NCOL * (DH / 8); idx += 128) {
+        const int c = wg * NCOL + idx / (DH / 8), ch = idx % (DH / 8);
         const bool in = c < nrows;
-        cp_async16(base + C::OFF_Q + swz_offset(c, ch, C::ROWS * 128), in ? P.q + (qrow0 + c) * D + ch * 8 : P.q,
+        cp_async16(base + C::OFF_Q + swz_offset(c, ch, C::ROWS * 128), in ? P.q + (qrow0 + c) * DH + ch * 8 : P.q,
                    in ? 16 : 0);
       }
       cp_async_arrive_noinc(QFULL);
@@ -823,14 +842,15 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
         }
         bar_sync(bar_wg, 128);
         // per 8-row block: the earlier accumulators first (independent loads), then the merged values
-        float* ap = P.ws_a + srow0 * D + tid;
+        // (threads past the head dimension hold the zero rows of O^T)
+        float* ap = P.ws_a + srow0 * DH + tid;
 #pragma unroll
-        for (int k = 0; k < NK; ++k) {
+        for (int k = 0; k < NK && tid < DH; ++k) {
           float olda[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int c = 8 * k + e;
-            olda[e] = (c < nr && hdr_w[c].epoch == P.epoch) ? ap[c * D] : 0.f;
+            olda[e] = (c < nr && hdr_w[c].epoch == P.epoch) ? ap[c * DH] : 0.f;
           }
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -842,7 +862,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
                 const float mn = fmaxf(mo, m);
                 if (mn != -INFINITY) a = olda[e] * exp2_approx(mo - mn) + a * exp2_approx(m - mn);
               }
-              ap[c * D] = a;
+              ap[c * DH] = a;
             }
           }
         }
@@ -876,22 +896,38 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
   }
 }
 
-template <int MODE, int NK>
+template <int MODE, int NK, int DH>
 cudaError_t launch_tc(const ChunkParams& p, int n_ctas, cudaStream_t stream) {
   using C = TcCfg<MODE>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e =
-        cudaFuncSetAttribute(chunk_attn_tc<MODE, NK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaFuncSetAttribute(chunk_attn_tc<MODE, NK, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_pdl(chunk_attn_tc<MODE, NK>, dim3(n_ctas), dim3(C::THREADS), C::SMEM, stream, p);
+  return launch_pdl(chunk_attn_tc<MODE, NK, DH>, dim3(n_ctas), dim3(C::THREADS), C::SMEM, stream, p);
+}
+
+template <int DH>
+cudaError_t launch_tc_dh(const ChunkParams& p, int mode, int n_ctas, cudaStream_t stream) {
+  const int R = p.group * p.n_query;
+  if (mode == kSingle) {  // one pass of R <= 32 rows: compute ceil(R / 8) column blocks
+    if (R < 1 || R > TcCfg<kSingle>::ROWS) return cudaErrorInvalidValue;
+    switch ((R + 7) / 8) {
+      case 1: return launch_tc<kSingle, 1, DH>(p, n_ctas, stream);
+      case 2: return launch_tc<kSingle, 2, DH>(p, n_ctas, stream);
+      case 3: return launch_tc<kSingle, 3, DH>(p, n_ctas, stream);
+      default: return launch_tc<kSingle, 4, DH>(p, n_ctas, stream);
+    }
+  }
+  if (mode == kRowSplit) return launch_tc<kRowSplit, 4, DH>(p, n_ctas, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-bool tc_supported(int head_dim, int rows) { return head_dim == 128 && rows >= 1; }
+bool tc_supported(int head_dim, int rows) { return (head_dim == 64 || head_dim == 128) && rows >= 1; }
 int tc_mode(int rows) { return rows <= TcCfg<kSingle>::ROWS ? kSingle : kRowSplit; }
 int tc_rows_per_pass(int mode) { return mode == kRowSplit ? TcCfg<kRowSplit>::ROWS : TcCfg<kSingle>::ROWS; }
 int tc_slots_per_segment(int) { return 1; }
@@ -926,20 +962,11 @@ int64_t tc_plan(ChunkParams& p, int mode, int64_t cta_budget, int64_t* slots) {
   return groups * cpg;
 }
 
-cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int mode, int n_ctas, cudaStream_t stream) {
+cudaError_t launch_chunk_attn_tc(const ChunkParams& p, int head_dim, int mode, int n_ctas, cudaStream_t stream) {
   if (n_ctas < 1) return cudaSuccess;
-  const int R = p.group * p.n_query;
   if (p.total_tiles > INT32_MAX) return cudaErrorInvalidValue;  // the kernel splits tiles in 32-bit arithmetic
-  if (mode == kSingle) {  // one pass of R <= 32 rows: compute ceil(R / 8) column blocks
-    if (R < 1 || R > TcCfg<kSingle>::ROWS) return cudaErrorInvalidValue;
-    switch ((R + 7) / 8) {
-      case 1: return launch_tc<kSingle, 1>(p, n_ctas, stream);
-      case 2: return launch_tc<kSingle, 2>(p, n_ctas, stream);
-      case 3: return launch_tc<kSingle, 3>(p, n_ctas, stream);
-      default: return launch_tc<kSingle, 4>(p, n_ctas, stream);
-    }
-  }
-  if (mode == kRowSplit) return launch_tc<kRowSplit, 4>(p, n_ctas, stream);
+  if (head_dim == 128) return launch_tc_dh<128>(p, mode, n_ctas, stream);
+  if (head_dim == 64) return launch_tc_dh<64>(p, mode, n_ctas, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -273,6 +273,21 @@ def test_full_size_sampled(svx, name):
     check_parity(o, l, *ref, rows=rows)
 
 
+@pytest.mark.parametrize("name", ["qwen3", "tree"])
+def test_head_dim_64_at_full_size_sampled(svx, name):
+    """The qwen3 and tree shapes with d = 64 (the tiny workload's head dimension) at full size, history
+    resident in HBM and pushed as one part per request, as the benchmark's resident round does."""
+    w0 = W.named(name)
+    w = w0.with_(name=name + "_d64", head_dim=64, chunk_tokens=max(w0.hist_len))
+    x, t = gpu_inputs(w, resident=True)
+    with make_verifier(svx, w, n_slots=3, chunk=w0.chunk_tokens) as v:
+        o, l = run_gpu(v, w, t, x)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
+    rows = sample_rows(w, 24)
+    ref = oracle_out(w, x, rows=rows)
+    check_parity(o, l, *ref, rows=rows)
+
+
 def test_full_depth_rounds_back_to_back_with_prefetch(svx):
     """36 layer rounds enqueued without any host wait (finish with timeout 0), so each layer's
     chunk copies queue behind the previous layer's: cross-layer prefetch through the slot events.
