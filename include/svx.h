@@ -86,7 +86,7 @@ typedef struct {
   void* copy_stream;        /* cudaStream_t for H2D chunk copies; NULL: library creates one */
   uint32_t flags;           /* SVX_FLAG_* */
   int32_t zero_copy_ctas;   /* with SVX_FLAG_ZERO_COPY: CTA budget (one CTA per SM) of a launch that
-                               reads host parts; 0 = all SMs.  A head-dim-128 launch uses
+                               reads host parts; 0 = all SMs.  A tensor-core launch uses
                                max(1, budget / groups) CTAs for each of its groups (one per KV head
                                and pass of up to 64 query rows).  Fewer leave SMs free for
                                co-running work; on GB300, 8 CTAs already fill the host link. */

@@ -1,0 +1,32 @@
+"""Host-side logic of the benchmark: workload selection and the L2 statement of its JSON line."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import workloads as W  # noqa: E402
+
+
+def test_head_dim_option_changes_only_the_head_dimension():
+    base = W.named("qwen3")
+    a = bench.parse_args(["--workload", "qwen3", "--head-dim", "64"])
+    w = bench.workload_of(a)
+    assert w.head_dim == 64
+    assert w == base.with_(head_dim=64)
+    assert bench.workload_of(bench.parse_args([])) == base
+    cfg = bench.workload_config(w, a)
+    assert "d=64" in cfg["workload"] and cfg["head_dim"] == 64
+
+
+def test_l2_statement_follows_the_bytes_one_round_reads():
+    for name, expect in (("qwen3", "1024 MiB"), ("tree", "2048 MiB"), ("fulldepth", "1024 MiB")):
+        a = bench.parse_args(["--workload", name])
+        l2 = bench.workload_config(bench.workload_of(a), a)["l2"]
+        assert expect in l2 and "more than the 129 MB L2" in l2, (name, l2)
+    a = bench.parse_args(["--workload", "tiny"])
+    l2 = bench.workload_config(bench.workload_of(a), a)["l2"]
+    assert "128 KiB" in l2 and "stays in" in l2
+    a = bench.parse_args(["--workload", "qwen3", "--head-dim", "64"])
+    assert "512 MiB" in bench.workload_config(bench.workload_of(a), a)["l2"]
