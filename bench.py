@@ -411,6 +411,17 @@ def main(argv=None):
         ly["stream_pushes"] = parts_of(ly["kh_h"], ly["vh_h"], False)
     n_res_pushes = len(layers[0]["res_pushes"])
 
+    def checked_round(vx, pushes):
+        """One round of layer 0 whose finish reads the context's device error word.  The word is kept
+        until a finish with a timeout reports it, so a kernel whose bounded wait ran out in any earlier
+        round of the context raises here, and no line is printed over aborted launches."""
+        ly = layers[0]
+        vx.round_begin(ly["q_d"], w.hist_len)
+        vx.candidate_attn(ly["kc_d"], ly["vc_d"], ly["parent"])
+        for p in pushes:
+            vx.push_raw(p)
+        vx.round_finish(ly["o_d"], ly["lse_d"], timeout_ms=60000)
+
     def resident_step(evs=None):
         for li, ly in enumerate(layers):
             v.round_begin(ly["q_d"], w.hist_len)
@@ -583,7 +594,7 @@ def main(argv=None):
                                 "hist_gb_per_s": hist_bytes / (ms_zc / 1e3) / 1e9,
                                 "link_frac": hist_bytes / (ms_zc / 1e3) / 1e9 / link_gbs,
                                 "ctas": cap if cap > 0 else torch.cuda.get_device_properties(dev).multi_processor_count}
-        zc_steps[cap] = (zc_step, vz)
+        zc_steps[cap] = (zc_step, vz, zc_pushes[0])
 
     # ---- Target priority: the streamed round again beside a low-priority Draft GEMM loop
     interference = None
@@ -595,7 +606,7 @@ def main(argv=None):
         interference = {"draft": "bf16 GEMM 4096^3, CUDA-graph replays of 8 on a lowest-priority stream",
                         "draft_tflops_alone": draft_alone, "modes": {}}
         modes = [("copy_engine", e2e_step, ms_e2e)]
-        for cap, (fn, _vz) in zc_steps.items():
+        for cap, (fn, _vz, _p) in zc_steps.items():
             modes.append((f"zero_copy_{cap}", fn, zc_results[str(cap)]["ms_per_step"]))
         for name, fn, ms_alone in modes:
             dl.start()
@@ -604,6 +615,11 @@ def main(argv=None):
             tf = dl.stop()
             interference["modes"][name] = {"delta_T": (ms_co - ms_alone) / ms_alone, "target_ms_alone": ms_alone,
                                            "target_ms_co": ms_co, "draft_tflops_co": tf}
+
+    # every context's kernels ran to completion (no bounded wait gave up) in all the passes above
+    checked_round(v, layers[0]["res_pushes"])
+    for _fn, vz, pushes in zc_steps.values():
+        checked_round(vz, pushes)
 
     # ---- overlap: one timed streamed layer vs the same chunks' kernels in resident mode
     vt = svx.Verifier(B, Hq, Hkv, d, nq, w.chunk_tokens, n_slots=a.slots, device=local, compute_stream=cs,
@@ -623,6 +639,7 @@ def main(argv=None):
             vt.push_raw(p)
         vt.round_finish(ly["o_d"], ly["lse_d"])
         st_r.append(vt.stats())
+    checked_round(vt, ly["res_plan_pushes"])
     vt.close()
     s_round = statistics.median(s["round_ms"] for s in st_s)
     s_copy = statistics.median(s["copy_busy_ms"] for s in st_s)

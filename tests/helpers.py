@@ -42,7 +42,9 @@ def gpu_inputs(w, layer=0, resident=False):
     return x, t
 
 
-def run_gpu(v, w, t, x, chunk_order=None, with_candidates=True, timeout_ms=0):
+def run_gpu(v, w, t, x, chunk_order=None, with_candidates=True, timeout_ms=60000):
+    """One round through the C ABI.  The finish waits with a timeout, so it also reads the device
+    error word: a kernel whose bounded wait ran out fails the test that launched it."""
     import torch
     B, Hq, nq, d = w.n_req, w.n_q_heads, w.n_query, w.head_dim
     o = torch.empty((B, Hq, nq, d), dtype=torch.bfloat16, device="cuda")
