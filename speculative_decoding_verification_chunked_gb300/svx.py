@@ -270,8 +270,9 @@ class Tier:
 
     def migrate(self, T: int, g: int, row_bytes: int, k_dev_at_H, v_dev_at_H, k_host, v_host, stream=None) -> int:
         E = ctypes.c_int64(0)
-        self._call(lib.svx_tier_migrate, T, g, row_bytes, _ptr(k_dev_at_H), _ptr(v_dev_at_H), _ptr(k_host),
-                   _ptr(v_host), _stream_handle(stream), ctypes.byref(E))
+        ptrs = [_dense_ptr(t, what) for t, what in ((k_dev_at_H, "k_dev_at_H"), (v_dev_at_H, "v_dev_at_H"),
+                                                     (k_host, "k_host"), (v_host, "v_host"))]
+        self._call(lib.svx_tier_migrate, T, g, row_bytes, *ptrs, _stream_handle(stream), ctypes.byref(E))
         return E.value
 
     def poll(self) -> bool:
@@ -389,15 +390,22 @@ def verify_static(q, hist_len: Sequence[int], hist_k: Sequence, hist_v: Sequence
         src = next((k for k in hist_k if k is not None), cand_k)
         n_kv_heads = int(src.shape[-2])
     h, hp = _i64(hist_len)
-    ks = (_P * B)(*[None if k is None else _ptr(k) for k in hist_k])
-    vs = (_P * B)(*[None if v is None else _ptr(v) for v in hist_v])
+    qp = _tensor_ptr(q, "bf16", (Hq, nq, d), B, "q")
+    kv = (n_kv_heads, d)
+    ks = (_P * B)(*[None if k is None else _tensor_ptr(k, "bf16", kv, int(C), f"history k of request {b}")
+                    for b, (k, C) in enumerate(zip(hist_k, hist_len))])
+    vs = (_P * B)(*[None if v is None else _tensor_ptr(v, "bf16", kv, int(C), f"history v of request {b}")
+                    for b, (v, C) in enumerate(zip(hist_v, hist_len))])
+    ckp = None if cand_k is None else _tensor_ptr(cand_k, "bf16", (nq,) + kv, B, "candidate k")
+    cvp = None if cand_v is None else _tensor_ptr(cand_v, "bf16", (nq,) + kv, B, "candidate v")
     par = None
     if parent is not None:
         parent = np.ascontiguousarray(np.asarray(parent, dtype=np.int32))
         par = parent.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
-    st = lib.svx_verify_static(B, Hq, n_kv_heads, d, nq, _ptr(q), hp, ks, vs,
-                               None if cand_k is None else _ptr(cand_k), None if cand_v is None else _ptr(cand_v),
-                               par, ctypes.c_float(scale), _ptr(o), _ptr(lse), _stream_handle(stream))
+    op = _tensor_ptr(o, "bf16", (Hq, nq, d), B, "o")
+    lp = _tensor_ptr(lse, "f32", (Hq, nq), B, "lse")
+    st = lib.svx_verify_static(B, Hq, n_kv_heads, d, nq, qp, hp, ks, vs, ckp, cvp, par, ctypes.c_float(scale), op, lp,
+                               _stream_handle(stream))
     if st != OK:
         raise SvxError(st, lib.svx_last_error(None).decode())
 
@@ -409,6 +417,37 @@ def _ptr(t) -> int:
     """Device or host address of a torch tensor (or an int address)."""
     if isinstance(t, int):
         return t
+    return t.data_ptr()
+
+
+_DTYPES = {"bf16": "torch.bfloat16", "f32": "torch.float32"}
+
+
+def _dense_ptr(t, what: str) -> int:
+    """Address of a dense row-major tensor (rows the C call steps over by a byte count)."""
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise SvxError(ERR_INVALID_ARG, f"{what}: not contiguous (the C layout is dense row-major)")
+    return t.data_ptr()
+
+
+def _tensor_ptr(t, dtype: str, tail: tuple, lead: Optional[int], what: str) -> int:
+    """Address of a tensor laid out as the C call expects it: element type, dense row-major, the
+    trailing dimensions `tail` and at least `lead` entries along the first.  The C calls see only an
+    address, so a view with other strides or another type would be read as garbage; such tensors
+    raise SvxError(SVX_ERR_INVALID_ARG) here.  Raw int addresses pass unchecked."""
+    if isinstance(t, int):
+        return t
+    if str(t.dtype) != _DTYPES[dtype]:
+        raise SvxError(ERR_INVALID_ARG, f"{what}: dtype {t.dtype}, expected {_DTYPES[dtype]}")
+    if not t.is_contiguous():
+        raise SvxError(ERR_INVALID_ARG, f"{what}: not contiguous (the C layout is dense row-major)")
+    shape = tuple(int(n) for n in t.shape)
+    if len(shape) != len(tail) + 1 or shape[1:] != tuple(int(n) for n in tail) or \
+            (lead is not None and shape[0] < lead):
+        want = (f">={lead}" if lead is not None else "n",) + tuple(tail)
+        raise SvxError(ERR_INVALID_ARG, f"{what}: shape {list(shape)}, expected [{', '.join(map(str, want))}]")
     return t.data_ptr()
 
 
@@ -462,15 +501,21 @@ class Verifier:
         """q: device bf16 [B][Hq][nq][d]."""
         n_req = len(hist_len)
         nq = n_query if n_query is not None else int(q.shape[2])
+        c = self.cfg
+        qp = _tensor_ptr(q, "bf16", (c.n_q_heads, nq, c.head_dim), n_req, "q")
         h, hp = _i64(hist_len)
-        self._check(lib.svx_round_begin(self._h, n_req, nq, _ptr(q), hp, ctypes.c_float(scale)))
+        self._check(lib.svx_round_begin(self._h, n_req, nq, qp, hp, ctypes.c_float(scale)))
+        self._round = (n_req, nq)
 
     def push_chunk(self, parts: Sequence[tuple]):
         """parts: (req, tok_start, k, v) with k, v bf16 [n_tok][Hkv][d] (pinned host or device)."""
         arr = (Part * max(1, len(parts)))()
+        tail = (self.cfg.n_kv_heads, self.cfg.head_dim)
         for i, (req, t0, k, v) in enumerate(parts):
-            n_tok = int(k.shape[0]) if not isinstance(k, int) else None
-            arr[i] = Part(req, n_tok, t0, _ptr(k), _ptr(v))
+            n_tok = int(k.shape[0])
+            kp = _tensor_ptr(k, "bf16", tail, None, f"part {i} k")
+            vp = _tensor_ptr(v, "bf16", tail, n_tok, f"part {i} v")
+            arr[i] = Part(req, n_tok, t0, kp, vp)
         self._check(lib.svx_push_chunk(self._h, arr, len(parts)))
 
     def push_raw(self, parts: Sequence[tuple]):
@@ -483,15 +528,25 @@ class Verifier:
     def candidate_attn(self, k, v, parent: Optional[np.ndarray] = None, n_cand: Optional[int] = None):
         """k, v: device bf16 [B][n_cand][Hkv][d]; parent: int32 [B][n_cand] or None (chain)."""
         nc = n_cand if n_cand is not None else int(k.shape[1])
+        n_req = getattr(self, "_round", (None, None))[0]
+        tail = (nc, self.cfg.n_kv_heads, self.cfg.head_dim)
+        kp = _tensor_ptr(k, "bf16", tail, n_req, "candidate k")
+        vp = _tensor_ptr(v, "bf16", tail, n_req, "candidate v")
         par = None
         if parent is not None:
             self._parent = np.ascontiguousarray(np.asarray(parent, dtype=np.int32))
             par = self._parent.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
-        self._check(lib.svx_candidate_attn(self._h, _ptr(k), _ptr(v), nc, par))
+        self._check(lib.svx_candidate_attn(self._h, kp, vp, nc, par))
 
     def round_finish(self, o, lse, timeout_ms: int = 0):
         """o: device bf16 [B][Hq][nq][d]; lse: device fp32 [B][Hq][nq]."""
-        self._check(lib.svx_round_finish(self._h, _ptr(o), _ptr(lse), timeout_ms))
+        n_req, nq = getattr(self, "_round", (None, None))
+        if nq is None:  # no round begun: the library reports the state error
+            self._check(lib.svx_round_finish(self._h, _ptr(o), _ptr(lse), timeout_ms))
+            return
+        op = _tensor_ptr(o, "bf16", (self.cfg.n_q_heads, nq, self.cfg.head_dim), n_req, "o")
+        lp = _tensor_ptr(lse, "f32", (self.cfg.n_q_heads, nq), n_req, "lse")
+        self._check(lib.svx_round_finish(self._h, op, lp, timeout_ms))
 
     def debug_expire_wait(self, wait_ms: int):
         """Test hook: a kernel whose bounded wait runs out raises the device error word."""
@@ -517,8 +572,11 @@ class Verifier:
         chunks = {}
         for j, _slot, b, t0, n in plan_chunks(hist_len, chunk_tokens, self.cfg.n_slots):
             chunks.setdefault(j, []).append((b, t0, n))
-        base_k = [None if k is None else _ptr(k) for k in hist_k]
-        base_v = [None if v is None else _ptr(v) for v in hist_v]
+        tail = (self.cfg.n_kv_heads, self.cfg.head_dim)
+        base_k = [None if k is None else _tensor_ptr(k, "bf16", tail, int(C), f"history k of request {b}")
+                  for b, (k, C) in enumerate(zip(hist_k, hist_len))]
+        base_v = [None if v is None else _tensor_ptr(v, "bf16", tail, int(C), f"history v of request {b}")
+                  for b, (v, C) in enumerate(zip(hist_v, hist_len))]
         for j in (chunk_order if chunk_order is not None else sorted(chunks)):
             parts = chunks[j]
             arr = (Part * len(parts))()

@@ -228,3 +228,28 @@ def test_kernel_split_arithmetic_matches_the_plan():
             while k > 0 and dev_begin(k) > x:
                 k -= 1
             assert k == _cta_of(x, c, T)
+
+
+def test_binding_refuses_tensors_not_in_the_c_layout(svx):
+    """The C calls see addresses only, so the binding checks a tensor's type, density and shape
+    against the C layout before passing its address on."""
+    import torch
+    q = torch.zeros((2, 8, 3, 128), dtype=torch.bfloat16)
+    assert svx._tensor_ptr(q, "bf16", (8, 3, 128), 2, "q") == q.data_ptr()
+    assert svx._tensor_ptr(q, "bf16", (8, 3, 128), 1, "q") == q.data_ptr()  # a buffer for more requests
+    assert svx._tensor_ptr(12345, "bf16", (8, 3, 128), 2, "q") == 12345      # raw addresses pass through
+    lse = torch.zeros((2, 8, 3), dtype=torch.float32)
+    assert svx._tensor_ptr(lse, "f32", (8, 3), 2, "lse") == lse.data_ptr()
+    bad = [(q.float(), (8, 3, 128), 2),          # element type
+           (q.transpose(1, 2), (3, 8, 128), 2),  # strides of a view
+           (q[:, :, :2], (8, 2, 128), 2),        # a slice inside a row
+           (q, (8, 3, 64), 2),                   # head dimension
+           (q, (8, 3, 128), 3),                  # fewer requests than the round has
+           (q[0], (8, 3, 128), 2)]               # rank
+    for t, tail, lead in bad:
+        with pytest.raises(svx.SvxError) as e:
+            svx._tensor_ptr(t, "bf16", tail, lead, "q")
+        assert e.value.status == svx.ERR_INVALID_ARG
+    with pytest.raises(svx.SvxError):
+        svx._dense_ptr(q.transpose(0, 1), "k_host")
+    assert svx._dense_ptr(q[1], "k_host") == q[1].data_ptr()

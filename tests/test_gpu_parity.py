@@ -239,7 +239,11 @@ def test_state_machine_and_argument_errors(svx):
         pk = torch.zeros((10, 2, 128), dtype=torch.bfloat16)
         assert status(v.push_chunk, [(0, 0, pk, pk)]) == svx.ERR_INVALID_ARG
         # wrong candidate count, bad tree
-        assert status(v.candidate_attn, t["kc"], t["vc"], None, 2) == svx.ERR_INVALID_ARG
+        assert status(v.candidate_attn, t["kc"][:, :2].contiguous(), t["vc"][:, :2].contiguous(), None, 2) \
+            == svx.ERR_INVALID_ARG
+        # tensors whose layout is not the C layout are refused before the call
+        assert status(v.candidate_attn, t["kc"].transpose(2, 3), t["vc"], None) == svx.ERR_INVALID_ARG
+        assert status(v.push_chunk, [(0, 0, kh[0][:64].float(), vh[0][:64])]) == svx.ERR_INVALID_ARG
         assert status(v.candidate_attn, t["kc"], t["vc"], np.array([[0, 0, 1], [-1, 0, 1]])) == svx.ERR_INVALID_ARG
         # a missing chunk fails the coverage check at finish and closes the round
         v.push_chunk([(0, 0, kh[0][:64], vh[0][:64]), (1, 0, kh[1][:50], vh[1][:50])])
