@@ -31,8 +31,9 @@
  *
  * Errors: every call returns an svx_status; svx_last_error() gives a
  * human-readable message for the last failing call on that context.  No call
- * throws, aborts or exits.  After SVX_ERR_CUDA the context should be
- * destroyed.
+ * throws, aborts or exits.  After SVX_ERR_CUDA from a failed CUDA call the
+ * context should be destroyed; the report of a kernel's expired bounded wait
+ * (svx_round_finish) is the exception, and the context runs on.
  *
  * Threads: a context is used by one host thread at a time.
  *
@@ -143,9 +144,11 @@ svx_status svx_candidate_attn(svx_ctx ctx, const void* k_dev, const void* v_dev,
  * [n_req][Hq][n_query] (natural log of the softmax denominator of the scaled scores) to device
  * memory.  A query with no visible key gets O = 0 and LSE = -inf.  timeout_ms = 0 returns
  * after enqueueing; > 0 waits on the host up to that long and returns SVX_ERR_TIMEOUT if the
- * work has not completed (the work stays enqueued), or SVX_ERR_CUDA if a kernel's bounded wait gave
- * up (2 s; its outputs are then invalid, and the device error word is cleared).  The context is ready for the next round
- * either way; its work is stream-ordered after this round's. */
+ * work has not completed (the work stays enqueued), or SVX_ERR_CUDA if a kernel's bounded wait
+ * gave up (2 s) in this round or in any round since the last finish with timeout_ms > 0: the
+ * context's device error word keeps an expiry until such a finish reads it, reports it and clears
+ * it.  The outputs of the round whose kernel gave up are invalid.  The context is ready for the
+ * next round either way; its work is stream-ordered after this round's. */
 svx_status svx_round_finish(svx_ctx ctx, void* o_dev, float* lse_dev, int32_t timeout_ms);
 
 /* Test hook of the failure path (the pages have no counterpart).  Enqueues on the compute stream,
