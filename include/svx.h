@@ -283,7 +283,9 @@ svx_status svx_tier_round(svx_tier_state* s, int64_t C, int64_t L);
  * in [*begin, *end); otherwise *begin = *end = H.  Host-only (the caller copies). */
 svx_status svx_tier_plan(svx_tier_state* s, int64_t T, int64_t g, int64_t* begin, int64_t* end);
 
-/* The caller's copy of the pending interval has completed: H advances to its endpoint. */
+/* The caller's copy of the pending interval has completed: H advances to its endpoint.
+ * SVX_ERR_BAD_STATE while a copy enqueued by svx_tier_migrate is in flight (svx_tier_poll and
+ * svx_tier_release advance H for those). */
 svx_status svx_tier_complete(svx_tier_state* s);
 
 /* End of round: keep the prefix [0, C_new), C <= C_new <= L, and release [C_new, L) on the GPU (the

@@ -51,6 +51,7 @@ svx_status svx_tier_plan(svx_tier_state* s, int64_t T, int64_t g, int64_t* begin
 
 svx_status svx_tier_complete(svx_tier_state* s) {
   if (!valid(s)) return SVX_ERR_INVALID_ARG;
+  if (s->event) return SVX_ERR_BAD_STATE;  // the library's own copy is in flight: poll or release it
   if (s->pending >= 0) {
     s->H = s->pending;
     s->pending = -1;

@@ -253,3 +253,16 @@ def test_binding_refuses_tensors_not_in_the_c_layout(svx):
     with pytest.raises(svx.SvxError):
         svx._dense_ptr(q.transpose(0, 1), "k_host")
     assert svx._dense_ptr(q[1], "k_host") == q[1].data_ptr()
+
+
+def test_manual_completion_is_refused_while_a_library_copy_is_in_flight(svx):
+    """H may advance past rows only once they are in host memory: while svx_tier_migrate's copy is
+    in flight (its event set), svx_tier_complete refuses, and H stays.  The event here is a stand-in
+    pointer that no CUDA call ever sees: it is cleared before the state is used any further."""
+    import ctypes
+    s = svx.TierState(0, 100, 104, 64, ctypes.c_void_p(1))
+    assert svx.lib.svx_tier_complete(ctypes.byref(s)) == svx.ERR_BAD_STATE
+    assert s.H == 0 and s.pending == 64
+    s.event = None
+    assert svx.lib.svx_tier_complete(ctypes.byref(s)) == svx.OK
+    assert s.H == 64 and s.pending == -1
