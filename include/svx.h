@@ -259,6 +259,13 @@ svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_t n_kv_head
                              const void* k_cand_dev, const void* v_cand_dev, const int32_t* parent_host,
                              float scale, void* o_dev, float* lse_dev, void* stream);
 
+/* Reads and clears the static scratch's device error word on the calling thread's current device:
+ * *expired = 1 if a kernel of some svx_verify_static call since the last check gave up a bounded
+ * wait (2 s; that call's outputs are invalid), else 0.  Waits for all work on the device
+ * (cudaDeviceSynchronize), so call it outside latency-critical loops and outside stream capture.
+ * Allocates nothing.  Errors: SVX_ERR_INVALID_ARG, _CUDA; message from svx_last_error(NULL). */
+svx_status svx_static_check(int32_t* expired);
+
 /* ---- commit-aware KV tiering (host side of the history that the rounds stream) ------------- */
 
 /* One request's Target KV regions (section 4.1, Eq. 4): Sealed History [0, H) in host memory,

@@ -228,3 +228,25 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
   if (e != cudaSuccess) return fail(SVX_ERR_CUDA, "finish kernel launch failed: %s", cudaGetErrorString(e));
   return SVX_OK;
 }
+
+extern "C" svx_status svx_static_check(int32_t* expired) {
+  if (!expired) return fail(SVX_ERR_INVALID_ARG, "expired is NULL");
+  *expired = 0;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return fail(SVX_ERR_CUDA, "no usable current CUDA device");
+  }
+  StaticDevice& sd = g_devices[dev];
+  std::lock_guard<std::mutex> lock(sd.mu);
+  if (!sd.ready) return SVX_OK;  // no static round has run on this device
+  int word = 0;
+  int* d_err = reinterpret_cast<int*>(sd.ptr + kErrOffset);
+  cudaError_t e = cudaDeviceSynchronize();  // every stream's static rounds have finished
+  if (e == cudaSuccess) e = cudaMemcpy(&word, d_err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && word != 0) e = cudaMemset(d_err, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(SVX_ERR_CUDA, "static error word: %s", cudaGetErrorString(e));
+  *expired = word != 0 ? 1 : 0;
+  return SVX_OK;
+}

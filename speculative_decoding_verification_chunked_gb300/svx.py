@@ -99,6 +99,7 @@ _SIGS = {
                                          ctypes.c_int32, _P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(_P),
                                          ctypes.POINTER(_P), _P, _P, ctypes.POINTER(ctypes.c_int32), ctypes.c_float,
                                          _P, _P, _P]),
+    "svx_static_check": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32)]),
     "svx_migration_endpoint": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                               ctypes.POINTER(ctypes.c_int64)]),
     "svx_tier_round": (ctypes.c_int, [ctypes.POINTER(TierState), ctypes.c_int64, ctypes.c_int64]),
@@ -374,6 +375,16 @@ class WidthController:
 
 
 STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def static_check() -> bool:
+    """svx_static_check: True if a kernel of some static round since the last check gave up a
+    bounded wait (that round's outputs are invalid); clears the flag.  Synchronises the device."""
+    e = ctypes.c_int32(0)
+    st = lib.svx_static_check(ctypes.byref(e))
+    if st != OK:
+        raise SvxError(st, lib.svx_last_error(None).decode())
+    return bool(e.value)
 
 
 def verify_static(q, hist_len: Sequence[int], hist_k: Sequence, hist_v: Sequence, o, lse, cand_k=None, cand_v=None,

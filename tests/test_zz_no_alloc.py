@@ -49,6 +49,9 @@ def test_static_round_matches_context_round_twice(svx):
             o_c, l_c = run_gpu(v, w, t, x)
         check_parity(o_s, l_s, o_c, l_c)
         check_parity(o_s, l_s, *oracle_out(w, x))
+    # no kernel of the static rounds gave up a bounded wait; the check clears what it reads
+    assert svx.static_check() is False
+    assert svx.static_check() is False
 
 
 def test_static_round_rejects_rounds_beyond_its_scratch(svx):
