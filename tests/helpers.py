@@ -74,24 +74,28 @@ def bf16_half_ulp(x):
 
 def check_parity(o_gpu, l_gpu, o_ref, l_ref, rows=None):
     """The bar (the stated tolerances, read for a bf16 output and an LSE that may sit near zero):
-    - O: the error beyond the output format's own rounding, max(0, |O - O_ref| - half a bf16 ulp at
-      |O_ref|), has max <= 1e-2 and mean <= 1e-3.  No bf16 output can meet an absolute 1e-2 on
-      |O| >= 4 (the rounding alone can be 0.0156), and rows with few visible keys reach it;
+    - O mean: mean |O - O_ref| <= 1e-3 on the raw error.  Rounding the exact value to bf16 averages
+      about a quarter of a bf16 ulp, far under 1e-3 where |O| < 1, so this bar sees any systematic
+      error above that;
+    - O max: the error beyond the output format's own rounding, max(0, |O - O_ref| - half a bf16 ulp
+      at |O_ref|), is <= 1e-2.  No bf16 output can meet an absolute 1e-2 on |O| >= 4 (the rounding
+      alone can be 0.0156), and rows with few visible keys reach such values;
     - LSE: |LSE - LSE_ref| <= 1e-4 * max(|LSE_ref|, 1), i.e. relative, except that near LSE = 0
       (a handful of keys) it is absolute;
     - LSE finiteness (no visible key: -inf) matches exactly."""
     if rows is not None:
         idx = tuple(np.array(rows).T)
         o_gpu, l_gpu, o_ref, l_ref = o_gpu[idx], l_gpu[idx], o_ref[idx], l_ref[idx]
-    err = np.maximum(np.abs(o_gpu - o_ref) - bf16_half_ulp(o_ref), 0.0)
+    raw = np.abs(o_gpu - o_ref)
+    err = np.maximum(raw - bf16_half_ulp(o_ref), 0.0)
     fin = np.isfinite(l_ref)
     rel = np.abs(l_gpu[fin] - l_ref[fin]) / np.maximum(np.abs(l_ref[fin]), 1.0)
     assert np.array_equal(np.isfinite(l_gpu), fin), "LSE finiteness differs"
     assert err.max() <= O_MAX_ABS, f"O max abs err beyond bf16 rounding {err.max():.3e}"
-    assert err.mean() <= O_MEAN_ABS, f"O mean abs err beyond bf16 rounding {err.mean():.3e}"
+    assert raw.mean() <= O_MEAN_ABS, f"O mean abs err {raw.mean():.3e}"
     if rel.size:
         assert rel.max() <= LSE_REL, f"LSE err {rel.max():.3e} (relative to max(|LSE|, 1))"
-    return float(err.max()), float(err.mean()), float(rel.max()) if rel.size else 0.0
+    return float(err.max()), float(raw.mean()), float(rel.max()) if rel.size else 0.0
 
 
 def sample_rows(w, n, seed=0):

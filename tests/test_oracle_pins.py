@@ -316,8 +316,9 @@ def test_round_bf16_matches_nearest_representable():
 
 
 def test_parity_bar_allows_only_the_bf16_output_rounding_beyond_the_tolerance():
-    """The GPU parity bar: O error beyond half a bf16 ulp of the exact value (max <= 1e-2, mean <=
-    1e-3), LSE error relative to max(|LSE|, 1).  Pinned on hand-made errors at the boundaries."""
+    """The GPU parity bar: O error beyond half a bf16 ulp of the exact value (max <= 1e-2), raw O
+    error (mean <= 1e-3), LSE error relative to max(|LSE|, 1).  Pinned on hand-made errors at the
+    boundaries."""
     import pytest as _pt
     from helpers import bf16_half_ulp, check_parity
     o_ref = np.zeros((1, 200))
@@ -337,6 +338,21 @@ def test_parity_bar_allows_only_the_bf16_output_rounding_beyond_the_tolerance():
         check_parity(bump(1, 0.0115), l_ref, o_ref, l_ref)
     with _pt.raises(AssertionError):  # the mean bar: 0.006 beyond rounding on every element
         check_parity(o_ref + 0.006 + bf16_half_ulp(o_ref), l_ref, o_ref, l_ref)
+    # the mean bar is on the raw error: a systematic 1.1e-3 on every element fails even where half a
+    # bf16 ulp would have covered it, and a 9e-4 one passes
+    o_mid = np.full((1, 200), 0.3)
+    l_mid = np.full(1, 5.0)
+    with _pt.raises(AssertionError):
+        check_parity(o_mid + 1.1e-3, l_mid, o_mid, l_mid)
+    check_parity(o_mid + 9e-4, l_mid, o_mid, l_mid)
+    # exact values rounded to bf16 (what a perfect kernel writes) pass at every magnitude the
+    # configured workloads produce
+    from oracle import round_bf16
+    rng = np.random.default_rng(3)
+    o_exact = rng.standard_normal((64, 128)) * 0.3
+    l_exact = np.full(64, 9.0)
+    _, mean_err, _ = check_parity(round_bf16(o_exact), l_exact, o_exact, l_exact)
+    assert mean_err < 5e-4
     # an LSE near zero is held to 1e-4 absolute, a large one to 1e-4 relative
     check_parity(o_ref, l_ref + [8e-4, 9e-5, 0, 1.9e-4], o_ref, l_ref)
     with _pt.raises(AssertionError):
