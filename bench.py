@@ -1,28 +1,33 @@
 #!/usr/bin/env python
 """Verification-attention benchmark (one JSON line on rank 0).
 
-A step is one verification round of one layer of the Qwen3-8B-shaped workload
-(8 requests, 32 query / 8 KV heads, d = 128, 32768 committed history tokens per
-request, k = 4 -> 5 verification queries, causal candidate chain): chunk plan,
-chunk attention, candidate-region attention and the final merge, all through
-the C ABI.
+A step is one verification round of every layer of the workload, through the C
+ABI: chunk plan, chunk attention, candidate-region attention and the final merge.
+The default workload is the full-depth round: 36 layers of the Qwen3-8B-shaped
+attention stack (32 query / 8 KV heads, d = 128), 2 requests x 131072 committed
+tokens (38.65 GB of bf16 K and V per step), k = 4 (5 verification queries, causal
+candidate chain), chunks of 8192 tokens.
 
   value  verification tokens/s with every input already in HBM (history read in
-         place as device parts): the HBM-bound form of the round.
+         place as device parts): the HBM-bound form of the step.
   e2e    the same metric through the same API with HOST buffers: Q and the
          candidate KV copied from pinned host memory, the committed history
-         streamed chunk by chunk (2048 tokens) from pinned host memory by the
-         library's copy engine, O and LSE copied back, all inside the timed
-         region.  This is the method's own setting (history offloaded to host).
+         streamed chunk by chunk from pinned host memory by the library's copy
+         engine (adaptive: host regions the copy engine reads slowly are read in
+         place by the chunk kernel), O and LSE copied back, all inside the timed
+         region; the next layer's chunk copies queue behind the current layer's
+         (cross-layer prefetch).  Overlap figures come from the same context's
+         timing window over the same timed steps.
 
-The history (1 GiB per round) is larger than L2, so no flush is needed between
-steps.  --impl reference times the float64 CPU oracle instead.
+The other named workloads (tiny, qwen3, internlm, tree) run as shorter
+sub-records under "workloads".  Every step reads more than the 129 MB L2 except
+tiny's (stated in its config), so no flush is needed.  --impl reference times
+the float64 CPU oracle on a bounded sample of each step instead.
 """
 from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -40,26 +45,36 @@ import workloads as W  # noqa: E402
 METRIC = "verify-attn tokens/s; streamed-KV GB/s vs host-link & HBM roofline"
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
+SUB_WORKLOADS = "tiny,qwen3,internlm,tree"
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["svx", "reference"], default="svx")
-    ap.add_argument("--workload", default="qwen3", choices=["tiny", "qwen3", "internlm", "tree", "fulldepth"])
+    ap.add_argument("--workload", default="fulldepth", choices=list(W.NAMES))
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layers per step (default: the workload's; fewer keep every launch's shape, for profiling)")
     ap.add_argument("--head-dim", type=int, choices=[64, 128], default=None,
                     help="the workload with another head dimension (same tokens, heads and queries)")
-    ap.add_argument("--zero-copy-ctas", default="0,8,32",
+    ap.add_argument("--sub-workloads", default=SUB_WORKLOADS,
+                    help="comma list of further workloads measured briefly under 'workloads' (empty = none)")
+    ap.add_argument("--zero-copy-ctas", default="8,32",
                     help="comma list of CTA caps for the zero-copy streamed variant (0 = all SMs; empty = skip)")
+    ap.add_argument("--adaptive-ctas", type=int, default=32,
+                    help="CTAs of a chunk launch that reads slow host regions in place (adaptive streaming)")
+    ap.add_argument("--staged-ctas", type=int, default=16,
+                    help="CTA budget of staged chunk launches in the Target-priority variant of the copy engine")
     ap.add_argument("--no-draft-load", dest="draft_load", action="store_false",
-                    help="skip timing the streamed round beside a low-priority bf16 GEMM loop (Target priority)")
+                    help="skip timing the streamed step beside a low-priority bf16 GEMM loop (Target priority)")
     ap.add_argument("--slots", type=int, default=3, choices=[2, 3])
     ap.add_argument("--resident-chunk", default="whole", choices=["whole", "plan"],
                     help="device-resident history pushed as one part per request, or in the plan's chunks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-pairs", type=int, default=0, help="(request, KV head) pairs in the CPU sample")
+    ap.add_argument("--cpu-sample-pairs", type=int, default=0,
+                    help="(layer, request, KV head) pairs in each CPU sample (default: one per core)")
     return ap.parse_args(argv)
 
 
@@ -165,7 +180,7 @@ class ClockSampler:
 
 
 def _oracle_pair(args):
-    """Oracle rows of one (request, KV head) pair: all G*nq queries of that KV head."""
+    """Oracle rows of one (layer, request, KV head) triple: all G*nq queries of that KV head."""
     import oracle
     q_bits, kh_bits, vh_bits, kc_bits, vc_bits, vis, scale = args
     f = W.bf16_to_f64
@@ -189,47 +204,58 @@ def cpu_sample_pairs(w: W.Workload, n: int):
     all_pairs = [(b, g) for b in range(w.n_req) for g in range(w.n_kv_heads)]
     rng = np.random.default_rng(123)
     idx = rng.permutation(len(all_pairs))[:n]
-    return [all_pairs[i] for i in sorted(idx)], len(all_pairs)
+    return [all_pairs[i] for i in sorted(idx)]
 
 
-def time_oracle(pool, tasks, n_total_pairs: int, w: W.Workload) -> tuple:
-    """Wall time of the sampled pairs on the pool, scaled to a whole round -> tokens/s."""
+def oracle_sample(pool, tasks, w: W.Workload, n_layers: int) -> dict:
+    """One bounded CPU sample: the oracle over `tasks` (one (request, KV head) pair of one layer each) on
+    the pool.  The fraction of a whole step it covers and the tokens/s that rate gives."""
     t0 = time.perf_counter()
     list(pool.map(_oracle_pair, tasks))
     dt = time.perf_counter() - t0
-    t_round = dt * n_total_pairs / len(tasks)
-    return w.n_req * w.n_query / t_round, dt
+    frac = len(tasks) / (n_layers * w.n_req * w.n_kv_heads)
+    return {"seconds": dt, "step_fraction": frac, "value": w.n_req * w.n_query * frac / dt}
 
 
 # ---------------------------------------------------------------- reference arm
 
 
 def run_reference(a, rank, world):
+    """The float64 oracle on the host cores, on this arm's workload, metric and unit.  Each timed step is
+    one bounded sample (one (request, KV head) pair of layer 0 per core); the line says what fraction of
+    a whole step that is, and `value` is the sample's tokens/s (the fraction of the step's tokens over
+    its time)."""
     if rank != 0:
         return 0
     import multiprocessing as mp
     w = workload_of(a)
+    L = w.n_layers
     cores = os.cpu_count() or 1
-    n_pairs = a.cpu_sample_pairs or min(cores, w.n_req * w.n_kv_heads)
-    pairs, total = cpu_sample_pairs(w, n_pairs)
-    x = W.layer_inputs(w, requests=None)
+    n_pairs = min(a.cpu_sample_pairs or cores, w.n_req * w.n_kv_heads)
+    pairs = cpu_sample_pairs(w, n_pairs)
+    x = W.layer_inputs(w, 0, requests=None) if w.n_layers == 1 or w.hist_bytes < (4 << 30) else None
+    if x is None:  # multi-GiB layers: draw only the sampled requests' histories
+        reqs = sorted({b for b, _g in pairs})
+        xs = W.layer_inputs(w, 0, requests=reqs)
+        full_k, full_v = [None] * w.n_req, [None] * w.n_req
+        for i, b in enumerate(reqs):
+            full_k[b], full_v[b] = xs.k_hist[i], xs.v_hist[i]
+        x = W.LayerInputs(xs.q, full_k, full_v, xs.k_cand, xs.v_cand, xs.parent)
     tasks = oracle_tasks(w, x, pairs)
     ctx = mp.get_context("spawn")
     with ctx.Pool(min(cores, len(tasks))) as pool:
         for _ in range(a.warmup):
-            time_oracle(pool, tasks[:1], total, w)
-        vals, dts = [], []
-        for _ in range(a.steps):
-            v, dt = time_oracle(pool, tasks, total, w)
-            vals.append(v)
-            dts.append(dt)
-    value = statistics.median(vals)
-    ms = statistics.median(dts) * 1e3 * total / len(tasks)
-    sample = (f"{len(tasks)} of {total} (request, KV head) pairs of one round ({len(tasks) * w.group * w.n_query} of "
-              f"{w.n_req * w.n_q_heads * w.n_query} query rows), scaled to the whole round")
+            oracle_sample(pool, tasks[:1], w, L)
+        samples = [oracle_sample(pool, tasks, w, L) for _ in range(a.steps)]
+    value = statistics.median(s["value"] for s in samples)
+    ms = statistics.median(s["seconds"] for s in samples) * 1e3
+    frac = samples[0]["step_fraction"]
+    sample = (f"each step: {len(tasks)} of {L * w.n_req * w.n_kv_heads} (layer, request, KV head) pairs of one step "
+              f"({len(tasks) * w.group * w.n_query} of {L * w.n_req * w.n_q_heads * w.n_query} layer query rows), "
+              f"a {frac:.4f} fraction of the step; value = that fraction of the step's tokens over the sample's time")
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-           "data": "synthetic", "impl": "reference",
+           "data": "synthetic", "impl": "reference", "sampled": True, "step_fraction": frac,
            "config": workload_config(w, a),
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, len(tasks)), "kind": "oracle",
                             "sample": sample},
@@ -240,18 +266,23 @@ def run_reference(a, rank, world):
 
 def workload_of(a) -> W.Workload:
     w = W.named(a.workload)
-    return w.with_(head_dim=a.head_dim) if a.head_dim else w
+    if a.head_dim:
+        w = w.with_(head_dim=a.head_dim)
+    if getattr(a, "layers", None):
+        w = w.with_(n_layers=a.layers)
+    return w
 
 
 def workload_config(w: W.Workload, a) -> dict:
     l2_bytes = 129e6
     per_round = 4 * w.n_kv_heads * w.head_dim * sum(w.hist_len)
-    return {"workload": f"{w.name}: {w.n_req} requests, {w.n_q_heads}/{w.n_kv_heads} heads, d={w.head_dim}, "
+    layers = f"{w.n_layers} layers x " if w.n_layers > 1 else ""
+    return {"workload": f"{w.name}: {layers}{w.n_req} requests, {w.n_q_heads}/{w.n_kv_heads} heads, d={w.head_dim}, "
                         f"history {min(w.hist_len)}..{max(w.hist_len)} tokens, chunk {w.chunk_tokens}, "
                         f"{w.n_query} verify queries ({'token tree' if w.tree else 'causal chain'})",
-            "n_req": w.n_req, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
-            "hist_tokens": int(sum(w.hist_len)), "chunk_tokens": w.chunk_tokens, "n_query": w.n_query,
-            "slots": a.slots, "resident_chunk": a.resident_chunk,
+            "n_layers": w.n_layers, "n_req": w.n_req, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+            "head_dim": w.head_dim, "hist_tokens": int(sum(w.hist_len)), "chunk_tokens": w.chunk_tokens,
+            "n_query": w.n_query, "slots": a.slots, "resident_chunk": a.resident_chunk,
             "l2": (f"no flush: one round reads {per_round / 2**20:.0f} MiB of history, more than the 129 MB L2"
                    if per_round > l2_bytes else
                    f"no flush: one round reads {per_round / 2**10:.0f} KiB of history, which stays in the 129 MB L2"),
@@ -317,6 +348,390 @@ class DraftLoad:
         return self.count * self.flops / dt / 1e12
 
 
+class Inputs:
+    """One workload's inputs on the device and in pinned host memory, per layer.
+
+    History: each layer's K and V as rows of one pinned [B][C_max][Hkv][d] tensor per tensor (the layout
+    of a batched host KV cache: a chunk's parts are equally strided, and the library stages each chunk
+    with one 2D copy for K and one for V), filled from the device-side seeded generator; optionally the
+    same history resident in HBM (device parts, the HBM-bound form)."""
+
+    def __init__(self, w: W.Workload, dev, resident=True):
+        import torch
+        self.w = w
+        B, Hq, Hkv, d, nq = w.n_req, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_query
+        bf = torch.bfloat16
+        self.row_bytes = Hkv * d * 2
+        self.layers = []
+        for layer in range(w.n_layers):
+            kb = torch.empty((B, max(w.hist_len), Hkv, d), dtype=bf, pin_memory=True)
+            vb = torch.empty((B, max(w.hist_len), Hkv, d), dtype=bf, pin_memory=True)
+            kh_h = [kb[b, :C] for b, C in enumerate(w.hist_len)]
+            vh_h = [vb[b, :C] for b, C in enumerate(w.hist_len)]
+            q, kh_d, vh_d, kc, vc, parent = W.layer_inputs_device(w, layer, dev)
+            for b in range(B):
+                kh_h[b].copy_(kh_d[b])
+                vh_h[b].copy_(vh_d[b])
+            ly = dict(q_h=q.cpu().pin_memory(), kc_h=kc.cpu().pin_memory(), vc_h=vc.cpu().pin_memory(),
+                      kh_h=kh_h, vh_h=vh_h, kh_d=kh_d if resident else None, vh_d=vh_d if resident else None,
+                      q_d=q, kc_d=kc, vc_d=vc, parent=parent,
+                      o_d=torch.empty((B, Hq, nq, d), dtype=bf, device=dev),
+                      lse_d=torch.empty((B, Hq, nq), dtype=torch.float32, device=dev),
+                      o_h=torch.empty((B, Hq, nq, d), dtype=bf).pin_memory(),
+                      lse_h=torch.empty((B, Hq, nq), dtype=torch.float32).pin_memory())
+            self.layers.append(ly)
+            del kh_d, vh_d
+        torch.cuda.synchronize(dev)
+        from speculative_decoding_verification_chunked_gb300 import svx
+        self.chunks = {}
+        for j, _s, b, t0, n in svx.plan_chunks(w.hist_len, w.chunk_tokens, 3):
+            self.chunks.setdefault(j, []).append((b, t0, n))
+
+    def parts(self, kh, vh, whole: bool):
+        """Pushes (lists of raw parts) of one layer: one part per request, or the plan's chunks."""
+        w, rb = self.w, self.row_bytes
+        if whole:
+            return [[(b, 0, w.hist_len[b], kh[b].data_ptr(), vh[b].data_ptr()) for b in range(w.n_req)
+                     if w.hist_len[b]]]
+        return [[(b, t0, n, kh[b].data_ptr() + t0 * rb, vh[b].data_ptr() + t0 * rb) for b, t0, n in self.chunks[j]]
+                for j in sorted(self.chunks)]
+
+    def drop_resident(self, keep_first=True):
+        """Free the device duplicates (a streaming deployment does not hold its history in HBM twice)."""
+        import torch
+        for ly in self.layers[1 if keep_first else 0:]:
+            ly["kh_d"] = ly["vh_d"] = None
+        torch.cuda.empty_cache()
+
+    def oracle_layer0(self) -> W.LayerInputs:
+        """Layer 0's inputs as drawn, read back from pinned host memory (bf16 bit patterns)."""
+        import torch
+        u16 = lambda t: t.view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+        ly = self.layers[0]
+        return W.LayerInputs(u16(ly["q_h"]), [u16(k) for k in ly["kh_h"]], [u16(v) for v in ly["vh_h"]],
+                             u16(ly["kc_h"]), u16(ly["vc_h"]), ly["parent"])
+
+
+class Runner:
+    """Timed steps of one workload on one GPU (rank)."""
+
+    def __init__(self, a, w, dev, world, cs, xs):
+        import torch
+        self.torch, self.a, self.w, self.dev, self.world, self.cs, self.xs = torch, a, w, dev, world, cs, xs
+
+    def verifier(self, **kw):
+        from speculative_decoding_verification_chunked_gb300 import svx
+        w = self.w
+        return svx.Verifier(w.n_req, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_query, w.chunk_tokens,
+                            n_slots=self.a.slots, device=self.dev.index, compute_stream=self.cs, copy_stream=self.xs,
+                            **kw)
+
+    def timed(self, step_fn, steps, warmup, between=None):
+        """Mean ms per step over `steps` steps after `warmup`, CUDA events on the compute stream, a barrier and
+        a device synchronisation on both sides.  `between()` runs after the warm-up, before the timing."""
+        torch = self.torch
+        for _ in range(warmup):
+            step_fn()
+        torch.cuda.synchronize(self.dev)
+        if between is not None:
+            between()
+        barrier(self.world)
+        torch.cuda.synchronize(self.dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.cs)
+        for _ in range(steps):
+            step_fn()
+        e1.record(self.cs)
+        torch.cuda.synchronize(self.dev)
+        barrier(self.world)
+        return e0.elapsed_time(e1) / steps
+
+    def round_of(self, v, ly, pushes, timeout_ms=0):
+        v.round_begin(ly["q_d"], self.w.hist_len)
+        v.candidate_attn(ly["kc_d"], ly["vc_d"], ly["parent"])
+        for p in pushes:
+            v.push_raw(p)
+        v.round_finish(ly["o_d"], ly["lse_d"], timeout_ms=timeout_ms)
+
+    def host_step(self, v, inp, pushes_of):
+        """One step with host inputs: Q and candidates copied in, every layer's round, O and LSE copied out
+        and read by the host (the step ends when its result is on the host, as a decode loop needs it to
+        accept or reject the drafts before the next round)."""
+        torch, cs = self.torch, self.cs
+        with torch.cuda.stream(cs):
+            for ly in inp.layers:
+                ly["q_d"].copy_(ly["q_h"], non_blocking=True)
+                ly["kc_d"].copy_(ly["kc_h"], non_blocking=True)
+                ly["vc_d"].copy_(ly["vc_h"], non_blocking=True)
+        for li, ly in enumerate(inp.layers):  # layer l+1's chunk copies queue behind layer l's: prefetch
+            self.round_of(v, ly, pushes_of(li))
+            with torch.cuda.stream(cs):
+                ly["o_h"].copy_(ly["o_d"], non_blocking=True)
+                ly["lse_h"].copy_(ly["lse_d"], non_blocking=True)
+        cs.synchronize()
+
+    def checked(self, v, inp, pushes):
+        """One round of layer 0 whose finish reads the context's device error word: a kernel whose bounded
+        wait ran out in any earlier round of the context raises here, so no line rests on aborted launches."""
+        self.round_of(v, inp.layers[0], pushes, timeout_ms=60000)
+
+
+def copy_rates(iv, push_bytes):
+    """Per-push copy-engine rates (GB/s) from window intervals: min, median, max and the share of pushes
+    below 150 GB/s."""
+    cp = iv[:, 1] - iv[:, 0]
+    ok = np.isfinite(cp) & (cp > 0)
+    if not ok.any():
+        return None
+    r = np.asarray(push_bytes, dtype=np.float64)[ok] / (cp[ok] / 1e3) / 1e9
+    return {"min": float(r.min()), "median": float(np.median(r)), "max": float(r.max()),
+            "below_150_frac": float((r < 150).mean()), "pushes": int(ok.sum())}
+
+
+def link_probe(inp, dev, xs):
+    """Pinned host -> HBM bandwidth now (one 256 MiB copy of layer 0's first K rows, best of 4)."""
+    import torch
+    src = inp.layers[0]["kh_h"][0]
+    n = min(src.shape[0], (256 << 20) // inp.row_bytes)
+    src = src[:n]
+    dst = torch.empty_like(src, device=dev)
+    best = 0.0
+    for _ in range(4):
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(xs):
+            e0.record(xs)
+            dst.copy_(src, non_blocking=True)
+            e1.record(xs)
+        torch.cuda.synchronize(dev)
+        best = max(best, src.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    return best
+
+
+def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
+    """All timed figures of one workload.  `full`: the headline record (every variant); otherwise a
+    shorter sub-record (resident value, kernel roofline, streamed e2e with overlap, zero-copy on 32 CTAs)."""
+    import torch
+    B, nq, L = w.n_req, w.n_query, w.n_layers
+    steps = a.steps if full else min(a.steps, 20)
+    warmup = a.warmup if full else min(a.warmup, 3)
+    inp = Inputs(w, dev)
+    R = Runner(a, w, dev, world, cs, xs)
+    hist_bytes = w.hist_bytes * L
+    row_bytes = inp.row_bytes
+    rec = {"config": workload_config(w, a)}
+
+    # ---- value: resident history (HBM-bound form of the step)
+    res_pushes = [inp.parts(ly["kh_d"], ly["vh_d"], a.resident_chunk == "whole") for ly in inp.layers]
+    v_res = R.verifier()
+
+    def resident_step():
+        for ly, pushes in zip(inp.layers, res_pushes):
+            R.round_of(v_res, ly, pushes)
+
+    ms_res = R.timed(resident_step, steps, warmup)
+    # the same steps with events around every chunk launch (an event between two kernels of a round keeps
+    # the second from launching early, so these are not the value's steps): the dominant kernel's time
+    kern_ev = []
+
+    def resident_step_events():
+        for ly, pushes in zip(inp.layers, res_pushes):
+            v_res.round_begin(ly["q_d"], w.hist_len)
+            v_res.candidate_attn(ly["kc_d"], ly["vc_d"], ly["parent"])
+            for p in pushes:
+                e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                e[0].record(cs)
+                v_res.push_raw(p)
+                e[1].record(cs)
+                kern_ev.append((e, sum(n for _b, _t, n, _k, _v in p)))
+            v_res.round_finish(ly["o_d"], ly["lse_d"])
+
+    R.timed(resident_step_events, steps, 1, between=kern_ev.clear)
+    kern = [(e[0].elapsed_time(e[1]), toks) for e, toks in kern_ev]
+    k1_ms = statistics.mean(k for k, _ in kern)
+    k1_bytes = statistics.mean(t for _, t in kern) * row_bytes * 2
+    R.checked(v_res, inp, res_pushes[0])
+    value, ms_res_job = job_throughput(B * nq, ms_res, world, dev)
+    rec.update(value=value, ms_per_step=ms_res_job, steps=steps, warmup=warmup,
+               launches_per_step=sum(len(p) for p in res_pushes) + L)
+    rec["roofline"] = {"bound": "hbm", "achieved": k1_bytes / (k1_ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                       "frac": k1_bytes / (k1_ms / 1e3) / 1e9 / hbm_peak, "traffic": profiled_traffic(w),
+                       "kernel": "chunk_attn_tc", "peak_source": f"{hbm_src} hbm_gbs (burst copy)",
+                       "algorithmic_bytes_per_launch": int(k1_bytes), "ms_per_launch": k1_ms}
+    rec["resident"] = {"hist_gb_per_s": hist_bytes / (ms_res / 1e3) / 1e9,
+                       "hbm_frac": hist_bytes / (ms_res / 1e3) / 1e9 / hbm_peak}
+    # the same chunks' kernels in resident mode (device parts in the plan's chunks): the compute the
+    # streamed step has to hide, for the hidden fraction over the step
+    v_rt = R.verifier(timing=True)
+    plan_pushes0 = inp.parts(inp.layers[0]["kh_d"], inp.layers[0]["vh_d"], False)
+
+    def resident_plan_step():
+        for ly in inp.layers:
+            R.round_of(v_rt, ly, plan_pushes0)
+
+    R.timed(resident_plan_step, min(steps, 5), 1, between=v_rt.window_reset)
+    res_chunk_ms_step = v_rt.window_stats()["chunk_kernel_ms"] / min(steps, 5)
+    R.checked(v_rt, inp, plan_pushes0)
+    v_rt.close()
+    v_res.close()
+    inp.drop_resident(keep_first=False)
+
+    # ---- e2e: streamed from pinned host through the public API, copies in the timed region
+    stream_pushes = [inp.parts(ly["kh_h"], ly["vh_h"], False) for ly in inp.layers]
+    push_bytes = [sum(n for _b, _t, n, _k, _v in p) * row_bytes * 2 for pl in stream_pushes for p in pl]
+    link_before = link_probe(inp, dev, xs)
+
+    def streamed(v, label, reps=1):
+        """Streamed steps through context v: throughput, overlap over the timed steps (the context's timing
+        window), per-push copy rates."""
+        ms = R.timed(lambda: R.host_step(v, inp, lambda li: stream_pushes[li]), steps, warmup,
+                     between=v.window_reset)
+        ws = v.window_stats()
+        iv = v.window_intervals()
+        val, ms_job = job_throughput(B * nq, ms, world, dev)
+        covered = ws["n_rounds"] / L  # steps in the window (all timed steps unless it filled up)
+        per_step = {k: ws[k] / covered for k in ("window_ms", "copy_busy_ms", "copy_gap_ms", "chunk_kernel_ms",
+                                               "chunk_kernel_exposed_ms", "transfer_busy_ms",
+                                               "zero_copy_kernel_ms", "finish_kernel_ms")}
+        out = {"value": val, "unit": UNIT, "ms_per_step": ms_job, "what": label,
+               "hist_gb_per_s": hist_bytes / (ms / 1e3) / 1e9,
+               "per_step_ms": per_step,
+               "zero_copy_push_frac": ws["n_zero_copy_pushes"] / max(1, ws["n_pushes"]),
+               "copy_rate_gbs": copy_rates(iv, push_bytes * steps) if ws["n_rounds"] == steps * L else None,
+               # chunk compute hidden under transfer: the time of chunk kernels over staged parts that lies
+               # inside transfer intervals (a kernel that reads host memory in place is the transfer)
+               "hidden_frac": (1.0 - ws["chunk_kernel_exposed_ms"] / (ws["chunk_kernel_ms"] - ws["zero_copy_kernel_ms"])
+                               if ws["chunk_kernel_ms"] - ws["zero_copy_kernel_ms"] > 0 else None),
+               # over the whole step: whatever of the step is not transfer time counts as exposed compute,
+               # against the same chunks' kernel time with resident history
+               "hidden_frac_step": 1.0 - max(0.0, per_step["window_ms"] - per_step["transfer_busy_ms"])
+               / res_chunk_ms_step}
+        return out, ms
+
+    v_e2e = R.verifier(timing=True, adaptive=True, zero_copy_ctas=a.adaptive_ctas)
+    e2e_rec, ms_e2e = streamed(v_e2e, f"adaptive copy engine: staged through {a.slots} slots; host regions the "
+                                      f"copy engine reads slowly are read in place on {a.adaptive_ctas} CTAs")
+    e2e_rec["adaptive_state"] = v_e2e.adaptive_state()
+    R.checked(v_e2e, inp, stream_pushes[0])
+    v_ce = R.verifier(timing=True)
+    ce_rec, ms_ce = streamed(v_ce, f"copy engine: every chunk staged through {a.slots} slots")
+    R.checked(v_ce, inp, stream_pushes[0])
+    link_after = link_probe(inp, dev, xs)
+    link_gbs = max(link_before, link_after)
+    for r in (e2e_rec, ce_rec):
+        r["link_frac"] = r["hist_gb_per_s"] / link_gbs
+    e2e_value, ms_e2e_job = job_throughput(B * nq, ms_e2e, world, dev)
+    h2d_step = hist_bytes + sum((ly["q_h"].numel() + ly["kc_h"].numel() + ly["vc_h"].numel()) * 2
+                                for ly in inp.layers)
+    d2h_step = sum(ly["o_h"].numel() * 2 + ly["lse_h"].numel() * 4 for ly in inp.layers)
+    rec["e2e"] = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d_step),
+                  "d2h_bytes_per_step": int(d2h_step), "ms_per_step": ms_e2e_job}
+    rec["streamed"] = dict(e2e_rec, link_gbs=link_gbs, link_gbs_before_after=[link_before, link_after])
+    rec["streamed_copy_engine"] = ce_rec
+
+    # ---- zero-copy: pinned host history read in place by the chunk kernel over the host link
+    zc = {}
+    caps = [int(x) for x in a.zero_copy_ctas.split(",") if x.strip() != ""] if full else [32]
+    zc_ctx = {}
+    for cap in caps:
+        vz = R.verifier(zero_copy=True, zero_copy_ctas=cap)
+        zc_pushes = [inp.parts(ly["kh_h"], ly["vh_h"], True) for ly in inp.layers]
+        ms = R.timed(lambda vz=vz, zp=zc_pushes: R.host_step(vz, inp, lambda li: zp[li]), steps, warmup)
+        R.checked(vz, inp, zc_pushes[0])
+        val, ms_job = job_throughput(B * nq, ms, world, dev)
+        zc[str(cap)] = {"value": val, "unit": UNIT, "ms_per_step": ms_job,
+                        "hist_gb_per_s": hist_bytes / (ms / 1e3) / 1e9,
+                        "link_frac": hist_bytes / (ms / 1e3) / 1e9 / link_gbs,
+                        "ctas": cap if cap > 0 else torch.cuda.get_device_properties(dev).multi_processor_count}
+        zc_ctx[cap] = (vz, zc_pushes, ms)
+    rec["streamed_zero_copy"] = zc
+
+    if full:
+        # ---- restore then verify (the paper's K1 ablation point, SD+Offload): each layer's whole history is
+        # copied to HBM first (one copy per request and tensor), then attended in place
+        restore_k = [torch.empty_like(k, device=dev) for k in inp.layers[0]["kh_h"]]
+        restore_v = [torch.empty_like(v_, device=dev) for v_ in inp.layers[0]["vh_h"]]
+        restored, consumed = torch.cuda.Event(), torch.cuda.Event()
+        consumed.record(cs)
+        rs_pushes = inp.parts(restore_k, restore_v, True)
+        v_rs = R.verifier()
+
+        def restore_step():
+            with torch.cuda.stream(cs):
+                for ly in inp.layers:
+                    ly["q_d"].copy_(ly["q_h"], non_blocking=True)
+                    ly["kc_d"].copy_(ly["kc_h"], non_blocking=True)
+                    ly["vc_d"].copy_(ly["vc_h"], non_blocking=True)
+            for ly in inp.layers:
+                xs.wait_event(consumed)  # the restore buffer is free once the previous layer was attended
+                with torch.cuda.stream(xs):
+                    for b in range(B):
+                        if w.hist_len[b]:
+                            restore_k[b].copy_(ly["kh_h"][b], non_blocking=True)
+                            restore_v[b].copy_(ly["vh_h"][b], non_blocking=True)
+                restored.record(xs)
+                cs.wait_event(restored)
+                R.round_of(v_rs, ly, rs_pushes)
+                consumed.record(cs)
+                with torch.cuda.stream(cs):
+                    ly["o_h"].copy_(ly["o_d"], non_blocking=True)
+                    ly["lse_h"].copy_(ly["lse_d"], non_blocking=True)
+            cs.synchronize()
+
+        ms_rs = R.timed(restore_step, steps, warmup)
+        R.checked(v_rs, inp, rs_pushes)
+        v_rs.close()
+        val_rs, ms_rs_job = job_throughput(B * nq, ms_rs, world, dev)
+        rec["restore_then_verify"] = {"value": val_rs, "unit": UNIT, "ms_per_step": ms_rs_job,
+                                      "streamed_over_restore": ms_rs / ms_e2e,
+                                      "what": "copy each layer's whole history to HBM, then attend (verification "
+                                              "waits for the restore)"}
+        del restore_k, restore_v
+
+        # ---- Target priority: the streamed step again beside a low-priority Draft GEMM loop
+        if a.draft_load:
+            dl = DraftLoad(dev)
+            dl.start()
+            time.sleep(1.0)
+            draft_alone = dl.stop()
+            v_st = R.verifier(staged_ctas=a.staged_ctas, timing=True)
+            st_rec, ms_st = streamed(v_st, f"copy engine, staged chunk launches on {a.staged_ctas} CTAs")
+            rec["streamed_copy_engine_staged"] = dict(st_rec, link_frac=st_rec["hist_gb_per_s"] / link_gbs)
+            modes = [("adaptive_copy_engine", v_e2e, stream_pushes, ms_e2e),
+                     ("copy_engine", v_ce, stream_pushes, ms_ce),
+                     (f"copy_engine_staged_{a.staged_ctas}_ctas", v_st, stream_pushes, ms_st)]
+            for cap, (vz, zp, ms) in zc_ctx.items():
+                modes.append((f"zero_copy_{cap}_ctas", vz, zp, ms))
+            tp = {"draft": "bf16 GEMM 4096^3, CUDA-graph replays of 8 on a lowest-priority stream",
+                  "draft_tflops_alone": draft_alone, "modes": {}}
+            for name, vx, pushes, ms_alone in modes:
+                timing = bool(vx.cfg.flags & 1)
+                dl.start()
+                time.sleep(0.2)
+                ms_co = R.timed(lambda vx=vx, pushes=pushes: R.host_step(vx, inp, lambda li: pushes[li]), steps, 1,
+                                between=vx.window_reset if timing else None)
+                tf = dl.stop()
+                m = {"delta_T": (ms_co - ms_alone) / ms_alone, "target_ms_alone": ms_alone, "target_ms_co": ms_co,
+                     "draft_tflops_co": tf}
+                if timing:  # where the Target's time went beside the Draft: slower copies, or a stalled pipeline
+                    ws = vx.window_stats()
+                    cov = ws["n_rounds"] / L
+                    m["co_per_step_ms"] = {k: ws[k] / cov for k in ("copy_busy_ms", "copy_gap_ms", "chunk_kernel_ms",
+                                                                    "zero_copy_kernel_ms", "transfer_busy_ms")}
+                    m["co_copy_rate_gbs"] = copy_rates(vx.window_intervals(), push_bytes * steps) \
+                        if ws["n_rounds"] == steps * L else None
+                tp["modes"][name] = m
+            R.checked(v_st, inp, stream_pushes[0])
+            v_st.close()
+            rec["target_priority"] = tp
+    for vz, _zp, _ms in zc_ctx.values():
+        vz.close()
+    v_e2e.close()
+    v_ce.close()
+    rec["_inputs"] = inp
+    return rec
+
+
 def main(argv=None):
     a = parse_args(argv)
     rank, world, local = dist_init()
@@ -326,7 +741,6 @@ def main(argv=None):
     import multiprocessing as mp
     w = workload_of(a)
     w = w.with_(seed=w.seed + 1000 * rank)
-    L = w.n_layers
     do_cpu = rank == 0 and world == 1 and not a.no_cpu_baseline
     cores = os.cpu_count() or 1
     pool = None
@@ -334,7 +748,7 @@ def main(argv=None):
         pool = mp.get_context("spawn").Pool(cores)
 
     import torch
-    from speculative_decoding_verification_chunked_gb300 import svx
+    from speculative_decoding_verification_chunked_gb300 import svx  # noqa: F401  (fails loudly if unbuilt)
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -345,360 +759,50 @@ def main(argv=None):
         pass
     hbm_peak = float(peaks.get("hbm_gbs") or FALLBACK_HBM_GBS)
     hbm_src = "measured" if peaks.get("hbm_gbs") else "fallback"
-    B, Hq, Hkv, d, nq = w.n_req, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_query
-    bf = torch.bfloat16
-
-    # ---- inputs: per layer, history in pinned host memory (streamed) and in device memory (resident)
-    def batched_host(lengths, src=None):
-        """The requests' histories as rows of one pinned [B][C_max][Hkv][d] tensor (views of C_b
-        tokens each), the layout of a batched host KV cache: a chunk's parts are then equally strided
-        and the library stages each chunk with one 2D copy for K and one for V."""
-        big = torch.empty((len(lengths), max(lengths), Hkv, d), dtype=bf, pin_memory=True)
-        views = [big[b_, :C] for b_, C in enumerate(lengths)]
-        if src is not None:
-            for v_, t_ in zip(views, src):
-                v_.copy_(t_)
-        return views
-
-    layers = []
-    x0 = None
-    for l in range(L):
-        if L == 1:
-            x = W.layer_inputs(w, l)  # numpy draws; the streamed copies live in batched pinned tensors
-            x0 = x
-            t16 = lambda arr: torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(bf)  # noqa: E731
-            q_h, kc_h, vc_h = (t16(arr).pin_memory() for arr in (x.q, x.k_cand, x.v_cand))
-            kh_h = batched_host(w.hist_len, [t16(k) for k in x.k_hist])
-            vh_h = batched_host(w.hist_len, [t16(v) for v in x.v_hist])
-            kh_d = [k.to(dev) for k in kh_h]
-            vh_d = [v.to(dev) for v in vh_h]
-            parent = x.parent
-        else:
-            kh_h, vh_h = batched_host(w.hist_len), batched_host(w.hist_len)
-            q, kh_d, vh_d, kc, vc, parent = W.layer_inputs_device(w, l, dev)
-            for b in range(B):
-                kh_h[b].copy_(kh_d[b])
-                vh_h[b].copy_(vh_d[b])
-            q_h, kc_h, vc_h = q.cpu().pin_memory(), kc.cpu().pin_memory(), vc.cpu().pin_memory()
-        layers.append(dict(q_h=q_h, kc_h=kc_h, vc_h=vc_h, kh_h=kh_h, vh_h=vh_h, kh_d=kh_d, vh_d=vh_d,
-                           q_d=q_h.to(dev), kc_d=kc_h.to(dev), vc_d=vc_h.to(dev), parent=parent,
-                           o_d=torch.empty((B, Hq, nq, d), dtype=bf, device=dev),
-                           lse_d=torch.empty((B, Hq, nq), dtype=torch.float32, device=dev)))
-        layers[-1]["o_h"] = torch.empty((B, Hq, nq, d), dtype=bf).pin_memory()
-        layers[-1]["lse_h"] = torch.empty((B, Hq, nq), dtype=torch.float32).pin_memory()
-    torch.cuda.synchronize(dev)
-    hist_bytes = w.hist_bytes * L
-    row_bytes = Hkv * d * 2
-
     cs = torch.cuda.Stream(device=dev, priority=-1)
     xs = torch.cuda.Stream(device=dev, priority=-1)
-    v = svx.Verifier(B, Hq, Hkv, d, nq, w.chunk_tokens, n_slots=a.slots, device=local, compute_stream=cs,
-                     copy_stream=xs)
-    plan = svx.plan_chunks(w.hist_len, w.chunk_tokens, a.slots)
-    chunks = {}
-    for j, _s, b, t0, n in plan:
-        chunks.setdefault(j, []).append((b, t0, n))
 
-    def parts_of(kh, vh, whole: bool):
-        if whole:
-            return [[(b, 0, w.hist_len[b], kh[b].data_ptr(), vh[b].data_ptr()) for b in range(B) if w.hist_len[b]]]
-        return [[(b, t0, n, kh[b].data_ptr() + t0 * row_bytes, vh[b].data_ptr() + t0 * row_bytes)
-                 for b, t0, n in chunks[j]] for j in sorted(chunks)]
-
-    for ly in layers:
-        ly["res_pushes"] = parts_of(ly["kh_d"], ly["vh_d"], a.resident_chunk == "whole")
-        ly["res_plan_pushes"] = parts_of(ly["kh_d"], ly["vh_d"], False)
-        ly["stream_pushes"] = parts_of(ly["kh_h"], ly["vh_h"], False)
-    n_res_pushes = len(layers[0]["res_pushes"])
-
-    def checked_round(vx, pushes):
-        """One round of layer 0 whose finish reads the context's device error word.  The word is kept
-        until a finish with a timeout reports it, so a kernel whose bounded wait ran out in any earlier
-        round of the context raises here, and no line is printed over aborted launches."""
-        ly = layers[0]
-        vx.round_begin(ly["q_d"], w.hist_len)
-        vx.candidate_attn(ly["kc_d"], ly["vc_d"], ly["parent"])
-        for p in pushes:
-            vx.push_raw(p)
-        vx.round_finish(ly["o_d"], ly["lse_d"], timeout_ms=60000)
-
-    def resident_step(evs=None):
-        for li, ly in enumerate(layers):
-            v.round_begin(ly["q_d"], w.hist_len)
-            v.candidate_attn(ly["kc_d"], ly["vc_d"], ly["parent"])
-            for i, p in enumerate(ly["res_pushes"]):
-                if evs is not None:
-                    evs[li * n_res_pushes + i][0].record(cs)
-                v.push_raw(p)
-                if evs is not None:
-                    evs[li * n_res_pushes + i][1].record(cs)
-            v.round_finish(ly["o_d"], ly["lse_d"])
-
-    def e2e_step():
-        with torch.cuda.stream(cs):
-            for ly in layers:
-                ly["q_d"].copy_(ly["q_h"], non_blocking=True)
-                ly["kc_d"].copy_(ly["kc_h"], non_blocking=True)
-                ly["vc_d"].copy_(ly["vc_h"], non_blocking=True)
-        for ly in layers:  # layer l+1's chunk copies queue behind layer l's: cross-layer prefetch
-            v.round_begin(ly["q_d"], w.hist_len)
-            v.candidate_attn(ly["kc_d"], ly["vc_d"], ly["parent"])
-            for p in ly["stream_pushes"]:
-                v.push_raw(p)
-            v.round_finish(ly["o_d"], ly["lse_d"])
-            with torch.cuda.stream(cs):
-                ly["o_h"].copy_(ly["o_d"], non_blocking=True)
-                ly["lse_h"].copy_(ly["lse_d"], non_blocking=True)
-
-    def timed(step_fn, steps, warmup, with_events=False):
-        for _ in range(warmup):
-            step_fn() if not with_events else step_fn(None)
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        evs = None
-        if with_events:
-            evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-                    for _ in range(L * n_res_pushes)] for _ in range(steps)]
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(cs)
-        for s_ in range(steps):
-            step_fn(evs[s_]) if with_events else step_fn()
-        e1.record(cs)
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        ms = e0.elapsed_time(e1) / steps
-        kern = None
-        if with_events:
-            kern = [ev[0].elapsed_time(ev[1]) for st in evs for ev in st]
-        return ms, kern
-
-    def link_probe():
-        """Pinned host -> HBM bandwidth of this machine now (one 256 MiB copy, best of 4).  The host memory
-        of a GB300 node is shared with other GPUs' jobs, so it is sampled before and after the
-        streamed phase."""
-        probe_h = layers[0]["kh_h"][0]
-        probe_d = torch.empty_like(probe_h, device=dev)
-        best = 0.0
-        for _ in range(4):
-            torch.cuda.synchronize(dev)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(xs):
-                e0.record(xs)
-                probe_d.copy_(probe_h, non_blocking=True)
-                e1.record(xs)
-            torch.cuda.synchronize(dev)
-            best = max(best, probe_h.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9)
-        return best
-
-    link_before = link_probe()
-    steps = a.steps if L == 1 else max(3, a.steps // 30)
-    warmup = a.warmup if L == 1 else max(3, min(a.warmup, 5))
-    # ---- value: resident history (HBM-bound form)
-    clk = ClockSampler(local).__enter__()  # sampled over both timed regions
-    # the value without per-launch events (an event record between two kernels of a round keeps the
-    # second from being launched early); then the same steps with events around every chunk launch for
-    # the roofline
-    ms_res, _ = timed(resident_step, steps, warmup)
-    _, kern_ms = timed(resident_step, steps, 1, with_events=True)
-    # The streamed phases run without the other layers' device-resident duplicates: a streaming deployment
-    # does not hold its history in HBM twice, and 35 GiB of them slowed the host-to-device copies of the
-    # full-depth round.  Layer 0's copy stays for the overlap comparison.
-    for ly in layers[1:]:
-        ly["kh_d"] = ly["vh_d"] = ly["res_pushes"] = ly["res_plan_pushes"] = None
+    clk = ClockSampler(local).__enter__()  # sampled over every timed region
+    head = measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full=True)
+    inp = head.pop("_inputs")
+    cpu = None
+    if do_cpu:  # the oracle on a bounded sample of the headline step (layer 0's inputs as drawn)
+        n_pairs = min(a.cpu_sample_pairs or cores, w.n_req * w.n_kv_heads)
+        tasks = oracle_tasks(w, inp.oracle_layer0(), cpu_sample_pairs(w, n_pairs))
+        s = oracle_sample(pool, tasks, w, w.n_layers)
+        cpu = {"value": s["value"], "unit": UNIT, "cores": min(cores, len(tasks)), "kind": "oracle",
+               "sample": f"{len(tasks)} of {w.n_layers * w.n_req * w.n_kv_heads} (layer, request, KV head) pairs of "
+                         f"one step in {s['seconds']:.1f} s (a {s['step_fraction']:.4f} fraction of the step); value "
+                         f"= that fraction of the step's tokens over the sample's time"}
+        pool.close()
+    del inp
     torch.cuda.empty_cache()
-    value, ms_res_job = job_throughput(B * nq, ms_res, world, dev)
-    toks_per_launch = [sum(n for _, _, n, _, _ in p) for p in layers[0]["res_pushes"]]
-    k1_ms_per_launch = statistics.mean(kern_ms)
-    k1_bytes_per_launch = statistics.mean(toks_per_launch) * 2 * Hkv * d * 2
-    achieved = k1_bytes_per_launch / (k1_ms_per_launch / 1e3) / 1e9
-
-    # ---- e2e: streamed from pinned host, copies in the timed region
-    ms_e2e, _ = timed(e2e_step, steps, warmup)
-    link_after = link_probe()
-    link_gbs = max(link_before, link_after)
+    subs = {}
+    for name in [n.strip() for n in a.sub_workloads.split(",") if n.strip()]:
+        if name == w.name:
+            continue
+        ws = W.named(name)
+        ws = ws.with_(seed=ws.seed + 1000 * rank)
+        r = measure(a, ws, dev, world, cs, xs, hbm_peak, hbm_src, full=False)
+        r.pop("_inputs")
+        torch.cuda.empty_cache()
+        subs[name] = r
     clk.__exit__(None, None, None)
     clocks = clk.summary()
-    e2e_value, ms_e2e_job = job_throughput(B * nq, ms_e2e, world, dev)
-    h2d_step = hist_bytes + sum((ly["q_h"].numel() + ly["kc_h"].numel() + ly["vc_h"].numel()) * 2 for ly in layers)
-    d2h_step = sum(ly["o_h"].numel() * 2 + ly["lse_h"].numel() * 4 for ly in layers)
 
-    # ---- restore then verify (the paper's K1 ablation point, SD+Offload): each layer's whole history is
-    # copied to HBM first (one copy per request and tensor), then attended in place
-    restore_k = [torch.empty_like(k, device=dev) for k in layers[0]["kh_h"]]
-    restore_v = [torch.empty_like(v_, device=dev) for v_ in layers[0]["vh_h"]]
-    restored = torch.cuda.Event()
-    consumed = torch.cuda.Event()
-    consumed.record(cs)
-    rs_pushes = parts_of(restore_k, restore_v, True)
-
-    def restore_step():
-        with torch.cuda.stream(cs):
-            for ly in layers:
-                ly["q_d"].copy_(ly["q_h"], non_blocking=True)
-                ly["kc_d"].copy_(ly["kc_h"], non_blocking=True)
-                ly["vc_d"].copy_(ly["vc_h"], non_blocking=True)
-        for ly in layers:
-            xs.wait_event(consumed)  # the restore buffer is free once the previous layer has been attended
-            with torch.cuda.stream(xs):
-                for b in range(B):
-                    if w.hist_len[b]:
-                        restore_k[b].copy_(ly["kh_h"][b], non_blocking=True)
-                        restore_v[b].copy_(ly["vh_h"][b], non_blocking=True)
-            restored.record(xs)
-            cs.wait_event(restored)
-            v.round_begin(ly["q_d"], w.hist_len)
-            v.candidate_attn(ly["kc_d"], ly["vc_d"], ly["parent"])
-            for p in rs_pushes:
-                v.push_raw(p)
-            v.round_finish(ly["o_d"], ly["lse_d"])
-            consumed.record(cs)
-            with torch.cuda.stream(cs):
-                ly["o_h"].copy_(ly["o_d"], non_blocking=True)
-                ly["lse_h"].copy_(ly["lse_d"], non_blocking=True)
-
-    ms_rs, _ = timed(restore_step, steps, warmup)
-    val_rs, ms_rs_job = job_throughput(B * nq, ms_rs, world, dev)
-    restore = {"value": val_rs, "unit": UNIT, "ms_per_step": ms_rs_job,
-               "streamed_over_restore": ms_rs / ms_e2e,
-               "what": "copy each layer's whole history to HBM, then attend (verification waits for the restore)"}
-    del restore_k, restore_v
-
-    # ---- zero-copy variant: pinned host history read in place by the chunk kernel over the host link
-    zc_results = {}
-    zc_steps = {}
-    for cap in [int(x) for x in a.zero_copy_ctas.split(",") if x.strip() != ""]:
-        vz = svx.Verifier(B, Hq, Hkv, d, nq, w.chunk_tokens, n_slots=a.slots, device=local, compute_stream=cs,
-                          copy_stream=xs, zero_copy=True, zero_copy_ctas=cap)
-        zc_pushes = [parts_of(ly["kh_h"], ly["vh_h"], True) for ly in layers]
-
-        def zc_step(vz=vz, zc_pushes=zc_pushes):
-            with torch.cuda.stream(cs):
-                for ly in layers:
-                    ly["q_d"].copy_(ly["q_h"], non_blocking=True)
-                    ly["kc_d"].copy_(ly["kc_h"], non_blocking=True)
-                    ly["vc_d"].copy_(ly["vc_h"], non_blocking=True)
-            for ly, pushes in zip(layers, zc_pushes):
-                vz.round_begin(ly["q_d"], w.hist_len)
-                vz.candidate_attn(ly["kc_d"], ly["vc_d"], ly["parent"])
-                for p in pushes:
-                    vz.push_raw(p)
-                vz.round_finish(ly["o_d"], ly["lse_d"])
-                with torch.cuda.stream(cs):
-                    ly["o_h"].copy_(ly["o_d"], non_blocking=True)
-                    ly["lse_h"].copy_(ly["lse_d"], non_blocking=True)
-
-        ms_zc, _ = timed(zc_step, steps, warmup)
-        val_zc, ms_zc_job = job_throughput(B * nq, ms_zc, world, dev)
-        zc_results[str(cap)] = {"value": val_zc, "unit": UNIT, "ms_per_step": ms_zc_job,
-                                "hist_gb_per_s": hist_bytes / (ms_zc / 1e3) / 1e9,
-                                "link_frac": hist_bytes / (ms_zc / 1e3) / 1e9 / link_gbs,
-                                "ctas": cap if cap > 0 else torch.cuda.get_device_properties(dev).multi_processor_count}
-        zc_steps[cap] = (zc_step, vz, zc_pushes[0])
-
-    # ---- Target priority: the streamed round again beside a low-priority Draft GEMM loop
-    interference = None
-    if a.draft_load:
-        dl = DraftLoad(dev)
-        dl.start()
-        time.sleep(1.0)
-        draft_alone = dl.stop()
-        interference = {"draft": "bf16 GEMM 4096^3, CUDA-graph replays of 8 on a lowest-priority stream",
-                        "draft_tflops_alone": draft_alone, "modes": {}}
-        modes = [("copy_engine", e2e_step, ms_e2e)]
-        for cap, (fn, _vz, _p) in zc_steps.items():
-            modes.append((f"zero_copy_{cap}", fn, zc_results[str(cap)]["ms_per_step"]))
-        for name, fn, ms_alone in modes:
-            dl.start()
-            time.sleep(0.2)
-            ms_co, _ = timed(fn, steps, 1)
-            tf = dl.stop()
-            interference["modes"][name] = {"delta_T": (ms_co - ms_alone) / ms_alone, "target_ms_alone": ms_alone,
-                                           "target_ms_co": ms_co, "draft_tflops_co": tf}
-
-    # every context's kernels ran to completion (no bounded wait gave up) in all the passes above
-    checked_round(v, layers[0]["res_pushes"])
-    for _fn, vz, pushes in zc_steps.values():
-        checked_round(vz, pushes)
-
-    # ---- overlap: one timed streamed layer vs the same chunks' kernels in resident mode
-    vt = svx.Verifier(B, Hq, Hkv, d, nq, w.chunk_tokens, n_slots=a.slots, device=local, compute_stream=cs,
-                      copy_stream=xs, timing=True)
-    ly = layers[0]
-    st_s, st_r = [], []
-    for rep in range(3):
-        vt.round_begin(ly["q_d"], w.hist_len)
-        vt.candidate_attn(ly["kc_d"], ly["vc_d"], ly["parent"])
-        for p in ly["stream_pushes"]:
-            vt.push_raw(p)
-        vt.round_finish(ly["o_d"], ly["lse_d"])
-        st_s.append(vt.stats())
-        vt.round_begin(ly["q_d"], w.hist_len)
-        vt.candidate_attn(ly["kc_d"], ly["vc_d"], ly["parent"])
-        for p in ly["res_plan_pushes"]:
-            vt.push_raw(p)
-        vt.round_finish(ly["o_d"], ly["lse_d"])
-        st_r.append(vt.stats())
-    checked_round(vt, ly["res_plan_pushes"])
-    vt.close()
-    s_round = statistics.median(s["round_ms"] for s in st_s)
-    s_copy = statistics.median(s["copy_busy_ms"] for s in st_s)
-    r_chunk = statistics.median(s["chunk_kernel_ms"] for s in st_r)
-    # compute hidden under transfer: chunk-kernel time inside the round's copy intervals
-    hidden = statistics.median(1.0 - s["chunk_kernel_exposed_ms"] / s["chunk_kernel_ms"] for s in st_s)
-    # the coarser bound: whatever of the round is not copy time counts as exposed compute
-    hidden_bound = 1.0 - max(0.0, s_round - s_copy) / r_chunk if r_chunk > 0 else None
-
-    # ---- CPU baseline: the oracle on a bounded sample of the same round
-    cpu = None
-    if do_cpu:
-        n_pairs = a.cpu_sample_pairs or min(cores, B * Hkv)
-        pairs, total = cpu_sample_pairs(w, n_pairs)
-        if x0 is None:  # multi-layer workloads: layer 0's inputs as drawn, read back from pinned memory
-            u16 = lambda t: t.view(torch.int16).numpy().view(np.uint16)  # noqa: E731
-            ly = layers[0]
-            x0 = W.LayerInputs(u16(ly["q_h"]), [u16(k) for k in ly["kh_h"]], [u16(vv) for vv in ly["vh_h"]],
-                               u16(ly["kc_h"]), u16(ly["vc_h"]), ly["parent"])
-        tasks = oracle_tasks(w, x0, pairs)
-        cpu_val, dt = time_oracle(pool, tasks, total * L, w)
-        cpu = {"value": cpu_val, "unit": UNIT, "cores": min(cores, len(tasks)), "kind": "oracle",
-               "sample": f"{len(tasks)} of {total * L} (layer, request, KV head) pairs of one step "
-                         f"({len(tasks) * w.group * nq} of {L * B * Hq * nq} query rows) in {dt:.1f} s, "
-                         f"scaled to the whole step"}
-        pool.close()
-
-    launches_per_step = L * (n_res_pushes + 1)  # chunk kernel launch(es) + the finish kernel per layer
-    out = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": warmup,
-        "ms_per_step": ms_res_job, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic", "config": workload_config(w, a),
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d_step),
-                "d2h_bytes_per_step": int(d2h_step), "ms_per_step": ms_e2e_job},
-        "gpu_launches": launches_per_step * steps,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": profiled_traffic(d, w.name),
-                     "kernel": "chunk_attn_tc",
-                     "peak_source": f"{hbm_src} hbm_gbs (burst copy)",
-                     "algorithmic_bytes_per_launch": int(k1_bytes_per_launch),
-                     "ms_per_launch": k1_ms_per_launch},
-        "streamed": {"hist_gb_per_s": hist_bytes / (ms_e2e / 1e3) / 1e9, "link_gbs": link_gbs,
-                     "link_gbs_before_after": [link_before, link_after],
-                     "link_frac": hist_bytes / (ms_e2e / 1e3) / 1e9 / link_gbs,
-                     "layer_copy_busy_ms": s_copy, "layer_round_ms": s_round, "hidden_frac": hidden,
-                     "hidden_frac_round_minus_copy": hidden_bound,
-                     "layer_resident_chunk_kernel_ms": r_chunk},
-        "resident": {"hist_gb_per_s": hist_bytes / (ms_res / 1e3) / 1e9,
-                     "hbm_frac": hist_bytes / (ms_res / 1e3) / 1e9 / hbm_peak},
-        "clocks": clocks,
-    }
-    out["restore_then_verify"] = restore
-    if zc_results:
-        out["streamed_zero_copy"] = zc_results
-    if interference:
-        out["target_priority"] = interference
+    out = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": head["steps"],
+           "warmup": head["warmup"], "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": head["config"],
+           "e2e": head["e2e"], "gpu_launches": head["launches_per_step"] * head["steps"],
+           "roofline": head["roofline"], "clocks": clocks}
+    for k in ("streamed", "streamed_copy_engine", "resident", "restore_then_verify", "streamed_zero_copy",
+              "target_priority"):
+        if k in head:
+            out[k] = head[k]
     if cpu:
         out["cpu_baseline"] = cpu
-    v.close()
+    if subs:
+        out["workloads"] = subs
     if rank == 0:
         print(json.dumps(out))
     if world > 1:
@@ -720,18 +824,18 @@ def code_digest(path: str) -> str:
     return hashlib.sha256("\n".join(lines).encode()).hexdigest()
 
 
-def profiled_traffic(d: int, workload: str):
-    """DRAM bytes per launch of the tensor-core chunk kernel on this workload (head dimension d) from
-    the committed ncu summary, if that summary was taken on the kernel source as it is now (else None)."""
+def profiled_traffic(w: W.Workload):
+    """DRAM bytes per launch of the tensor-core chunk kernel on this workload from the committed ncu
+    summary, if that summary was taken on the kernel source as it is now (else None)."""
     src = os.path.join(ROOT, "speculative_decoding_verification_chunked_gb300", "csrc", "svx_tc_kernel.cu")
     summ = os.path.join(ROOT, "profiles", "chunk_attn_tc_traffic.txt")
     try:
         kv = {k.strip(): v.strip() for k, v in
               (line.split(":", 1) for line in open(summ) if ":" in line and not line.startswith("#"))}
-        digest = code_digest(src)
-        if kv.get("kernel_code_sha256", "") != digest:
+        if kv.get("kernel_code_sha256", "") != code_digest(src):
             return None
-        return float(kv[f"{workload}.dram_bytes_per_launch" if d == 128 else f"{workload}_d{d}.dram_bytes_per_launch"])
+        key = w.name if w.head_dim == 128 else f"{w.name}_d{w.head_dim}"
+        return float(kv[f"{key}.dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         return None
 

@@ -70,6 +70,9 @@ typedef struct svx_ctx_s* svx_ctx;
 #define SVX_FLAG_NO_TENSOR_CORES 2u  /* run the history chunk kernel on FP32 FMA instead of tcgen05 */
 #define SVX_FLAG_ZERO_COPY 4u        /* read pinned host parts in place over the host link (no staging copy);
                                         the chunk kernel then runs at link speed on zero_copy_ctas SMs */
+#define SVX_FLAG_ADAPTIVE 8u         /* stage pinned host parts through the copy engine, but read in place
+                                        (as SVX_FLAG_ZERO_COPY) those whose host memory the copy engine has
+                                        been measured to read slowly: see below */
 
 /* Context configuration.  Shapes are fixed for the context's lifetime (the
  * Cohort compatibility rule of section 4.2: one layer shape, verification
@@ -91,6 +94,10 @@ typedef struct {
                                max(1, budget / groups) CTAs for each of its groups (one per KV head
                                and pass of up to 64 query rows).  Fewer leave SMs free for
                                co-running work; on GB300, 8 CTAs already fill the host link. */
+  int32_t staged_ctas;      /* CTA budget of chunk launches over parts the copy engine staged; 0 = all
+                               SMs.  Such a launch only has to keep up with the host link, so a few
+                               SMs suffice, and a smaller launch starts sooner beside co-running
+                               work (a Draft model on the other SMs, section 4.3). */
 } svx_config;
 
 /* One request's contiguous slice of committed history, [tok_start, tok_start + n_tok).
@@ -105,6 +112,25 @@ typedef struct {
   const void* k;
   const void* v;
 } svx_part;
+
+/* Adaptive streaming (SVX_FLAG_ADAPTIVE).  How fast the copy engine reads pinned host memory can depend
+ * on the host: on GB300 hosts some pinned buffers were read at 5-150 GB/s by the copy engine while SM
+ * loads of the same buffers (SVX_FLAG_ZERO_COPY on 32 SMs) held the ~210 GB/s of the host link, and the
+ * copy engine slowed by half beside a co-running GEMM while in-place reads did not.  With this flag the
+ * context times its pushes' transfers (CUDA events around each push's copies, or around the chunk kernel
+ * of a push read in place; read without waiting once they have completed) and keeps each engine's
+ * recent ms per GB (decayed sums of time and bytes over about the last 30 pushes).  The engine is chosen per round, when it begins, so no round mixes them:
+ * round 0 is staged and round 1 read in place (each engine measured once); after that, rounds are
+ * staged through the copy engine unless in-place reads on zero_copy_ctas SMs were measured 10% faster
+ * per byte, and one whole round uses the other engine after 8 rounds, then 16, 32, ... up to 1024
+ * while the preference holds (back to 8 when it changes), so a change of either rate is followed.
+ * Results do not depend on the choice (both paths run the same arithmetic); only the transfer engine
+ * changes. */
+
+/* The adaptive policy's current figures: each engine's recent ms per GB of host history (-1 before its
+ * first completed measurement) and whether it now prefers in-place reads.  Host-only; no waiting.
+ * SVX_ERR_BAD_STATE without SVX_FLAG_ADAPTIVE. */
+svx_status svx_adaptive_state(svx_ctx ctx, double* ce_ms_per_gb, double* ip_ms_per_gb, int32_t* prefer_in_place);
 
 /* Allocates n_slots staging slots of max_req * max_chunk_tokens * Hkv * d * 2 bf16 each, the
  * fp32 (m, l, a) workspace and events on cfg->device.  Returns SVX_ERR_OOM, _INVALID_ARG,
@@ -159,6 +185,23 @@ svx_status svx_round_finish(svx_ctx ctx, void* o_dev, float* lse_dev, int32_t ti
  * SVX_ERR_BAD_STATE inside a round. */
 svx_status svx_debug_expire_wait(svx_ctx ctx, int32_t wait_ms);
 
+/* Test hooks of the host-side failure and overlap paths (the pages have no counterpart); they make a
+ * failure on the host, never on the GPU.  Copy submissions are counted from the arming call (1 = the
+ * next one the context issues); nth = 0 disarms.
+ * svx_debug_fail_copy: the nth submission is refused as if cudaMemcpyAsync / cudaMemcpy2DAsync had
+ * failed.  The push that meets it returns SVX_ERR_CUDA without launching its chunk kernel: copies it had
+ * already issued are joined back into the copy stream, its parts do not count as pushed, and the round
+ * stays open, so pushing the same chunk again completes it.  A failure of the CUDA call itself takes
+ * the same path.
+ * svx_debug_delay_copy: the host sleeps delay_ms (0..10000) before the nth submission.  A push's copy
+ * interval starts at its first submission, so a pause before a push's first copy shows as copy-stream
+ * idle time (copy_gap_ms, and chunk_kernel_exposed_ms for a chunk kernel that runs in it), and a pause
+ * between two copies of a push lies inside that push's copy interval (a slow copy).
+ * A 2D copy that the runtime refuses (its rows lie in different allocations; the parts are then copied
+ * one by one) counts as a submission too. */
+svx_status svx_debug_fail_copy(svx_ctx ctx, int64_t nth);
+svx_status svx_debug_delay_copy(svx_ctx ctx, int64_t nth, int32_t delay_ms);
+
 /* Message for the last failing call on ctx (never NULL; "" if none).  NULL ctx: last failure of
  * svx_create or svx_verify_static on this thread. */
 const char* svx_last_error(svx_ctx ctx);
@@ -176,10 +219,54 @@ typedef struct {
   int32_t n_chunk_launches;
   int32_t n_copies;       /* host-to-device copy calls issued: two per host part, or two per chunk when
                              its host parts are equally strided rows of one batched tensor (2D copies) */
-  double chunk_kernel_exposed_ms; /* chunk-kernel time outside every H2D copy interval of the round;
-                                     1 - exposed / chunk_kernel_ms is the compute hidden under transfer */
+  double chunk_kernel_exposed_ms; /* time of chunk kernels that read staged or device parts, outside every
+                                     transfer interval of the round (copies, and the kernels that read host
+                                     parts in place); 1 - exposed / chunk_kernel_ms is the compute hidden
+                                     under transfer */
+  double transfer_busy_ms; /* length of the union of the transfer intervals */
+  int32_t n_zero_copy_pushes; /* pushes whose chunk kernel read host parts in place */
 } svx_stats;
 svx_status svx_round_stats(svx_ctx ctx, svx_stats* out);
+
+/* Timing over several rounds (needs SVX_FLAG_TIMING): the copy/compute timeline of a whole
+ * multi-layer step, where layer l + 1's chunk copies overlap layer l's kernels (section 4.2,
+ * "Pipelined KV transfers and prefetching").  A window opens at the first svx_round_begin after
+ * svx_window_reset (or after svx_create) and takes every round up to the last finished one; it
+ * holds at most 4096 rounds and 65536 pushes, and a round past either limit opens a new window.
+ * Overlap within the window: copy_busy_ms sums the pushes' copy intervals on the copy stream
+ * (slot released -> last copy of the push done), chunk_kernel_ms the chunk kernels' intervals on
+ * the compute stream (from the moment the staging slot is ready), chunk_kernel_exposed_ms the
+ * kernel time outside every copy interval, and copy_gap_ms the copy stream's idle time between its
+ * first copy and its last.  1 - max(0, window_ms - copy_busy_ms) / (the same chunks' kernel time
+ * with resident history) is the hidden fraction of compute over the whole step. */
+typedef struct {
+  double window_ms;        /* first round's begin (or the window's first copy, if that started earlier)
+                              to the last finished round's finish-kernel end */
+  double copy_busy_ms;
+  double copy_gap_ms;
+  double chunk_kernel_ms;
+  double chunk_kernel_exposed_ms;
+  double finish_kernel_ms; /* summed over the window's rounds */
+  double transfer_busy_ms; /* union of copy intervals and in-place (zero-copy) chunk-kernel intervals */
+  double zero_copy_kernel_ms; /* chunk-kernel time of pushes that read host parts in place */
+  int32_t n_zero_copy_pushes;
+  int32_t pad;
+  int64_t h2d_bytes;       /* history bytes staged or read from host memory in the window */
+  int64_t device_bytes;    /* history bytes read in place from device memory */
+  int32_t n_rounds;
+  int32_t n_pushes;
+  int32_t n_chunk_launches;
+  int32_t n_copies;
+} svx_window_summary;
+/* Opens a new window at the next svx_round_begin.  SVX_ERR_BAD_STATE inside a round. */
+svx_status svx_window_reset(svx_ctx ctx);
+/* Waits for the window's last finished round, then reports it.  SVX_ERR_BAD_STATE if none. */
+svx_status svx_window_stats(svx_ctx ctx, svx_window_summary* out);
+/* The window's pushes in issue order, 4 doubles each: copy start, copy end (both NaN for a push
+ * without copies), chunk-kernel start, end; ms from the window's first round begin (a copy that the
+ * copy stream started before the compute stream reached that event has a negative start).  Writes at most
+ * cap pushes to out and the count to *n_out.  Waits like svx_window_stats. */
+svx_status svx_window_intervals(svx_ctx ctx, double* out, int64_t cap, int64_t* n_out);
 
 /* ---- host-only bookkeeping (no GPU needed) ----------------------------------------------- */
 
@@ -247,8 +334,9 @@ svx_status svx_plan_tc(int32_t n_parts, const int32_t* n_tok, int32_t n_kv_heads
  *   parent_host      NULL (causal chain) or int32[n_req][n_query] token-tree parents
  *   scale            0 means 1/sqrt(head_dim)
  *   o_dev, lse_dev   bf16 [n_req][n_q_heads][n_query][head_dim], fp32 [n_req][n_q_heads][n_query]
- * Rounds whose state does not fit (about 3,500 query rows at head_dim 128) return
- * SVX_ERR_INVALID_ARG and enqueue nothing.  The first call on a device sets up the scratch
+ * The state needs 8 * (16 + 4 * head_dim) bytes per query row (n_req * n_q_heads * n_query rows)
+ * after a 256-byte header, so a call takes at most 7,943 query rows at head_dim 128 and 15,420 at
+ * head_dim 64; larger rounds return SVX_ERR_INVALID_ARG and enqueue nothing.  The first call on a device sets up the scratch
  * (cudaGetSymbolAddress and a zeroing cudaMemset, synchronous); make that first call before any
  * stream capture.  All calls share the one array: calls whose GPU work overlaps (different
  * streams, or several host threads) race and give wrong results - order them on one stream.
@@ -380,6 +468,11 @@ svx_status svx_width_cost(svx_width w, int32_t q, double* cost_out);
 
 /* Library version string. */
 const char* svx_version(void);
+
+/* sizeof of the ABI's structs, for bindings to check their layouts: svx_config, svx_part, svx_stats,
+ * svx_window_summary, svx_plan_entry, svx_tier_state, svx_sched_config, svx_draft_instr, in this order.
+ * Writes min(cap, count) entries to out and returns the count.  Host-only. */
+int32_t svx_abi_sizes(int64_t* out, int32_t cap);
 
 #ifdef __cplusplus
 }

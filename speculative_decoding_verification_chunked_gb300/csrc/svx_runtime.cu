@@ -38,7 +38,31 @@ constexpr ptrdiff_t kMaxCopyPitch = ptrdiff_t(1) << 31;  // larger source stride
 struct PushEvents {
   cudaEvent_t copy0, copy1, k0, k1;
   bool has_copy;
+  bool zero_copy;  // the push's chunk kernel read host parts in place (no copy)
 };
+
+// Adaptive streaming (SVX_FLAG_ADAPTIVE): the context measures both transfer engines on its own pushes
+// and uses the faster one.
+constexpr int kRateRing = 4096;      // pushes whose transfer time is still to be read
+constexpr double kAdaptDecay = 0.97;     // per-sample decay of the time and byte sums (~33 pushes)
+constexpr double kAdaptMargin = 0.10;   // in-place reads must be this much faster to replace the copy engine
+constexpr int64_t kExploreFirst = 8;    // rounds between two measurements of the other engine, at first
+constexpr int64_t kExploreMax = 1024;   // ... doubling after each measurement up to this
+
+struct RateSample {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  int64_t bytes = 0;
+  bool in_place = false;  // timed chunk kernel that read host parts in place; else the push's copies
+};
+
+struct RoundEvents {
+  cudaEvent_t begin, f0, f1;
+};
+
+// A timing window holds at most this many rounds and pushes; a round that would pass either limit
+// starts a new window.
+constexpr int kWindowRounds = 4096;
+constexpr int kWindowPushes = 65536;
 
 }  // namespace
 
@@ -91,15 +115,37 @@ struct svx_ctx_s {
   std::vector<std::array<int64_t, 3>> parts_seen;  // (req, tok_start, n_tok)
   bool cand_done = false;
 
-  // timing (SVX_FLAG_TIMING)
+  // timing (SVX_FLAG_TIMING): event pools indexed by round and by push since the timing window began
   std::vector<PushEvents> ev_push;
-  int n_push = 0;
-  cudaEvent_t ev_begin = nullptr, ev_f0 = nullptr, ev_f1 = nullptr;
-  bool stats_valid = false;
+  std::vector<RoundEvents> ev_round;
+  int n_push = 0;          // pushes recorded in the window
+  int n_round = 0;         // rounds begun in the window
+  int round_push0 = 0;     // first push of the open round
+  bool window_restart = true;  // the next round starts a new window
   int64_t h2d_bytes = 0, dev_bytes = 0;
   int n_launch = 0, n_copies = 0;
+  int64_t win_h2d = 0, win_dev = 0;
+  int win_launch = 0, win_copies = 0, win_rounds_done = 0;
   svx_stats last_stats{};
+  int last_round = -1, last_push0 = 0, last_push1 = 0;  // the last finished round of the window
   bool last_stats_pending = false;
+
+  // adaptive streaming: decayed sums of transfer ms and GB of host history for each engine, whose ratio
+  // is the engine's recent ms per GB (< 0: not measured)
+  std::vector<RateSample> rate_ring;
+  int rate_head = 0, rate_tail = 0;  // samples [tail, head) wait for their transfers to complete
+  double ce_ms = 0.0, ce_gb = 0.0, ip_ms = 0.0, ip_gb = 0.0;
+  double ce_ms_per_gb = -1.0, ip_ms_per_gb = -1.0;
+  int ce_pending = 0, ip_pending = 0;  // samples in flight per engine
+  int64_t adapt_rounds = 0;            // rounds begun under the policy
+  int64_t next_explore = 1, explore_gap = kExploreFirst;
+  bool prefer_ip = false;              // the engine the measurements favour
+  bool round_ip = false;               // the open round reads its host parts in place
+  int n_zc_push = 0;                 // pushes of the open round read in place by the adaptive policy
+
+  // host-side fault injection (test hooks): copy submissions counted from the arming call
+  int64_t copy_seq = 0, fail_at = 0, delay_at = 0;
+  int32_t delay_ms = 0;
 
   std::string err;
 };
@@ -226,8 +272,14 @@ void destroy_all(svx_ctx c) {
   for (auto& pe : c->ev_push) {
     cudaEventDestroy(pe.copy0); cudaEventDestroy(pe.copy1); cudaEventDestroy(pe.k0); cudaEventDestroy(pe.k1);
   }
-  for (cudaEvent_t e : {c->ev_begin, c->ev_f0, c->ev_f1, c->done})
-    if (e) cudaEventDestroy(e);
+  for (auto& re : c->ev_round) {
+    cudaEventDestroy(re.begin); cudaEventDestroy(re.f0); cudaEventDestroy(re.f1);
+  }
+  if (c->done) cudaEventDestroy(c->done);
+  for (auto& rs : c->rate_ring) {
+    if (rs.e0) cudaEventDestroy(rs.e0);
+    if (rs.e1) cudaEventDestroy(rs.e1);
+  }
   if (c->ws_h) cudaFree(c->ws_h);
   if (c->d_err) cudaFree(c->d_err);
   if (c->ws_a) cudaFree(c->ws_a);
@@ -282,7 +334,17 @@ uint32_t nonempty_splits(int64_t n_tok, int splits) {
 
 extern "C" {
 
-const char* svx_version(void) { return "svx 0.1.0 (sm_103a)"; }
+const char* svx_version(void) { return "svx 0.2.0 (sm_103a)"; }
+
+int32_t svx_abi_sizes(int64_t* out, int32_t cap) {
+  const int64_t sz[] = {static_cast<int64_t>(sizeof(svx_config)),     static_cast<int64_t>(sizeof(svx_part)),
+                        static_cast<int64_t>(sizeof(svx_stats)),      static_cast<int64_t>(sizeof(svx_window_summary)),
+                        static_cast<int64_t>(sizeof(svx_plan_entry)), static_cast<int64_t>(sizeof(svx_tier_state)),
+                        static_cast<int64_t>(sizeof(svx_sched_config)), static_cast<int64_t>(sizeof(svx_draft_instr))};
+  const int32_t n = static_cast<int32_t>(sizeof(sz) / sizeof(sz[0]));
+  for (int32_t i = 0; i < n && i < cap; ++i) out[i] = sz[i];
+  return n;
+}
 
 const char* svx_last_error(svx_ctx ctx) { return ctx ? ctx->err.c_str() : g_create_error.c_str(); }
 
@@ -302,6 +364,7 @@ svx_status svx_create(const svx_config* cfg, svx_ctx* out) {
   if (k.max_chunk_tokens < 1) return fail(nullptr, SVX_ERR_INVALID_ARG, "max_chunk_tokens must be >= 1");
   if (k.n_slots < 2 || k.n_slots > 3) return fail(nullptr, SVX_ERR_INVALID_ARG, "n_slots must be 2 or 3");
   if (k.zero_copy_ctas < 0) return fail(nullptr, SVX_ERR_INVALID_ARG, "zero_copy_ctas must be >= 0");
+  if (k.staged_ctas < 0) return fail(nullptr, SVX_ERR_INVALID_ARG, "staged_ctas must be >= 0");
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
     cudaGetLastError();
@@ -380,12 +443,6 @@ svx_status svx_create(const svx_config* cfg, svx_ctx* out) {
   }
   c->done = make_event(false);
   if (!c->done) return bail(SVX_ERR_CUDA, "event creation failed");
-  if (k.flags & SVX_FLAG_TIMING) {
-    c->ev_begin = make_event(true);
-    c->ev_f0 = make_event(true); c->ev_f1 = make_event(true);
-    if (!c->ev_begin || !c->ev_f0 || !c->ev_f1)
-      return bail(SVX_ERR_CUDA, "event creation failed");
-  }
   *out = c;
   return SVX_OK;
 }
@@ -394,6 +451,10 @@ svx_status svx_destroy(svx_ctx ctx) {
   destroy_all(ctx);
   return SVX_OK;
 }
+
+namespace {
+bool choose_round_in_place(svx_ctx c);  // adaptive streaming, below
+}  // namespace
 
 svx_status svx_round_begin(svx_ctx c, int32_t n_req, int32_t n_query, const void* q_dev, const int64_t* hist_len,
                            float scale) {
@@ -419,12 +480,31 @@ svx_status svx_round_begin(svx_ctx c, int32_t n_req, int32_t n_query, const void
   c->slot_mask.assign(static_cast<size_t>(n_req), 0u);
   c->parts_seen.clear();
   c->cand_done = false;
-  c->n_push = 0;
-  c->last_stats_pending = false;
   c->h2d_bytes = c->dev_bytes = 0;
   c->n_launch = c->n_copies = 0;
+  c->n_zc_push = 0;
+  c->round_ip = (c->cfg.flags & SVX_FLAG_ADAPTIVE) ? choose_round_in_place(c) : false;
   c->epoch = c->epoch == 0xffffffffu ? 1u : c->epoch + 1u;
-  if (c->cfg.flags & SVX_FLAG_TIMING) SVX_CUDA(c, cudaEventRecord(c->ev_begin, c->cs));
+  if (c->cfg.flags & SVX_FLAG_TIMING) {
+    if (c->window_restart || c->n_round >= kWindowRounds || c->n_push >= kWindowPushes) {
+      c->n_round = c->n_push = 0;
+      c->win_h2d = c->win_dev = 0;
+      c->win_launch = c->win_copies = c->win_rounds_done = 0;
+      c->last_stats_pending = false;
+      c->window_restart = false;
+    }
+    if (c->n_round >= static_cast<int>(c->ev_round.size())) {
+      RoundEvents re{make_event(true), make_event(true), make_event(true)};
+      if (!re.begin || !re.f0 || !re.f1) {
+        for (cudaEvent_t e : {re.begin, re.f0, re.f1})
+          if (e) cudaEventDestroy(e);
+        return fail(c, SVX_ERR_CUDA, "event creation failed");
+      }
+      c->ev_round.push_back(re);
+    }
+    SVX_CUDA(c, cudaEventRecord(c->ev_round[static_cast<size_t>(c->n_round)].begin, c->cs));
+    c->round_push0 = c->n_push;
+  }
   c->state = RoundState::kOpen;
   return SVX_OK;
 }
@@ -483,6 +563,76 @@ svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, int cta_cap) {
   return SVX_OK;
 }
 
+// Adaptive streaming: reads the transfer times of pushes whose transfers have completed (without
+// waiting) into their engine's decayed sums.  The ratio of sums is the time per byte over the recent
+// pushes, which weighs a slow push by its time (a per-push average of rates would not: copy rates on
+// some hosts are bimodal, full speed or a tenth of it).
+void harvest_rates(svx_ctx c) {
+  while (c->rate_tail != c->rate_head) {
+    RateSample& rs = c->rate_ring[static_cast<size_t>(c->rate_tail)];
+    const cudaError_t q = cudaEventQuery(rs.e1);
+    if (q == cudaErrorNotReady) break;
+    float ms = 0.f;
+    if (q == cudaSuccess && cudaEventElapsedTime(&ms, rs.e0, rs.e1) == cudaSuccess && ms > 0.f && rs.bytes > 0) {
+      double& sm = rs.in_place ? c->ip_ms : c->ce_ms;
+      double& sg = rs.in_place ? c->ip_gb : c->ce_gb;
+      sm = kAdaptDecay * sm + static_cast<double>(ms);
+      sg = kAdaptDecay * sg + static_cast<double>(rs.bytes) / 1e9;
+      (rs.in_place ? c->ip_ms_per_gb : c->ce_ms_per_gb) = sm / sg;
+    } else {
+      cudaGetLastError();
+    }
+    (rs.in_place ? c->ip_pending : c->ce_pending) -= 1;
+    c->rate_tail = (c->rate_tail + 1) % kRateRing;
+  }
+}
+
+// The engine for a round's host parts (true = read in place), chosen when the round begins, so that no
+// round mixes the engines (an in-place kernel ahead of staged ones on the compute stream would hold back
+// their slots, and so the copy engine).  Round 0 is staged, round 1 read in place (each engine measured
+// once); then the copy engine unless in-place reads were measured kAdaptMargin faster per byte, and a
+// whole round on the other engine every explore_gap rounds, the gap doubling while the preference holds.
+bool choose_round_in_place(svx_ctx c) {
+  harvest_rates(c);
+  const int64_t r = c->adapt_rounds++;
+  if (r == 0) return false;
+  if (r == 1) return true;
+  const bool pref = c->ce_ms_per_gb >= 0.0 && c->ip_ms_per_gb >= 0.0 &&
+                    c->ip_ms_per_gb * (1.0 + kAdaptMargin) < c->ce_ms_per_gb;
+  if (pref != c->prefer_ip) {  // the preference changed: measure the other engine again soon
+    c->prefer_ip = pref;
+    c->explore_gap = kExploreFirst;
+    c->next_explore = r + kExploreFirst;
+  }
+  if (r >= c->next_explore) {
+    c->next_explore = r + c->explore_gap;
+    c->explore_gap = std::min(kExploreMax, 2 * c->explore_gap);
+    return !pref;
+  }
+  return pref;
+}
+
+// A ring entry for the next transfer sample (the oldest is dropped when the ring is full).
+RateSample* next_sample(svx_ctx c) {
+  if (c->rate_ring.empty()) c->rate_ring.resize(kRateRing);
+  const int next = (c->rate_head + 1) % kRateRing;
+  if (next == c->rate_tail) {
+    (c->rate_ring[static_cast<size_t>(c->rate_tail)].in_place ? c->ip_pending : c->ce_pending) -= 1;
+    c->rate_tail = (c->rate_tail + 1) % kRateRing;
+  }
+  RateSample* rs = &c->rate_ring[static_cast<size_t>(c->rate_head)];
+  if (!rs->e0) rs->e0 = make_event(true);
+  if (!rs->e1) rs->e1 = make_event(true);
+  return rs->e0 && rs->e1 ? rs : nullptr;
+}
+
+void commit_sample(svx_ctx c, RateSample* rs, int64_t bytes, bool in_place) {
+  rs->bytes = bytes;
+  rs->in_place = in_place;
+  (in_place ? c->ip_pending : c->ce_pending) += 1;
+  c->rate_head = (c->rate_head + 1) % kRateRing;
+}
+
 }  // namespace
 
 svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
@@ -523,9 +673,27 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
       ++n_host;
     }
   }
-  const bool timing = (c->cfg.flags & SVX_FLAG_TIMING) != 0;
+  std::vector<int> host_idx;  // parts the copy engine stages, in slot order
+  for (int i = 0; i < n_parts; ++i)
+    if (kind[static_cast<size_t>(i)] == 1) host_idx.push_back(i);
+  const size_t row_bytes = static_cast<size_t>(row_elems) * 2;
+  const bool adaptive = (c->cfg.flags & SVX_FLAG_ADAPTIVE) != 0;
+  bool adaptive_ip = false;  // this push's host parts are read in place by the adaptive policy
+  int64_t host_bytes = 0;
+  if (adaptive && n_host > 0) {
+    harvest_rates(c);
+    for (int i : host_idx) host_bytes += 2 * static_cast<int64_t>(parts[i].n_tok) * static_cast<int64_t>(row_bytes);
+    if (c->round_ip) {
+      for (int i : host_idx) kind[static_cast<size_t>(i)] = 3;
+      host_idx.clear();
+      n_host = 0;
+      adaptive_ip = true;
+      ++c->n_zc_push;
+    }
+  }
+  const bool timing = (c->cfg.flags & SVX_FLAG_TIMING) != 0 && c->n_push < kWindowPushes;
   if (timing && c->n_push >= static_cast<int>(c->ev_push.size())) {
-    PushEvents pe{make_event(true), make_event(true), make_event(true), make_event(true), false};
+    PushEvents pe{make_event(true), make_event(true), make_event(true), make_event(true), false, false};
     if (!pe.copy0 || !pe.copy1 || !pe.k0 || !pe.k1) return fail(c, SVX_ERR_CUDA, "event creation failed");
     c->ev_push.push_back(pe);
   }
@@ -539,22 +707,17 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
     slot = c->next_slot;
     c->next_slot = (c->next_slot + 1) % c->cfg.n_slots;
     SVX_CUDA(c, cudaStreamWaitEvent(c->xs, c->slot_free[static_cast<size_t>(slot)], 0));
-    if (pe) SVX_CUDA(c, cudaEventRecord(pe->copy0, c->xs));
-    // fork: the further copy streams start after the slot is free (and after copy0)
+    RateSample* rs = nullptr;
+    if (adaptive) {  // this push's copy time, read by a later push once the copies have completed
+      rs = next_sample(c);
+      if (!rs) return fail(c, SVX_ERR_CUDA, "event creation failed");
+    }
     const size_t si = static_cast<size_t>(slot);
-    SVX_CUDA(c, cudaEventRecord(c->fork_ev[si], c->xs));
-    for (auto s : c->xs_more) SVX_CUDA(c, cudaStreamWaitEvent(s, c->fork_ev[si], 0));
-    size_t nc = 0;  // copies issued; copy n goes to stream n % kCopyStreams
-    auto copy_stream = [&]() { const size_t k = nc++ % kCopyStreams; return k == 0 ? c->xs : c->xs_more[k - 1]; };
     // Host part h goes to slot position h: K at 2h * part_elems, V right after it.  When the host parts
     // have one length and their K (and V) pointers are equally strided in increasing order -- the
     // requests' rows of one batched [B][C][Hkv][d] tensor -- one 2D copy moves all K parts and one
     // all V parts (qwen3 chunks: 208 GB/s against 192 GB/s for 4 MiB copies one by one).
-    std::vector<int> host_idx;
-    for (int i = 0; i < n_parts; ++i)
-      if (kind[static_cast<size_t>(i)] == 1) host_idx.push_back(i);
     const size_t dpitch = static_cast<size_t>(2 * c->part_elems) * 2;
-    const size_t row_bytes = static_cast<size_t>(row_elems) * 2;
     bool strided = host_idx.size() > 1;
     ptrdiff_t sk = 0, sv = 0;
     if (strided) {
@@ -571,29 +734,86 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
                   static_cast<const char*>(p.v) - v0 == static_cast<ptrdiff_t>(h) * sv;
       }
     }
+    // Two copies (one K and one V, 2D or of a single part) go on the copy stream alone: one stream already
+    // fills the host link with large copies, and each fork/join adds commands between pushes.  More copies
+    // are spread over the further streams, forked from and joined back into it.
+    const bool fork = !strided && host_idx.size() > 1;
+    // Right before the push's first copy is submitted (so a host-side pause before it shows as copy-stream
+    // idle time, not as copy time): the copy-start events, then the fork, after which the further copy
+    // streams start (after the slot is free).
+    bool started = false;
+    auto start_copies = [&]() -> cudaError_t {
+      if (started) return cudaSuccess;
+      started = true;
+      cudaError_t e = cudaSuccess;
+      if (pe && e == cudaSuccess) e = cudaEventRecord(pe->copy0, c->xs);
+      if (rs && e == cudaSuccess) e = cudaEventRecord(rs->e0, c->xs);
+      if (fork && e == cudaSuccess) e = cudaEventRecord(c->fork_ev[si], c->xs);
+      for (auto s : c->xs_more)
+        if (fork && e == cudaSuccess) e = cudaStreamWaitEvent(s, c->fork_ev[si], 0);
+      return e;
+    };
+    size_t nc = 0;  // copies issued; with the fork, copy n goes to stream n % kCopyStreams
+    auto copy_stream = [&]() {
+      const size_t k = fork ? nc++ % kCopyStreams : 0;
+      return k == 0 ? c->xs : c->xs_more[k - 1];
+    };
+    const int64_t h2d0 = c->h2d_bytes;
+    const int copies0 = c->n_copies;
+    // A copy submission that fails leaves the push unprocessed: the further streams are joined back (so
+    // later pushes stay ordered after the copies already issued), no kernel is launched, the parts do not
+    // count as pushed, and the round stays open for the chunk to be pushed again.
+    auto abandon = [&](const char* what, cudaError_t e) -> svx_status {
+      for (size_t k = 0; started && fork && k < c->xs_more.size(); ++k) {
+        cudaEventRecord(c->join_ev[si][k], c->xs_more[k]);
+        cudaStreamWaitEvent(c->xs, c->join_ev[si][k], 0);
+      }
+      c->h2d_bytes = h2d0;
+      c->n_copies = copies0;
+      return fail(c, SVX_ERR_CUDA, "%s failed: %s; the chunk was not processed (the round stays open)", what,
+                  e == cudaSuccess ? "injected failure" : cudaGetErrorString(e));
+    };
+    // Every copy submission passes the test hooks first: a host-side delay, or a refusal (reported as
+    // cudaSuccess with `injected` set, so that it is told apart from a refusal by the runtime).
+    bool injected = false;
+    auto hooks = [&]() {
+      ++c->copy_seq;
+      if (c->delay_at > 0 && c->copy_seq == c->delay_at) {
+        c->delay_at = 0;
+        std::this_thread::sleep_for(std::chrono::milliseconds(c->delay_ms));
+      }
+      if (c->fail_at > 0 && c->copy_seq == c->fail_at) {
+        c->fail_at = 0;
+        injected = true;
+      }
+      return !injected;
+    };
     __nv_bfloat16* const slot_base = c->slot_buf[static_cast<size_t>(slot)];
     // A 2D copy reads only its rows, each a whole part inside its own pinned allocation.  When the rows
     // belong to different allocations cudaMemcpy2DAsync refuses the call (invalid value, nothing enqueued);
     // those parts are then copied one by one.
-    auto copy_2d = [&](__nv_bfloat16* dst, const void* src, ptrdiff_t spitch, bool& ok) -> svx_status {
-      if (!ok) return SVX_OK;
+    auto copy_2d = [&](__nv_bfloat16* dst, const void* src, ptrdiff_t spitch, bool& ok) -> cudaError_t {
+      if (!ok) return cudaSuccess;
+      if (!hooks()) return cudaSuccess;
+      const cudaError_t es = start_copies();
+      if (es != cudaSuccess) return es;
       const size_t width = static_cast<size_t>(parts[host_idx[0]].n_tok) * row_bytes;
       const cudaError_t e = cudaMemcpy2DAsync(dst, dpitch, src, static_cast<size_t>(spitch), width, host_idx.size(),
                                               cudaMemcpyHostToDevice, copy_stream());
       if (e == cudaSuccess) {
         c->n_copies += 1;
-        return SVX_OK;
+        return cudaSuccess;
       }
-      if (e != cudaErrorInvalidValue) return fail(c, SVX_ERR_CUDA, "cudaMemcpy2DAsync failed: %s", cudaGetErrorString(e));
+      if (e != cudaErrorInvalidValue) return e;
       cudaGetLastError();
       ok = false;
-      return SVX_OK;
+      return cudaSuccess;
     };
     bool k2d = strided, v2d = strided;
-    svx_status cst = copy_2d(slot_base, strided ? parts[host_idx[0]].k : nullptr, sk, k2d);
-    if (cst != SVX_OK) return cst;
-    cst = copy_2d(slot_base + c->part_elems, strided ? parts[host_idx[0]].v : nullptr, sv, v2d);
-    if (cst != SVX_OK) return cst;
+    cudaError_t ce = copy_2d(slot_base, strided ? parts[host_idx[0]].k : nullptr, sk, k2d);
+    if (ce != cudaSuccess || injected) return abandon("cudaMemcpy2DAsync", ce);
+    ce = copy_2d(slot_base + c->part_elems, strided ? parts[host_idx[0]].v : nullptr, sv, v2d);
+    if (ce != cudaSuccess || injected) return abandon("cudaMemcpy2DAsync", ce);
     for (size_t h = 0; h < host_idx.size(); ++h) {
       const int i = host_idx[h];
       const svx_part& p = parts[i];
@@ -601,22 +821,30 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
       __nv_bfloat16* dv = dk + c->part_elems;
       const size_t bytes = static_cast<size_t>(p.n_tok) * row_bytes;
       if (!k2d) {
-        SVX_CUDA(c, cudaMemcpyAsync(dk, p.k, bytes, cudaMemcpyHostToDevice, copy_stream()));
+        if (hooks()) ce = start_copies();
+        if (ce == cudaSuccess && !injected) ce = cudaMemcpyAsync(dk, p.k, bytes, cudaMemcpyHostToDevice, copy_stream());
+        if (ce != cudaSuccess || injected) return abandon("cudaMemcpyAsync", ce);
         c->n_copies += 1;
       }
       if (!v2d) {
-        SVX_CUDA(c, cudaMemcpyAsync(dv, p.v, bytes, cudaMemcpyHostToDevice, copy_stream()));
+        if (hooks()) ce = start_copies();
+        if (ce == cudaSuccess && !injected) ce = cudaMemcpyAsync(dv, p.v, bytes, cudaMemcpyHostToDevice, copy_stream());
+        if (ce != cudaSuccess || injected) return abandon("cudaMemcpyAsync", ce);
         c->n_copies += 1;
       }
       desc[static_cast<size_t>(i)] = PartDesc{dk, dv, 0, p.req, p.n_tok};
       c->h2d_bytes += 2 * static_cast<int64_t>(bytes);
     }
     // join: the copy stream waits for the further ones, then marks the slot ready
-    for (size_t k = 0; k < c->xs_more.size(); ++k) {
+    for (size_t k = 0; fork && k < c->xs_more.size(); ++k) {
       SVX_CUDA(c, cudaEventRecord(c->join_ev[si][k], c->xs_more[k]));
       SVX_CUDA(c, cudaStreamWaitEvent(c->xs, c->join_ev[si][k], 0));
     }
     if (pe) SVX_CUDA(c, cudaEventRecord(pe->copy1, c->xs));
+    if (rs) {
+      SVX_CUDA(c, cudaEventRecord(rs->e1, c->xs));
+      commit_sample(c, rs, c->h2d_bytes - h2d0, false);
+    }
     SVX_CUDA(c, cudaEventRecord(c->slot_ready[static_cast<size_t>(slot)], c->xs));
     SVX_CUDA(c, cudaStreamWaitEvent(c->cs, c->slot_ready[static_cast<size_t>(slot)], 0));
   }
@@ -633,10 +861,21 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
   }
   if (pe) {
     pe->has_copy = n_host > 0;
+    pe->zero_copy = zero_copy;
     SVX_CUDA(c, cudaEventRecord(pe->k0, c->cs));
   }
-  svx_status st = launch_parts(c, desc, zero_copy ? c->cfg.zero_copy_ctas : 0);
+  RateSample* ip_rs = nullptr;  // an in-place push's kernel time is its transfer time
+  if (adaptive_ip) {
+    ip_rs = next_sample(c);
+    if (!ip_rs) return fail(c, SVX_ERR_CUDA, "event creation failed");
+    SVX_CUDA(c, cudaEventRecord(ip_rs->e0, c->cs));
+  }
+  svx_status st = launch_parts(c, desc, zero_copy ? c->cfg.zero_copy_ctas : (n_host > 0 ? c->cfg.staged_ctas : 0));
   if (st != SVX_OK) return st;
+  if (ip_rs) {
+    SVX_CUDA(c, cudaEventRecord(ip_rs->e1, c->cs));
+    commit_sample(c, ip_rs, host_bytes, true);
+  }
   if (pe) {
     SVX_CUDA(c, cudaEventRecord(pe->k1, c->cs));
     ++c->n_push;
@@ -682,6 +921,7 @@ svx_status svx_round_finish(svx_ctx c, void* o_dev, float* lse_dev, int32_t time
   std::string why;
   if (!coverage_impl(c->n_req, c->hist_len.data(), c->parts_seen, &why)) {
     c->state = RoundState::kIdle;  // the round is abandoned; its enqueued work is harmless
+    if (c->cfg.flags & SVX_FLAG_TIMING) c->n_push = c->round_push0;  // and it leaves the timing window
     return fail(c, SVX_ERR_INVALID_ARG, "chunk coverage check failed: %s", why.c_str());
   }
   FinishParams p;
@@ -708,9 +948,10 @@ svx_status svx_round_finish(svx_ctx c, void* o_dev, float* lse_dev, int32_t time
   for (int b = 0; b < c->n_req; ++b) p.slot_mask[b] = c->slot_mask[static_cast<size_t>(b)];
   const bool timing = (c->cfg.flags & SVX_FLAG_TIMING) != 0;
   c->state = RoundState::kIdle;
-  if (timing) SVX_CUDA(c, cudaEventRecord(c->ev_f0, c->cs));
+  const RoundEvents* re = timing ? &c->ev_round[static_cast<size_t>(c->n_round)] : nullptr;
+  if (re) SVX_CUDA(c, cudaEventRecord(re->f0, c->cs));
   SVX_CUDA(c, svx::launch_finish(p, c->cfg.head_dim, c->cs));
-  if (timing) SVX_CUDA(c, cudaEventRecord(c->ev_f1, c->cs));
+  if (re) SVX_CUDA(c, cudaEventRecord(re->f1, c->cs));
   SVX_CUDA(c, cudaEventRecord(c->done, c->cs));
   if (timing) {
     c->last_stats_pending = true;
@@ -719,6 +960,15 @@ svx_status svx_round_finish(svx_ctx c, void* o_dev, float* lse_dev, int32_t time
     c->last_stats.device_bytes = c->dev_bytes;
     c->last_stats.n_chunk_launches = c->n_launch;
     c->last_stats.n_copies = c->n_copies;
+    c->last_round = c->n_round;
+    c->last_push0 = c->round_push0;
+    c->last_push1 = c->n_push;
+    ++c->n_round;
+    ++c->win_rounds_done;
+    c->win_h2d += c->h2d_bytes;
+    c->win_dev += c->dev_bytes;
+    c->win_launch += c->n_launch;
+    c->win_copies += c->n_copies;
   }
   if (timeout_ms > 0) {
     const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms);
@@ -742,6 +992,87 @@ svx_status svx_round_finish(svx_ctx c, void* o_dev, float* lse_dev, int32_t time
   return SVX_OK;
 }
 
+namespace {
+
+// Event intervals of one push, in ms from `origin` (negative for events before it: a copy stream can run
+// ahead of the compute stream's round-begin event); the copy interval is {NaN, NaN} without copies.
+svx_status push_intervals(svx_ctx c, cudaEvent_t origin, const PushEvents& pe, double iv[4]) {
+  float a = 0.f;
+  iv[0] = iv[1] = std::nan("");
+  if (pe.has_copy) {
+    SVX_CUDA(c, cudaEventElapsedTime(&a, origin, pe.copy0));
+    iv[0] = a;
+    SVX_CUDA(c, cudaEventElapsedTime(&a, origin, pe.copy1));
+    iv[1] = a;
+  }
+  SVX_CUDA(c, cudaEventElapsedTime(&a, origin, pe.k0));
+  iv[2] = a;
+  SVX_CUDA(c, cudaEventElapsedTime(&a, origin, pe.k1));
+  iv[3] = a;
+  return SVX_OK;
+}
+
+// Overlap over pushes [p0, p1), in ms.  Transfer intervals are the staged pushes' copy intervals and
+// the chunk kernels of pushes that read host memory in place (those kernels are the transfer).
+struct Overlap {
+  double copy_busy = 0.0;      // sum of copy intervals
+  double transfer_busy = 0.0;  // length of the union of transfer intervals
+  double kernel = 0.0;         // sum of chunk-kernel intervals
+  double zc_kernel = 0.0;      // sum of the in-place pushes' chunk-kernel intervals
+  double exposed = 0.0;        // kernel time of the other pushes outside every transfer interval
+  double gaps = 0.0;           // copy-stream idle time between its first copy and its last
+  int n_zc = 0;
+};
+
+svx_status overlap_of(svx_ctx c, cudaEvent_t origin, int p0, int p1, Overlap* o) {
+  std::vector<std::pair<double, double>> cp, tr, kr;
+  *o = Overlap{};
+  for (int i = p0; i < p1; ++i) {
+    const PushEvents& pe = c->ev_push[static_cast<size_t>(i)];
+    double iv[4];
+    svx_status st = push_intervals(c, origin, pe, iv);
+    if (st != SVX_OK) return st;
+    if (pe.has_copy) {
+      cp.push_back({iv[0], iv[1]});
+      tr.push_back({iv[0], iv[1]});
+    }
+    o->kernel += iv[3] - iv[2];
+    if (pe.zero_copy) {
+      tr.push_back({iv[2], iv[3]});
+      o->zc_kernel += iv[3] - iv[2];
+      ++o->n_zc;
+    } else {
+      kr.push_back({iv[2], iv[3]});
+    }
+  }
+  std::sort(cp.begin(), cp.end());
+  for (size_t i = 0; i < cp.size(); ++i) {
+    o->copy_busy += cp[i].second - cp[i].first;
+    if (i > 0) o->gaps += std::max(0.0, cp[i].first - cp[i - 1].second);
+  }
+  // union of the transfer intervals: sorted, merged, disjoint
+  std::sort(tr.begin(), tr.end());
+  std::vector<std::pair<double, double>> un;
+  for (const auto& x : tr) {
+    if (!un.empty() && x.first <= un.back().second) un.back().second = std::max(un.back().second, x.second);
+    else un.push_back(x);
+  }
+  for (const auto& x : un) o->transfer_busy += x.second - x.first;
+  for (const auto& k : kr) {
+    double covered = 0.0;
+    auto it = std::lower_bound(un.begin(), un.end(), std::make_pair(k.first, -1e300),
+                               [](const std::pair<double, double>& x, const std::pair<double, double>& y) {
+                                 return x.second < y.first;
+                               });
+    for (; it != un.end() && it->first < k.second; ++it)
+      covered += std::max(0.0, std::min(k.second, it->second) - std::max(k.first, it->first));
+    o->exposed += std::max(0.0, (k.second - k.first) - covered);
+  }
+  return SVX_OK;
+}
+
+}  // namespace
+
 svx_status svx_round_stats(svx_ctx c, svx_stats* out) {
   if (!c || !out) return SVX_ERR_INVALID_ARG;
   if (!(c->cfg.flags & SVX_FLAG_TIMING)) return fail(c, SVX_ERR_BAD_STATE, "context created without SVX_FLAG_TIMING");
@@ -749,43 +1080,90 @@ svx_status svx_round_stats(svx_ctx c, svx_stats* out) {
   DeviceGuard dg(c->cfg.device);
   SVX_CUDA(c, cudaEventSynchronize(c->done));
   svx_stats s = c->last_stats;
+  const RoundEvents& re = c->ev_round[static_cast<size_t>(c->last_round)];
   float ms = 0.f;
-  SVX_CUDA(c, cudaEventElapsedTime(&ms, c->ev_begin, c->ev_f1));
+  SVX_CUDA(c, cudaEventElapsedTime(&ms, re.begin, re.f1));
   s.round_ms = ms;
-  for (int i = 0; i < c->n_push; ++i) {
-    const PushEvents& pe = c->ev_push[static_cast<size_t>(i)];
-    if (pe.has_copy) {
-      SVX_CUDA(c, cudaEventElapsedTime(&ms, pe.copy0, pe.copy1));
-      s.copy_busy_ms += ms;
-    }
-    SVX_CUDA(c, cudaEventElapsedTime(&ms, pe.k0, pe.k1));
-    s.chunk_kernel_ms += ms;
-  }
-  SVX_CUDA(c, cudaEventElapsedTime(&ms, c->ev_f0, c->ev_f1));
+  SVX_CUDA(c, cudaEventElapsedTime(&ms, re.f0, re.f1));
   s.finish_kernel_ms = ms;
-  // chunk-kernel time not covered by any copy interval of the round (exposed compute)
-  std::vector<std::pair<double, double>> cp, kr;
-  for (int i = 0; i < c->n_push; ++i) {
-    const PushEvents& pe = c->ev_push[static_cast<size_t>(i)];
-    float a = 0.f, b = 0.f;
-    if (pe.has_copy) {
-      SVX_CUDA(c, cudaEventElapsedTime(&a, c->ev_begin, pe.copy0));
-      SVX_CUDA(c, cudaEventElapsedTime(&b, c->ev_begin, pe.copy1));
-      cp.push_back({a, b});
-    }
-    SVX_CUDA(c, cudaEventElapsedTime(&a, c->ev_begin, pe.k0));
-    SVX_CUDA(c, cudaEventElapsedTime(&b, c->ev_begin, pe.k1));
-    kr.push_back({a, b});
-  }
-  std::sort(cp.begin(), cp.end());
-  double exposed = 0.0;
-  for (const auto& k : kr) {
-    double covered = 0.0;
-    for (const auto& x : cp) covered += std::max(0.0, std::min(k.second, x.second) - std::max(k.first, x.first));
-    exposed += std::max(0.0, (k.second - k.first) - covered);
-  }
-  s.chunk_kernel_exposed_ms = exposed;
+  Overlap ov;
+  svx_status st = overlap_of(c, re.begin, c->last_push0, c->last_push1, &ov);
+  if (st != SVX_OK) return st;
+  s.copy_busy_ms = ov.copy_busy;
+  s.chunk_kernel_ms = ov.kernel;
+  s.chunk_kernel_exposed_ms = ov.exposed;
+  s.transfer_busy_ms = ov.transfer_busy;
+  s.n_zero_copy_pushes = ov.n_zc;
   *out = s;
+  return SVX_OK;
+}
+
+svx_status svx_window_reset(svx_ctx c) {
+  if (!c) return SVX_ERR_INVALID_ARG;
+  if (!(c->cfg.flags & SVX_FLAG_TIMING)) return fail(c, SVX_ERR_BAD_STATE, "context created without SVX_FLAG_TIMING");
+  if (c->state == RoundState::kOpen) return fail(c, SVX_ERR_BAD_STATE, "svx_window_reset: a round is open");
+  c->window_restart = true;
+  return SVX_OK;
+}
+
+svx_status svx_window_stats(svx_ctx c, svx_window_summary* out) {
+  if (!c || !out) return SVX_ERR_INVALID_ARG;
+  if (!(c->cfg.flags & SVX_FLAG_TIMING)) return fail(c, SVX_ERR_BAD_STATE, "context created without SVX_FLAG_TIMING");
+  if (c->window_restart || c->win_rounds_done == 0)
+    return fail(c, SVX_ERR_BAD_STATE, "no finished round in the timing window");
+  DeviceGuard dg(c->cfg.device);
+  SVX_CUDA(c, cudaEventSynchronize(c->done));
+  svx_window_summary w{};
+  const RoundEvents& r0 = c->ev_round[0];
+  const RoundEvents& r1 = c->ev_round[static_cast<size_t>(c->last_round)];
+  float ms = 0.f;
+  SVX_CUDA(c, cudaEventElapsedTime(&ms, r0.begin, r1.f1));
+  w.window_ms = ms;
+  // the copy stream may have started the window's first copies before the compute stream reached the
+  // first round's begin event: the window then starts at the first copy
+  for (int i = 0; i < c->last_push1; ++i)
+    if (c->ev_push[static_cast<size_t>(i)].has_copy) {
+      SVX_CUDA(c, cudaEventElapsedTime(&ms, r0.begin, c->ev_push[static_cast<size_t>(i)].copy0));
+      if (ms < 0.f) w.window_ms -= ms;
+      break;
+    }
+  for (int r = 0; r <= c->last_round; ++r) {
+    SVX_CUDA(c, cudaEventElapsedTime(&ms, c->ev_round[static_cast<size_t>(r)].f0, c->ev_round[static_cast<size_t>(r)].f1));
+    w.finish_kernel_ms += ms;
+  }
+  Overlap ov;
+  svx_status st = overlap_of(c, r0.begin, 0, c->last_push1, &ov);
+  if (st != SVX_OK) return st;
+  w.copy_busy_ms = ov.copy_busy;
+  w.copy_gap_ms = ov.gaps;
+  w.chunk_kernel_ms = ov.kernel;
+  w.chunk_kernel_exposed_ms = ov.exposed;
+  w.transfer_busy_ms = ov.transfer_busy;
+  w.zero_copy_kernel_ms = ov.zc_kernel;
+  w.n_zero_copy_pushes = ov.n_zc;
+  w.h2d_bytes = c->win_h2d;
+  w.device_bytes = c->win_dev;
+  w.n_rounds = c->win_rounds_done;
+  w.n_pushes = c->last_push1;
+  w.n_chunk_launches = c->win_launch;
+  w.n_copies = c->win_copies;
+  *out = w;
+  return SVX_OK;
+}
+
+svx_status svx_window_intervals(svx_ctx c, double* out, int64_t cap, int64_t* n_out) {
+  if (!c || !n_out || cap < 0 || (cap > 0 && !out)) return SVX_ERR_INVALID_ARG;
+  if (!(c->cfg.flags & SVX_FLAG_TIMING)) return fail(c, SVX_ERR_BAD_STATE, "context created without SVX_FLAG_TIMING");
+  if (c->window_restart || c->win_rounds_done == 0)
+    return fail(c, SVX_ERR_BAD_STATE, "no finished round in the timing window");
+  DeviceGuard dg(c->cfg.device);
+  SVX_CUDA(c, cudaEventSynchronize(c->done));
+  const int n = c->last_push1;
+  for (int i = 0; i < n && i < cap; ++i) {
+    svx_status st = push_intervals(c, c->ev_round[0].begin, c->ev_push[static_cast<size_t>(i)], out + 4 * i);
+    if (st != SVX_OK) return st;
+  }
+  *n_out = n;
   return SVX_OK;
 }
 
@@ -836,6 +1214,28 @@ svx_status svx_debug_expire_wait(svx_ctx c, int32_t wait_ms) {
   if (c->state == RoundState::kOpen) return fail(c, SVX_ERR_BAD_STATE, "svx_debug_expire_wait: a round is open");
   DeviceGuard dg(c->cfg.device);
   SVX_CUDA(c, svx::launch_expire_wait(c->d_err, static_cast<uint64_t>(wait_ms) * 1000000ull, c->cs));
+  return SVX_OK;
+}
+
+svx_status svx_adaptive_state(svx_ctx c, double* ce_ms_per_gb, double* ip_ms_per_gb, int32_t* prefer_in_place) {
+  if (!c || !ce_ms_per_gb || !ip_ms_per_gb || !prefer_in_place) return SVX_ERR_INVALID_ARG;
+  if (!(c->cfg.flags & SVX_FLAG_ADAPTIVE)) return fail(c, SVX_ERR_BAD_STATE, "context created without SVX_FLAG_ADAPTIVE");
+  *ce_ms_per_gb = c->ce_ms_per_gb;
+  *ip_ms_per_gb = c->ip_ms_per_gb;
+  *prefer_in_place = c->prefer_ip ? 1 : 0;
+  return SVX_OK;
+}
+
+svx_status svx_debug_fail_copy(svx_ctx c, int64_t nth) {
+  if (!c || nth < 0) return SVX_ERR_INVALID_ARG;
+  c->fail_at = nth > 0 ? c->copy_seq + nth : 0;
+  return SVX_OK;
+}
+
+svx_status svx_debug_delay_copy(svx_ctx c, int64_t nth, int32_t delay_ms) {
+  if (!c || nth < 0 || delay_ms < 0 || delay_ms > 10000) return SVX_ERR_INVALID_ARG;
+  c->delay_at = nth > 0 ? c->copy_seq + nth : 0;
+  c->delay_ms = delay_ms;
   return SVX_OK;
 }
 

@@ -21,6 +21,7 @@ STATUS_NAMES = {0: "SVX_OK", 1: "SVX_ERR_INVALID_ARG", 2: "SVX_ERR_BAD_STATE", 3
 FLAG_TIMING = 1
 FLAG_NO_TENSOR_CORES = 2
 FLAG_ZERO_COPY = 4
+FLAG_ADAPTIVE = 8
 
 
 class SvxError(RuntimeError):
@@ -34,7 +35,8 @@ class Config(ctypes.Structure):
     _fields_ = [("max_req", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("max_query", ctypes.c_int32), ("max_chunk_tokens", ctypes.c_int32),
                 ("n_slots", ctypes.c_int32), ("device", ctypes.c_int32), ("compute_stream", ctypes.c_void_p),
-                ("copy_stream", ctypes.c_void_p), ("flags", ctypes.c_uint32), ("zero_copy_ctas", ctypes.c_int32)]
+                ("copy_stream", ctypes.c_void_p), ("flags", ctypes.c_uint32), ("zero_copy_ctas", ctypes.c_int32),
+                ("staged_ctas", ctypes.c_int32)]
 
 
 class Part(ctypes.Structure):
@@ -47,7 +49,17 @@ class Stats(ctypes.Structure):
                 ("chunk_kernel_ms", ctypes.c_double), ("cand_kernel_ms", ctypes.c_double),
                 ("finish_kernel_ms", ctypes.c_double), ("h2d_bytes", ctypes.c_int64),
                 ("device_bytes", ctypes.c_int64), ("n_chunk_launches", ctypes.c_int32),
-                ("n_copies", ctypes.c_int32), ("chunk_kernel_exposed_ms", ctypes.c_double)]
+                ("n_copies", ctypes.c_int32), ("chunk_kernel_exposed_ms", ctypes.c_double),
+                ("transfer_busy_ms", ctypes.c_double), ("n_zero_copy_pushes", ctypes.c_int32)]
+
+
+class WindowStats(ctypes.Structure):
+    _fields_ = [("window_ms", ctypes.c_double), ("copy_busy_ms", ctypes.c_double), ("copy_gap_ms", ctypes.c_double),
+                ("chunk_kernel_ms", ctypes.c_double), ("chunk_kernel_exposed_ms", ctypes.c_double),
+                ("finish_kernel_ms", ctypes.c_double), ("transfer_busy_ms", ctypes.c_double),
+                ("zero_copy_kernel_ms", ctypes.c_double), ("n_zero_copy_pushes", ctypes.c_int32), ("pad", ctypes.c_int32),
+                ("h2d_bytes", ctypes.c_int64), ("device_bytes", ctypes.c_int64), ("n_rounds", ctypes.c_int32), ("n_pushes", ctypes.c_int32), ("n_chunk_launches", ctypes.c_int32),
+                ("n_copies", ctypes.c_int32)]
 
 
 class TierState(ctypes.Structure):
@@ -82,6 +94,12 @@ _SIGS = {
     "svx_round_finish": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32]),
     "svx_last_error": (ctypes.c_char_p, [_P]),
     "svx_round_stats": (ctypes.c_int, [_P, ctypes.POINTER(Stats)]),
+    "svx_adaptive_state": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                          ctypes.POINTER(ctypes.c_int32)]),
+    "svx_window_reset": (ctypes.c_int, [_P]),
+    "svx_window_stats": (ctypes.c_int, [_P, ctypes.POINTER(WindowStats)]),
+    "svx_window_intervals": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_double), ctypes.c_int64,
+                                            ctypes.POINTER(ctypes.c_int64)]),
     "svx_plan_chunks": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), ctypes.c_int32,
                                        ctypes.c_int32, ctypes.POINTER(PlanEntry), ctypes.c_int64,
                                        ctypes.POINTER(ctypes.c_int64)]),
@@ -91,6 +109,8 @@ _SIGS = {
                                           ctypes.POINTER(ctypes.c_int64), ctypes.c_int64,
                                           ctypes.POINTER(ctypes.c_int32)]),
     "svx_debug_expire_wait": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    "svx_debug_fail_copy": (ctypes.c_int, [_P, ctypes.c_int64]),
+    "svx_debug_delay_copy": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int32]),
     "svx_plan_tc": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
                                    ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32),
                                    ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64),
@@ -132,6 +152,7 @@ _SIGS = {
     "svx_width_next": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "svx_width_cost": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(ctypes.c_double)]),
     "svx_version": (ctypes.c_char_p, []),
+    "svx_abi_sizes": (ctypes.c_int32, [ctypes.POINTER(ctypes.c_int64), ctypes.c_int32]),
 }
 
 
@@ -152,6 +173,16 @@ SYMBOLS = tuple(_SIGS)
 
 def version() -> str:
     return lib.svx_version().decode()
+
+
+ABI_STRUCTS = ("Config", "Part", "Stats", "WindowStats", "PlanEntry", "TierState", "SchedConfig", "DraftInstr")
+
+
+def abi_sizes() -> dict:
+    """sizeof of each C ABI struct as the library was compiled, keyed by the binding's class name."""
+    out = (ctypes.c_int64 * len(ABI_STRUCTS))()
+    n = lib.svx_abi_sizes(out, len(ABI_STRUCTS))
+    return dict(zip(ABI_STRUCTS, list(out[:min(n, len(ABI_STRUCTS))])))
 
 
 def _i64(seq) -> ctypes.Array:
@@ -397,8 +428,12 @@ def verify_static(q, hist_len: Sequence[int], hist_k: Sequence, hist_v: Sequence
     C_b = 0); cand_k, cand_v: device bf16 [B][nq][Hkv][d] or None; o, lse: device outputs.
     """
     B, Hq, nq, d = (int(x) for x in q.shape)
+    if len(hist_len) != B or len(hist_k) != B or len(hist_v) != B:
+        raise SvxError(ERR_INVALID_ARG, f"hist_len, hist_k and hist_v need one entry per request ({B})")
     if n_kv_heads is None:
         src = next((k for k in hist_k if k is not None), cand_k)
+        if src is None:
+            raise SvxError(ERR_INVALID_ARG, "n_kv_heads is required when no history or candidate tensor is given")
         n_kv_heads = int(src.shape[-2])
     h, hp = _i64(hist_len)
     qp = _tensor_ptr(q, "bf16", (Hq, nq, d), B, "q")
@@ -410,8 +445,11 @@ def verify_static(q, hist_len: Sequence[int], hist_k: Sequence, hist_v: Sequence
     ckp = None if cand_k is None else _tensor_ptr(cand_k, "bf16", (nq,) + kv, B, "candidate k")
     cvp = None if cand_v is None else _tensor_ptr(cand_v, "bf16", (nq,) + kv, B, "candidate v")
     par = None
-    if parent is not None:
-        parent = np.ascontiguousarray(np.asarray(parent, dtype=np.int32))
+    if parent is not None:  # the C call reads n_req * n_query parents
+        parent = np.asarray(parent, dtype=np.int32)
+        if parent.size != B * nq:
+            raise SvxError(ERR_INVALID_ARG, f"parent: {parent.size} entries, expected [{B}, {nq}]")
+        parent = np.ascontiguousarray(parent.reshape(B, nq))
         par = parent.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
     op = _tensor_ptr(o, "bf16", (Hq, nq, d), B, "o")
     lp = _tensor_ptr(lse, "f32", (Hq, nq), B, "lse")
@@ -474,12 +512,12 @@ class Verifier:
     def __init__(self, max_req: int, n_q_heads: int, n_kv_heads: int, head_dim: int, max_query: int,
                  max_chunk_tokens: int, n_slots: int = 2, device: int = 0, compute_stream=None, copy_stream=None,
                  timing: bool = False, tensor_cores: bool = True, zero_copy: bool = False,
-                 zero_copy_ctas: int = 0):
+                 zero_copy_ctas: int = 0, staged_ctas: int = 0, adaptive: bool = False):
         self._keep = (compute_stream, copy_stream)
         flags = ((FLAG_TIMING if timing else 0) | (0 if tensor_cores else FLAG_NO_TENSOR_CORES)
-                 | (FLAG_ZERO_COPY if zero_copy else 0))
+                 | (FLAG_ZERO_COPY if zero_copy else 0) | (FLAG_ADAPTIVE if adaptive else 0))
         cfg = Config(max_req, n_q_heads, n_kv_heads, head_dim, max_query, max_chunk_tokens, n_slots, device,
-                     _stream_handle(compute_stream), _stream_handle(copy_stream), flags, zero_copy_ctas)
+                     _stream_handle(compute_stream), _stream_handle(copy_stream), flags, zero_copy_ctas, staged_ctas)
         h = ctypes.c_void_p(None)
         st = lib.svx_create(ctypes.byref(cfg), ctypes.byref(h))
         if st != OK:
@@ -563,10 +601,44 @@ class Verifier:
         """Test hook: a kernel whose bounded wait runs out raises the device error word."""
         self._check(lib.svx_debug_expire_wait(self._h, wait_ms))
 
+    def debug_fail_copy(self, nth: int):
+        """Test hook: the nth copy submission from now is refused (0 disarms)."""
+        self._check(lib.svx_debug_fail_copy(self._h, nth))
+
+    def debug_delay_copy(self, nth: int, delay_ms: int):
+        """Test hook: the host sleeps delay_ms before the nth copy submission from now (0 disarms)."""
+        self._check(lib.svx_debug_delay_copy(self._h, nth, delay_ms))
+
     def stats(self) -> dict:
         s = Stats()
         self._check(lib.svx_round_stats(self._h, ctypes.byref(s)))
         return {f: getattr(s, f) for f, _ in Stats._fields_}
+
+    def adaptive_state(self) -> dict:
+        """The adaptive policy's figures: ms per GB of each engine (None before measured), preference."""
+        a, b, p = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_int32(0)
+        self._check(lib.svx_adaptive_state(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(p)))
+        return {"copy_engine_ms_per_gb": None if a.value < 0 else a.value,
+                "in_place_ms_per_gb": None if b.value < 0 else b.value, "prefer_in_place": bool(p.value)}
+
+    def window_reset(self):
+        """Opens a new timing window at the next round."""
+        self._check(lib.svx_window_reset(self._h))
+
+    def window_stats(self) -> dict:
+        s = WindowStats()
+        self._check(lib.svx_window_stats(self._h, ctypes.byref(s)))
+        return {f: getattr(s, f) for f, _ in WindowStats._fields_}
+
+    def window_intervals(self) -> np.ndarray:
+        """[n_pushes][4] float64: copy start, copy end (NaN without copies), kernel start, end (ms from the
+        window's first round begin)."""
+        n = ctypes.c_int64(0)
+        self._check(lib.svx_window_intervals(self._h, None, 0, ctypes.byref(n)))
+        out = np.zeros((max(1, n.value), 4), dtype=np.float64)
+        self._check(lib.svx_window_intervals(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), n.value,
+                                             ctypes.byref(n)))
+        return out[:n.value]
 
     def run_round(self, q, hist_len: Sequence[int], hist_k: Sequence, hist_v: Sequence, chunk_tokens: int,
                   o, lse, cand_k=None, cand_v=None, parent: Optional[np.ndarray] = None,

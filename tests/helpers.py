@@ -105,3 +105,34 @@ def sample_rows(w, n, seed=0):
             for _ in range(n)}
     rows |= {(w.n_req - 1, w.n_q_heads - 1, w.n_query - 1), (0, 0, 0)}
     return sorted(rows)
+
+
+def oracle_pair(args):
+    """Oracle rows of one (request, KV head) pair: all G * nq query rows of that KV head.  A top-level
+    function, so that a spawn process pool can run pairs in parallel."""
+    import oracle
+    q, kh, vh, kc, vc, vis, scale = args
+    f = W.bf16_to_f64
+    return oracle.verify_attention(f(q), [f(kh)], [f(vh)], f(kc), f(vc), vis, scale=scale)
+
+
+def oracle_all_rows_parallel(w, x, processes=None):
+    """Every row of one layer from the oracle, one (request, KV head) pair per task on a spawn pool (a
+    forked pool could inherit a CUDA context).  Returns O [B][Hq][nq][d] and LSE [B][Hq][nq]."""
+    import multiprocessing as mp
+    import os
+    vis = O.visibility_table(w.n_req, w.n_query, x.parent)
+    G = w.group
+    tasks, keys = [], []
+    for b in range(w.n_req):
+        for g in range(w.n_kv_heads):
+            tasks.append((x.q[b:b + 1, g * G:(g + 1) * G], x.k_hist[b][:, g:g + 1], x.v_hist[b][:, g:g + 1],
+                          x.k_cand[b:b + 1, :, g:g + 1], x.v_cand[b:b + 1, :, g:g + 1], vis[b:b + 1], w.scale))
+            keys.append((b, g))
+    o_ref = np.full((w.n_req, w.n_q_heads, w.n_query, w.head_dim), np.nan)
+    l_ref = np.full((w.n_req, w.n_q_heads, w.n_query), np.nan)
+    with mp.get_context("spawn").Pool(processes or os.cpu_count() or 1) as pool:
+        for (b, g), (o, lse) in zip(keys, pool.imap(oracle_pair, tasks)):
+            o_ref[b, g * G:(g + 1) * G] = o[0]
+            l_ref[b, g * G:(g + 1) * G] = lse[0]
+    return o_ref, l_ref

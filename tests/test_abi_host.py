@@ -266,3 +266,12 @@ def test_manual_completion_is_refused_while_a_library_copy_is_in_flight(svx):
     s.event = None
     assert svx.lib.svx_tier_complete(ctypes.byref(s)) == svx.OK
     assert s.H == 64 and s.pending == -1
+
+
+def test_binding_structs_match_the_compiled_layouts(svx):
+    """Every struct the binding passes by pointer has the size the library was compiled with."""
+    import ctypes
+    sizes = svx.abi_sizes()
+    assert set(sizes) == set(svx.ABI_STRUCTS)
+    for name, size in sizes.items():
+        assert ctypes.sizeof(getattr(svx, name)) == size, name

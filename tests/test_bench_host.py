@@ -15,7 +15,7 @@ def test_head_dim_option_changes_only_the_head_dimension():
     w = bench.workload_of(a)
     assert w.head_dim == 64
     assert w == base.with_(head_dim=64)
-    assert bench.workload_of(bench.parse_args([])) == base
+    assert bench.workload_of(bench.parse_args([])) == W.named("fulldepth")  # the default headline workload
     cfg = bench.workload_config(w, a)
     assert "d=64" in cfg["workload"] and cfg["head_dim"] == 64
 
@@ -30,3 +30,18 @@ def test_l2_statement_follows_the_bytes_one_round_reads():
     assert "128 KiB" in l2 and "stays in" in l2
     a = bench.parse_args(["--workload", "qwen3", "--head-dim", "64"])
     assert "512 MiB" in bench.workload_config(bench.workload_of(a), a)["l2"]
+
+
+def test_layers_option_keeps_every_launch_shape():
+    w = bench.workload_of(bench.parse_args(["--layers", "2"]))
+    assert w == W.named("fulldepth").with_(n_layers=2)
+    cfg = bench.workload_config(w, bench.parse_args([]))
+    assert cfg["n_layers"] == 2 and "2 layers x 2 requests" in cfg["workload"]
+
+
+def test_copy_rates_skip_pushes_without_copies():
+    import numpy as np
+    iv = np.array([[0.0, 1.0, 1.0, 1.1], [np.nan, np.nan, 1.1, 1.5], [1.0, 3.0, 3.0, 3.1]])
+    r = bench.copy_rates(iv, [200e6, 200e6, 200e6])
+    assert r["pushes"] == 2 and abs(r["max"] - 200.0) < 1e-9 and abs(r["min"] - 100.0) < 1e-9
+    assert r["below_150_frac"] == 0.5
