@@ -348,6 +348,129 @@ class DraftLoad:
         return self.count * self.flops / dt / 1e12
 
 
+class AdmittedDraft:
+    """Draft steps admitted by the library's Target-priority scheduler (section 4.3, "Target-priority
+    scheduling" and the two paragraphs after it), in place of a free-running Draft.
+
+    The Draft stand-in runs one bf16 4096^3 GEMM (cuBLAS) per Draft step on a lowest-priority stream,
+    from a host thread.  For each request it asks svx_sched_try_admit with the time left in the
+    Target's current round (the round began at t0 and is predicted to take S ms); an admitted
+    instruction is checked again with svx_sched_check_start right before the launch (the Draft side of
+    the protocol: same request and round, t_latest not passed) and acknowledged from the step's
+    completion event with its measured time.  The Target side calls begin_round before each
+    verification round and end_round with the round's measured time, which feeds
+    svx_sched_observe_target (an observed increase over eps_T pauses new submissions)."""
+
+    def __init__(self, dev, n_req, eps_target=0.05, delta_ms=0.5, ema=0.3, t_draft_ms=0.1, n=4096):
+        import threading
+        import torch
+        from speculative_decoding_verification_chunked_gb300 import svx
+        self.torch, self.dev, self.n_req = torch, dev, n_req
+        lo, _hi = torch.cuda.Stream.priority_range()
+        self.stream = torch.cuda.Stream(device=dev, priority=lo)
+        self.a = torch.randn((n, n), device=dev, dtype=torch.bfloat16)
+        self.b = torch.randn((n, n), device=dev, dtype=torch.bfloat16)
+        self.c = torch.empty((n, n), device=dev, dtype=torch.bfloat16)
+        with torch.cuda.stream(self.stream):
+            torch.matmul(self.a, self.b, out=self.c)
+        torch.cuda.synchronize(dev)
+        self.flops = 2.0 * n ** 3
+        self.eps = eps_target
+        self.sched = svx.Scheduler(eps_target, delta_ms, ema, t_draft_ms, 0.0, alloc=0)
+        self.lock = threading.Lock()
+        self.round, self.t0, self.S = -1, 0.0, 0.0
+        self.log = []  # (host time at launch, t_latest) of every executed step
+        self.rejected = self.admitted = self.paused_rounds = 0
+        self.stop_flag = False
+
+    @staticmethod
+    def now_ms():
+        return time.perf_counter() * 1e3
+
+    def begin_round(self, r, predicted_ms):
+        with self.lock:
+            self.sched.new_round()
+            if self.sched.estimates()[2]:
+                self.paused_rounds += 1
+            self.round, self.t0, self.S = r, self.now_ms(), predicted_ms
+
+    def end_round(self, t_co_ms, t_alone_ms):
+        with self.lock:
+            self.sched.observe_target(t_co_ms, t_alone_ms)
+
+    def _run(self):
+        torch = self.torch
+        torch.cuda.set_device(self.dev)
+        while not self.stop_flag:
+            launched = False
+            for req in range(self.n_req):
+                with self.lock:
+                    now = self.now_ms()
+                    ins = self.sched.try_admit(req, self.round, now, self.t0 + self.S - now)
+                if ins is None:
+                    continue
+                self.admitted += 1
+                with self.lock:  # the Draft side's check right before it starts the step
+                    now = self.now_ms()
+                    ok = self.sched.check_start(ins, req, self.round, now)
+                if not ok:
+                    self.rejected += 1
+                    continue
+                self.log.append((now, ins.t_latest))
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(self.stream):
+                    e0.record(self.stream)
+                    torch.matmul(self.a, self.b, out=self.c)
+                    e1.record(self.stream)
+                e1.synchronize()
+                with self.lock:
+                    self.sched.ack(req, ins.seq, e0.elapsed_time(e1))
+                launched = True
+            if not launched:
+                time.sleep(0.0002)
+
+    def start(self):
+        import threading
+        self.stop_flag = False
+        self.log.clear()
+        self.rejected = self.admitted = self.paused_rounds = 0
+        self.t_start = time.perf_counter()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self) -> float:
+        """Stops the Draft thread; returns the Draft's TFLOP/s since start()."""
+        self.stop_flag = True
+        self.thread.join()
+        return len(self.log) * self.flops / (time.perf_counter() - self.t_start) / 1e12
+
+
+def run_admitted(R, step_fn, steps, ms_alone, draft):
+    """Target steps with Draft steps admitted by the scheduler: each step is one verification round,
+    timed with CUDA events on the compute stream and reported to the scheduler.  Returns the mean step
+    time and the admission figures."""
+    torch = R.torch
+    draft.start()
+    times = []
+    for r in range(steps):
+        draft.begin_round(r, ms_alone)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(R.cs)
+        step_fn()
+        e1.record(R.cs)
+        e1.synchronize()
+        t = e0.elapsed_time(e1)
+        times.append(t)
+        draft.end_round(t, ms_alone)
+    tf = draft.stop()
+    late = sum(1 for t_launch, t_latest in draft.log if t_launch > t_latest)
+    ms = statistics.mean(times)
+    return ms, {"delta_T": (ms - ms_alone) / ms_alone, "target_ms_alone": ms_alone, "target_ms_co": ms,
+                "draft_tflops_co": tf, "eps_T": draft.eps, "draft_steps": len(draft.log),
+                "instructions": draft.admitted, "expired_or_stale": draft.rejected,
+                "started_after_t_latest": late, "paused_rounds": draft.paused_rounds}
+
+
 class Inputs:
     """One workload's inputs on the device and in pinned host memory, per layer.
 
@@ -488,6 +611,34 @@ def copy_rates(iv, push_bytes):
             "below_150_frac": float((r < 150).mean()), "pushes": int(ok.sum())}
 
 
+def step_overlap(iv, rounds, pushes_per_step: int, layers: int):
+    """Per step of a timing window: (T_step, T_transfer) in ms.  T_step runs from the step's first round
+    begin to its last finish-kernel end; T_transfer is the length of the union, inside the step, of its
+    pushes' copy intervals and of the chunk kernels of pushes read in place (no copy interval)."""
+    n_steps = min(len(rounds) // layers, len(iv) // pushes_per_step)
+    out = []
+    for s in range(n_steps):
+        t0, t1 = rounds[s * layers, 0], rounds[(s + 1) * layers - 1, 2]
+        seg = iv[s * pushes_per_step:(s + 1) * pushes_per_step]
+        tr = [(a, b) if np.isfinite(a) else (k0, k1) for a, b, k0, k1 in seg]
+        tr.sort()
+        busy, cur = 0.0, None
+        for a, b in tr:
+            a, b = max(a, t0), min(b, t1)
+            if b <= a:
+                continue
+            if cur is None or a > cur[1]:
+                if cur is not None:
+                    busy += cur[1] - cur[0]
+                cur = [a, b]
+            else:
+                cur[1] = max(cur[1], b)
+        if cur is not None:
+            busy += cur[1] - cur[0]
+        out.append((t1 - t0, busy))
+    return out
+
+
 def link_probe(inp, dev, xs):
     """Pinned host -> HBM bandwidth now (one 256 MiB copy of layer 0's first K rows, best of 4)."""
     import torch
@@ -588,6 +739,7 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
                      between=v.window_reset)
         ws = v.window_stats()
         iv = v.window_intervals()
+        so = step_overlap(iv, v.window_rounds(), len(stream_pushes[0]) * L, L)
         val, ms_job = job_throughput(B * nq, ms, world, dev)
         covered = ws["n_rounds"] / L  # steps in the window (all timed steps unless it filled up)
         per_step = {k: ws[k] / covered for k in ("window_ms", "copy_busy_ms", "copy_gap_ms", "chunk_kernel_ms",
@@ -602,10 +754,13 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
                # inside transfer intervals (a kernel that reads host memory in place is the transfer)
                "hidden_frac": (1.0 - ws["chunk_kernel_exposed_ms"] / (ws["chunk_kernel_ms"] - ws["zero_copy_kernel_ms"])
                                if ws["chunk_kernel_ms"] - ws["zero_copy_kernel_ms"] > 0 else None),
-               # over the whole step: whatever of the step is not transfer time counts as exposed compute,
-               # against the same chunks' kernel time with resident history
-               "hidden_frac_step": 1.0 - max(0.0, per_step["window_ms"] - per_step["transfer_busy_ms"])
-               / res_chunk_ms_step}
+               # per step (first round begin to last finish end): whatever of the step is not transfer time
+               # counts as exposed compute, against the same chunks' kernel time with resident history;
+               # the median over the timed steps
+               "hidden_frac_step": statistics.median(1.0 - max(0.0, t - tr) / res_chunk_ms_step for t, tr in so),
+               "step_ms_median": statistics.median(t for t, _ in so),
+               "step_transfer_ms_median": statistics.median(tr for _, tr in so),
+               "resident_chunk_kernel_ms_per_step": res_chunk_ms_step}
         return out, ms
 
     v_e2e = R.verifier(timing=True, adaptive=True, zero_copy_ctas=a.adaptive_ctas)
@@ -703,12 +858,16 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
             for cap, (vz, zp, ms) in zc_ctx.items():
                 modes.append((f"zero_copy_{cap}_ctas", vz, zp, ms))
             tp = {"draft": "bf16 GEMM 4096^3, CUDA-graph replays of 8 on a lowest-priority stream",
-                  "draft_tflops_alone": draft_alone, "modes": {}}
-            for name, vx, pushes, ms_alone in modes:
+                  "draft_tflops_alone": draft_alone, "modes": {},
+                  "baseline": "each mode's Target steps timed alone right before its co-run"}
+            tp_steps = max(3, min(steps, 10))
+            for name, vx, pushes, _ms in modes:
                 timing = bool(vx.cfg.flags & 1)
+                ms_alone = R.timed(lambda vx=vx, pushes=pushes: R.host_step(vx, inp, lambda li: pushes[li]), tp_steps,
+                                   1)
                 dl.start()
                 time.sleep(0.2)
-                ms_co = R.timed(lambda vx=vx, pushes=pushes: R.host_step(vx, inp, lambda li: pushes[li]), steps, 1,
+                ms_co = R.timed(lambda vx=vx, pushes=pushes: R.host_step(vx, inp, lambda li: pushes[li]), tp_steps, 1,
                                 between=vx.window_reset if timing else None)
                 tf = dl.stop()
                 m = {"delta_T": (ms_co - ms_alone) / ms_alone, "target_ms_alone": ms_alone, "target_ms_co": ms_co,
@@ -718,9 +877,21 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
                     cov = ws["n_rounds"] / L
                     m["co_per_step_ms"] = {k: ws[k] / cov for k in ("copy_busy_ms", "copy_gap_ms", "chunk_kernel_ms",
                                                                     "zero_copy_kernel_ms", "transfer_busy_ms")}
-                    m["co_copy_rate_gbs"] = copy_rates(vx.window_intervals(), push_bytes * steps) \
-                        if ws["n_rounds"] == steps * L else None
+                    m["co_copy_rate_gbs"] = copy_rates(vx.window_intervals(), push_bytes * tp_steps) \
+                        if ws["n_rounds"] == tp_steps * L else None
                 tp["modes"][name] = m
+            # the same steps with Draft steps admitted by the scheduler instead of a free-running Draft (a new
+            # scheduler per mode, each against its own baseline timed right before)
+            tp["admission"] = {"draft": "one bf16 GEMM 4096^3 per Draft step, admitted per request by "
+                                        "svx_sched_try_admit, checked by svx_sched_check_start, ACKed",
+                               "modes": {}}
+            for name, vx, pushes, _ms in modes:
+                if name == "copy_engine" or name.startswith(f"zero_copy_{max(zc_ctx) if zc_ctx else -1}"):
+                    continue  # the adaptive and staged copy engines and the small zero-copy budget suffice
+                fn = (lambda vx=vx, pushes=pushes: R.host_step(vx, inp, lambda li: pushes[li]))
+                ms_alone = R.timed(fn, tp_steps, 1)
+                _ms, rec_ad = run_admitted(R, fn, 2 * tp_steps, ms_alone, AdmittedDraft(dev, B))
+                tp["admission"]["modes"][name] = rec_ad
             R.checked(v_st, inp, stream_pushes[0])
             v_st.close()
             rec["target_priority"] = tp

@@ -267,6 +267,10 @@ svx_status svx_window_stats(svx_ctx ctx, svx_window_summary* out);
  * copy stream started before the compute stream reached that event has a negative start).  Writes at most
  * cap pushes to out and the count to *n_out.  Waits like svx_window_stats. */
 svx_status svx_window_intervals(svx_ctx ctx, double* out, int64_t cap, int64_t* n_out);
+/* The window's rounds in order, 3 doubles each: round begin, finish-kernel start, finish-kernel end; ms
+ * from the window's first round begin.  With svx_window_intervals this gives each round's (or each
+ * step's) own length and transfer time.  Writes at most cap rounds; waits like svx_window_stats. */
+svx_status svx_window_rounds(svx_ctx ctx, double* out, int64_t cap, int64_t* n_out);
 
 /* ---- host-only bookkeeping (no GPU needed) ----------------------------------------------- */
 

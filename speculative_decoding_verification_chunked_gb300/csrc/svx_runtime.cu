@@ -1217,6 +1217,29 @@ svx_status svx_debug_expire_wait(svx_ctx c, int32_t wait_ms) {
   return SVX_OK;
 }
 
+svx_status svx_window_rounds(svx_ctx c, double* out, int64_t cap, int64_t* n_out) {
+  if (!c || !n_out || cap < 0 || (cap > 0 && !out)) return SVX_ERR_INVALID_ARG;
+  if (!(c->cfg.flags & SVX_FLAG_TIMING)) return fail(c, SVX_ERR_BAD_STATE, "context created without SVX_FLAG_TIMING");
+  if (c->window_restart || c->win_rounds_done == 0)
+    return fail(c, SVX_ERR_BAD_STATE, "no finished round in the timing window");
+  DeviceGuard dg(c->cfg.device);
+  SVX_CUDA(c, cudaEventSynchronize(c->done));
+  const int n = c->last_round + 1;
+  const cudaEvent_t origin = c->ev_round[0].begin;
+  for (int r = 0; r < n && r < cap; ++r) {
+    const RoundEvents& re = c->ev_round[static_cast<size_t>(r)];
+    float ms = 0.f;
+    SVX_CUDA(c, cudaEventElapsedTime(&ms, origin, re.begin));
+    out[3 * r] = ms;
+    SVX_CUDA(c, cudaEventElapsedTime(&ms, origin, re.f0));
+    out[3 * r + 1] = ms;
+    SVX_CUDA(c, cudaEventElapsedTime(&ms, origin, re.f1));
+    out[3 * r + 2] = ms;
+  }
+  *n_out = n;
+  return SVX_OK;
+}
+
 svx_status svx_adaptive_state(svx_ctx c, double* ce_ms_per_gb, double* ip_ms_per_gb, int32_t* prefer_in_place) {
   if (!c || !ce_ms_per_gb || !ip_ms_per_gb || !prefer_in_place) return SVX_ERR_INVALID_ARG;
   if (!(c->cfg.flags & SVX_FLAG_ADAPTIVE)) return fail(c, SVX_ERR_BAD_STATE, "context created without SVX_FLAG_ADAPTIVE");

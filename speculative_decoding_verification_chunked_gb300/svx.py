@@ -94,6 +94,8 @@ _SIGS = {
     "svx_round_finish": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32]),
     "svx_last_error": (ctypes.c_char_p, [_P]),
     "svx_round_stats": (ctypes.c_int, [_P, ctypes.POINTER(Stats)]),
+    "svx_window_rounds": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_double), ctypes.c_int64,
+                                         ctypes.POINTER(ctypes.c_int64)]),
     "svx_adaptive_state": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                           ctypes.POINTER(ctypes.c_int32)]),
     "svx_window_reset": (ctypes.c_int, [_P]),
@@ -638,6 +640,15 @@ class Verifier:
         out = np.zeros((max(1, n.value), 4), dtype=np.float64)
         self._check(lib.svx_window_intervals(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), n.value,
                                              ctypes.byref(n)))
+        return out[:n.value]
+
+    def window_rounds(self) -> np.ndarray:
+        """[n_rounds][3] float64: round begin, finish-kernel start, end (ms from the window's first round)."""
+        n = ctypes.c_int64(0)
+        self._check(lib.svx_window_rounds(self._h, None, 0, ctypes.byref(n)))
+        out = np.zeros((max(1, n.value), 3), dtype=np.float64)
+        self._check(lib.svx_window_rounds(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), n.value,
+                                          ctypes.byref(n)))
         return out[:n.value]
 
     def run_round(self, q, hist_len: Sequence[int], hist_k: Sequence, hist_v: Sequence, chunk_tokens: int,

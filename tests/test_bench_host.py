@@ -45,3 +45,17 @@ def test_copy_rates_skip_pushes_without_copies():
     r = bench.copy_rates(iv, [200e6, 200e6, 200e6])
     assert r["pushes"] == 2 and abs(r["max"] - 200.0) < 1e-9 and abs(r["min"] - 100.0) < 1e-9
     assert r["below_150_frac"] == 0.5
+
+
+def test_step_overlap_takes_the_union_of_transfers_inside_each_step():
+    import numpy as np
+    nan = np.nan
+    # two steps of one layer with two pushes each; push 1 of step 0 is read in place (no copy interval)
+    iv = np.array([[0.0, 2.0, 2.0, 2.5], [nan, nan, 2.5, 4.0],
+                   [10.0, 12.0, 12.0, 12.4], [12.1, 14.0, 14.0, 14.3]])
+    rounds = np.array([[-0.5, 4.0, 4.2], [9.8, 14.3, 14.5]])
+    so = bench.step_overlap(iv, rounds, 2, 1)
+    assert len(so) == 2
+    (t0, b0), (t1, b1) = so
+    assert abs(t0 - 4.7) < 1e-9 and abs(b0 - 3.5) < 1e-9  # [0, 2] and the in-place kernel [2.5, 4]
+    assert abs(t1 - 4.7) < 1e-9 and abs(b1 - 3.9) < 1e-9  # [10, 12] and [12.1, 14]
