@@ -127,9 +127,13 @@ cudaError_t launch_finish(const FinishParams& p, int head_dim, cudaStream_t stre
 cudaError_t launch_expire_wait(int* err, uint64_t limit_ns, cudaStream_t stream);
 
 // Tensor-core chunk kernel (d = 64 or 128).  Modes: 0 one softmax warpgroup (<= 32 query rows per pass),
-// 2 two warpgroups on 32 rows each (<= 64 rows per pass), both reading every K/V tile once.
+// 2 two warpgroups on 32 rows each (<= 64 rows per pass), both reading every K/V tile once, 3 (d = 64)
+// two warpgroups on two adjacent KV heads whose 64 dimensions form one 128-dimension tile row.
 bool tc_supported(int head_dim, int rows);
 int tc_mode(int rows);
+// The mode for a launch: head pairs (mode 3) for head dimension 64, an even KV-head count and at most
+// 32 rows per head, else tc_mode(rows).
+int tc_mode_for(int head_dim, int n_kv_heads, int rows);
 int tc_rows_per_pass(int mode);
 int tc_slots_per_segment(int mode);
 int tc_max_ctas(int num_sms);

@@ -535,7 +535,7 @@ svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, int cta_cap) {
     p.n_parts = n;
     for (int i = 0; i < n; ++i) p.parts[i] = parts[i0 + i];
     if (c->use_tc) {
-      const int mode = svx::tc_mode(R);
+      const int mode = svx::tc_mode_for(c->cfg.head_dim, c->cfg.n_kv_heads, R);
       int64_t budget = svx::tc_max_ctas(c->num_sms);
       if (cta_cap > 0) budget = std::min<int64_t>(budget, cta_cap);
       int64_t slots = 0;

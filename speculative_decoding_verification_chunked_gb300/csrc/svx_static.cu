@@ -177,7 +177,7 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
     }
     cudaError_t e;
     if (svx::tc_supported(head_dim, R)) {
-      const int mode = svx::tc_mode(R);
+      const int mode = svx::tc_mode_for(head_dim, n_kv_heads, R);
       int64_t slots = 0;
       const int64_t ctas = svx::tc_plan(p, mode, svx::tc_max_ctas(num_sms), &slots);
       for (int i = 0; i < n; ++i) slot_mask[p.parts[i].req] |= (1u << slots) - 1u;

@@ -63,7 +63,15 @@ constexpr float kTau = 8.0f;
 //   kSingle    one warpgroup: up to 32 rows of a (request, KV head) pair per pass.
 //   kRowSplit  two warpgroups on 64 rows, 32 each; both consume every K/V tile, so a tile read
 //              from HBM serves all 64 rows (the token-tree shape: G = 4, 16 nodes).
-enum : int { kSingle = 0, kRowSplit = 2 };
+//   kHeadPair  head dimension 64, up to 32 rows per KV head: one tile row is the 128 contiguous
+//              dimensions of two adjacent KV heads (the history's [token][Hkv][64] row holds them side
+//              by side), and warpgroup w takes the rows of head 2p + w.  Its Q rows fill only their
+//              head's 64 dimensions (the other half is zero), so the 128-dimension S product is
+//              block-diagonal: each row scores its own head's keys.  The PV product gives both heads'
+//              values for every row, and each thread keeps the half of O that belongs to its
+//              warpgroup's head.  A tile then carries 128 dimensions of history for the same softmax
+//              work, as with d = 128.
+enum : int { kSingle = 0, kRowSplit = 2, kHeadPair = 3 };
 
 template <int MODE>
 struct TcCfg {
@@ -371,6 +379,9 @@ struct Waiter {
 template <int MODE, int NK, int DH>
 __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const __grid_constant__ ChunkParams P) {
   static_assert(DH == 64 || DH == TILE_D, "head dimension");
+  constexpr bool PAIR = MODE == kHeadPair;
+  static_assert(!PAIR || DH == 64, "head pairs need head dimension 64");
+  constexpr int TD = PAIR ? TILE_D : DH;  // dimensions of a tile row that are loaded and multiplied
   using C = TcCfg<MODE>;
   constexpr int NCOL = C::NCOL;
   constexpr int NWG = C::NWG;
@@ -416,7 +427,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async();
   }
-  if constexpr (DH < TILE_D) {
+  if constexpr (TD < TILE_D) {
     // the upper 64 dimensions of every V slot stay zero for the whole launch (the producers write only
     // the lower half), so the PV product's rows 64..127 are zero
     for (uint32_t o = threadIdx.x * 16u; o < static_cast<uint32_t>(C::VST * HALF_BYTES); o += C::THREADS * 16u)
@@ -456,7 +467,8 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       const Seg sg = seg_at(P, split, grp, x, x_end, hint);
       const PartDesc& pd = P.parts[sg.part];
       const int64_t n_tok = pd.n_tok;
-      const __nv_bfloat16* src = (is_v ? pd.v : pd.k) + static_cast<int64_t>(sg.g) * DH;
+      // a group's head (or, for head pairs, pair p: heads 2p and 2p + 1, dimensions 128p .. 128p + 127)
+      const __nv_bfloat16* src = (is_v ? pd.v : pd.k) + static_cast<int64_t>(sg.g) * TD;
       for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
         const int slot = static_cast<int>(i % nst);
         const uint32_t use = static_cast<uint32_t>(i / nst);
@@ -468,7 +480,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
         const uint32_t dst = ring + static_cast<uint32_t>(slot) * TILE_BYTES;
         // a token row of one head is PC 16-byte pieces; lane copies piece c = lane % PC of rows
         // r0 + RPI*j (j < TOK/RPI); rows past n_tok read nothing
-        constexpr int PC = DH / 8, RPI = 32 / PC;
+        constexpr int PC = TD / 8, RPI = 32 / PC;
         const int c = lane % PC, r0 = lane / PC;
         const int64_t valid_rows = (n_tok - tok0 < TOK) ? (n_tok - tok0) : static_cast<int64_t>(TOK);
         const __nv_bfloat16* ps = src + (tok0 + r0) * kv_stride + c * 8;
@@ -515,7 +527,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
         const uint32_t d = tmem + C::S_COL + static_cast<uint32_t>(j & 1) * ROWS;
         const uint32_t ka = desc_lo(kaddr, 16);
 #pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk)
+        for (int kk = 0; kk < TD / 16; ++kk)
           mma_bf16(d, ka + desc_adv((kk >> 2) * HALF_BYTES + (kk & 3) * 32),
                    qa + desc_adv((kk >> 2) * (ROWS * 128) + (kk & 3) * 32), kDescHi, idesc_s, kk > 0 ? 1u : 0u);
         mma_commit(SFULL + 8u * static_cast<uint32_t>(j & 1));
@@ -650,21 +662,35 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     };
 
     // This warpgroup's 32 Q rows of a pass into shared memory (K-major swizzled [ROWS][128], padding
-    // rows zero; with d = 64 the upper half is never read) with cp.async; QFULL completes when every
-    // softmax thread's copies have landed.
+    // rows zero; with d = 64 and one head per group the upper half is never read) with cp.async; QFULL
+    // completes when every softmax thread's copies have landed.  Head pairs: warpgroup wg's rows are head
+    // 2p + wg's, written into dimension half wg, and the other half is zero-filled.
     int hint_q = 0;
     auto load_q = [&](int64_t xq) {
       const Seg sq = seg_at(P, split, grp, xq, x_end, hint_q);
-      const int rblk = sq.rb * C::ROWS;
-      const int nrows = min(C::ROWS, P.group * P.n_query - rblk);
-      const int64_t qrow0 = (static_cast<int64_t>(P.parts[sq.part].req) * P.n_q_heads +
-                             static_cast<int64_t>(sq.g) * P.group) * P.n_query + rblk;
+      if constexpr (PAIR) {
+        const int nrows = min(NCOL, P.group * P.n_query);
+        const int64_t qrow0 = (static_cast<int64_t>(P.parts[sq.part].req) * P.n_q_heads +
+                               static_cast<int64_t>(2 * sq.g + wg) * P.group) * P.n_query;
 #pragma unroll
-      for (int idx = tid; idx < NCOL * (DH / 8); idx += 128) {
-        const int c = wg * NCOL + idx / (DH / 8), ch = idx % (DH / 8);
-        const bool in = c < nrows;
-        cp_async16(base + C::OFF_Q + swz_offset(c, ch, C::ROWS * 128), in ? P.q + (qrow0 + c) * DH + ch * 8 : P.q,
-                   in ? 16 : 0);
+        for (int idx = tid; idx < NCOL * (TILE_D / 8); idx += 128) {
+          const int r = idx / (TILE_D / 8), ch = idx % (TILE_D / 8);
+          const bool in = r < nrows && (ch >> 3) == wg;
+          cp_async16(base + C::OFF_Q + swz_offset(wg * NCOL + r, ch, C::ROWS * 128),
+                     in ? P.q + (qrow0 + r) * DH + (ch & 7) * 8 : P.q, in ? 16 : 0);
+        }
+      } else {
+        const int rblk = sq.rb * C::ROWS;
+        const int nrows = min(C::ROWS, P.group * P.n_query - rblk);
+        const int64_t qrow0 = (static_cast<int64_t>(P.parts[sq.part].req) * P.n_q_heads +
+                               static_cast<int64_t>(sq.g) * P.group) * P.n_query + rblk;
+#pragma unroll
+        for (int idx = tid; idx < NCOL * (DH / 8); idx += 128) {
+          const int c = wg * NCOL + idx / (DH / 8), ch = idx % (DH / 8);
+          const bool in = c < nrows;
+          cp_async16(base + C::OFF_Q + swz_offset(c, ch, C::ROWS * 128), in ? P.q + (qrow0 + c) * DH + ch * 8 : P.q,
+                     in ? 16 : 0);
+        }
       }
       cp_async_arrive_noinc(QFULL);
     };
@@ -678,10 +704,12 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       const int b = pd.req;
       const int R = P.group * P.n_query;
       const int rblk = sg.rb * C::ROWS;                          // first row of this pass
-      const int r0 = rblk + ((MODE == kRowSplit) ? wg * NCOL : 0);  // this warpgroup's first row
+      // this warpgroup's first row (of its head's rows; head pairs: each warpgroup has its own head)
+      const int r0 = PAIR ? 0 : rblk + ((MODE == kRowSplit) ? wg * NCOL : 0);
       nr = max(0, min(NCOL, R - r0));
+      const int head = PAIR ? 2 * sg.g + wg : sg.g;
       const int64_t qrow0 =
-          (static_cast<int64_t>(b) * P.n_q_heads + static_cast<int64_t>(sg.g) * P.group) * P.n_query;
+          (static_cast<int64_t>(b) * P.n_q_heads + static_cast<int64_t>(head) * P.group) * P.n_query;
 
       if (!q_loaded) load_q(x);
       q_loaded = false;
@@ -842,10 +870,13 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
         }
         bar_sync(bar_wg, 128);
         // per 8-row block: the earlier accumulators first (independent loads), then the merged values
-        // (threads past the head dimension hold the zero rows of O^T)
-        float* ap = P.ws_a + srow0 * DH + tid;
+        // (threads past the head dimension hold the zero rows of O^T; with head pairs, thread tid holds
+        // dimension tid - 64 wg of its warpgroup's head, and the other half holds the other head's values)
+        const int dim = PAIR ? tid - 64 * wg : tid;
+        const bool dim_ok = dim >= 0 && dim < DH;
+        float* ap = P.ws_a + srow0 * DH + (dim_ok ? dim : 0);
 #pragma unroll
-        for (int k = 0; k < NK && tid < DH; ++k) {
+        for (int k = 0; k < NK && dim_ok; ++k) {
           float olda[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -922,6 +953,17 @@ cudaError_t launch_tc_dh(const ChunkParams& p, int mode, int n_ctas, cudaStream_
     }
   }
   if (mode == kRowSplit) return launch_tc<kRowSplit, 4, DH>(p, n_ctas, stream);
+  if constexpr (DH == 64) {
+    if (mode == kHeadPair) {  // each head's R <= 32 rows: ceil(R / 8) column blocks
+      if (R < 1 || R > TcCfg<kHeadPair>::NCOL) return cudaErrorInvalidValue;
+      switch ((R + 7) / 8) {
+        case 1: return launch_tc<kHeadPair, 1, 64>(p, n_ctas, stream);
+        case 2: return launch_tc<kHeadPair, 2, 64>(p, n_ctas, stream);
+        case 3: return launch_tc<kHeadPair, 3, 64>(p, n_ctas, stream);
+        default: return launch_tc<kHeadPair, 4, 64>(p, n_ctas, stream);
+      }
+    }
+  }
   return cudaErrorInvalidValue;
 }
 
@@ -929,7 +971,14 @@ cudaError_t launch_tc_dh(const ChunkParams& p, int mode, int n_ctas, cudaStream_
 
 bool tc_supported(int head_dim, int rows) { return (head_dim == 64 || head_dim == 128) && rows >= 1; }
 int tc_mode(int rows) { return rows <= TcCfg<kSingle>::ROWS ? kSingle : kRowSplit; }
-int tc_rows_per_pass(int mode) { return mode == kRowSplit ? TcCfg<kRowSplit>::ROWS : TcCfg<kSingle>::ROWS; }
+int tc_mode_for(int head_dim, int n_kv_heads, int rows) {
+  if (head_dim == 64 && n_kv_heads % 2 == 0 && rows <= TcCfg<kHeadPair>::NCOL) return kHeadPair;
+  return tc_mode(rows);
+}
+int tc_rows_per_pass(int mode) {
+  if (mode == kRowSplit) return TcCfg<kRowSplit>::ROWS;
+  return TcCfg<kSingle>::ROWS;  // kSingle; kHeadPair: the rows of one head per warpgroup
+}
 int tc_slots_per_segment(int) { return 1; }
 int tc_max_ctas(int num_sms) { return num_sms; }  // one CTA per SM (shared memory)
 
@@ -937,9 +986,11 @@ int64_t tc_plan(ChunkParams& p, int mode, int64_t cta_budget, int64_t* slots) {
   const int R = p.group * p.n_query;
   const int rpp = tc_rows_per_pass(mode);
   p.n_rowblk = (R + rpp - 1) / rpp;
-  // one CTA group per (head, row block); each group's tiles (that head and row block of every part,
-  // part after part) are split evenly over its CTAs, so CTA j of every group covers the same tokens
-  const int64_t groups = static_cast<int64_t>(p.n_kv_heads) * p.n_rowblk;
+  // one CTA group per (head, row block), or per pair of heads; each group's tiles (that head and row
+  // block of every part, part after part) are split evenly over its CTAs, so CTA j of every group
+  // covers the same tokens
+  const int64_t groups = mode == kHeadPair ? static_cast<int64_t>(p.n_kv_heads / 2)
+                                           : static_cast<int64_t>(p.n_kv_heads) * p.n_rowblk;
   int64_t T = 0;
   for (int i = 0; i < p.n_parts; ++i) {
     p.parts[i].tile_base = T;

@@ -44,6 +44,9 @@ SMALL = [
     W.Workload("r12", 2, 8, 4, 128, (600, 1025), 256, 6, seed=24),    # 12 rows: two 8-row column blocks
     W.Workload("r16", 3, 16, 8, 128, (129, 2000, 64), 512, 8, seed=25),  # 16 rows, exactly two blocks
     W.Workload("g1d128", 2, 8, 8, 128, (300, 129), 128, 3, seed=28),    # one query head per KV head
+    # head dimension 64 with an even KV-head count and <= 32 rows per head: two heads per tile row
+    W.Workload("pair_r32", 3, 64, 2, 64, (1000, 1, 300), 256, 1, seed=26),   # 32 rows per head, one pair
+    W.Workload("pair_h6", 2, 12, 6, 64, (777, 129), 128, 5, seed=27),        # 10 rows per head, three pairs
 ]
 
 
