@@ -11,13 +11,15 @@ candidate chain), chunks of 8192 tokens.
   value  verification tokens/s with every input already in HBM (history read in
          place as device parts): the HBM-bound form of the step.
   e2e    the same metric through the same API with HOST buffers: Q and the
-         candidate KV copied from pinned host memory, the committed history
-         streamed chunk by chunk from pinned host memory by the library's copy
-         engine (adaptive: host regions the copy engine reads slowly are read in
-         place by the chunk kernel), O and LSE copied back, all inside the timed
-         region; the next layer's chunk copies queue behind the current layer's
-         (cross-layer prefetch).  Overlap figures come from the same context's
-         timing window over the same timed steps.
+         candidate KV copied from pinned host memory, the committed history of
+         every layer read from pinned host memory over the host link by the chunk
+         kernel itself (in-place reads on 32 CTAs), O and LSE copied back and read
+         on the host, all inside the timed region.  Overlap figures come from the
+         same context's timing window over the same timed steps.  The copy engine
+         (chunks staged through triple-buffered slots, the next layer's copies
+         queued behind the current layer's) and the adaptive choice between the
+         two engines are measured the same way under "streamed_copy_engine" and
+         "streamed_adaptive".
 
 The other named workloads (tiny, qwen3, internlm, tree) run as shorter
 sub-records under "workloads".  Every step reads more than the 129 MB L2 except
@@ -727,33 +729,37 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
     v_res.close()
     inp.drop_resident(keep_first=False)
 
-    # ---- e2e: streamed from pinned host through the public API, copies in the timed region
-    stream_pushes = [inp.parts(ly["kh_h"], ly["vh_h"], False) for ly in inp.layers]
+    # ---- e2e: streamed from pinned host through the public API, every transfer in the timed region.  The
+    # e2e engine is the chunk kernel's in-place reads of pinned host memory over the host link; the copy
+    # engine (staging slots) and the adaptive choice between the two are measured the same way beside it.
+    stream_pushes = [inp.parts(ly["kh_h"], ly["vh_h"], False) for ly in inp.layers]  # the plan's chunks
+    whole_pushes = [inp.parts(ly["kh_h"], ly["vh_h"], True) for ly in inp.layers]    # one part per request
     push_bytes = [sum(n for _b, _t, n, _k, _v in p) * row_bytes * 2 for pl in stream_pushes for p in pl]
     link_before = link_probe(inp, dev, xs)
 
-    def streamed(v, label, reps=1):
+    def streamed(v, pushes, label):
         """Streamed steps through context v: throughput, overlap over the timed steps (the context's timing
         window), per-push copy rates."""
-        ms = R.timed(lambda: R.host_step(v, inp, lambda li: stream_pushes[li]), steps, warmup,
-                     between=v.window_reset)
+        ms = R.timed(lambda: R.host_step(v, inp, lambda li: pushes[li]), steps, warmup, between=v.window_reset)
         ws = v.window_stats()
         iv = v.window_intervals()
-        so = step_overlap(iv, v.window_rounds(), len(stream_pushes[0]) * L, L)
+        so = step_overlap(iv, v.window_rounds(), len(pushes[0]) * L, L)
         val, ms_job = job_throughput(B * nq, ms, world, dev)
         covered = ws["n_rounds"] / L  # steps in the window (all timed steps unless it filled up)
         per_step = {k: ws[k] / covered for k in ("window_ms", "copy_busy_ms", "copy_gap_ms", "chunk_kernel_ms",
                                                "chunk_kernel_exposed_ms", "transfer_busy_ms",
                                                "zero_copy_kernel_ms", "finish_kernel_ms")}
+        staged_kernel = ws["chunk_kernel_ms"] - ws["zero_copy_kernel_ms"]
         out = {"value": val, "unit": UNIT, "ms_per_step": ms_job, "what": label,
                "hist_gb_per_s": hist_bytes / (ms / 1e3) / 1e9,
                "per_step_ms": per_step,
-               "zero_copy_push_frac": ws["n_zero_copy_pushes"] / max(1, ws["n_pushes"]),
-               "copy_rate_gbs": copy_rates(iv, push_bytes * steps) if ws["n_rounds"] == steps * L else None,
+               "in_place_push_frac": ws["n_zero_copy_pushes"] / max(1, ws["n_pushes"]),
+               "copy_rate_gbs": (copy_rates(iv, push_bytes * steps)
+                                 if pushes is stream_pushes and ws["n_rounds"] == steps * L else None),
                # chunk compute hidden under transfer: the time of chunk kernels over staged parts that lies
-               # inside transfer intervals (a kernel that reads host memory in place is the transfer)
-               "hidden_frac": (1.0 - ws["chunk_kernel_exposed_ms"] / (ws["chunk_kernel_ms"] - ws["zero_copy_kernel_ms"])
-                               if ws["chunk_kernel_ms"] - ws["zero_copy_kernel_ms"] > 0 else None),
+               # inside transfer intervals; a kernel that reads host memory in place is the transfer itself
+               # (1.0 when every push is read in place)
+               "hidden_frac": 1.0 - ws["chunk_kernel_exposed_ms"] / staged_kernel if staged_kernel > 0 else 1.0,
                # per step (first round begin to last finish end): whatever of the step is not transfer time
                # counts as exposed compute, against the same chunks' kernel time with resident history;
                # the median over the timed steps
@@ -763,17 +769,22 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
                "resident_chunk_kernel_ms_per_step": res_chunk_ms_step}
         return out, ms
 
-    v_e2e = R.verifier(timing=True, adaptive=True, zero_copy_ctas=a.adaptive_ctas)
-    e2e_rec, ms_e2e = streamed(v_e2e, f"adaptive copy engine: staged through {a.slots} slots; host regions the "
-                                      f"copy engine reads slowly are read in place on {a.adaptive_ctas} CTAs")
-    e2e_rec["adaptive_state"] = v_e2e.adaptive_state()
-    R.checked(v_e2e, inp, stream_pushes[0])
+    e2e_ctas = a.adaptive_ctas
+    v_e2e = R.verifier(timing=True, zero_copy=True, zero_copy_ctas=e2e_ctas)
+    e2e_rec, ms_e2e = streamed(v_e2e, whole_pushes, f"in-place reads: the chunk kernel reads each layer's pinned host "
+                                                    f"history over the host link on {e2e_ctas} CTAs")
+    R.checked(v_e2e, inp, whole_pushes[0])
     v_ce = R.verifier(timing=True)
-    ce_rec, ms_ce = streamed(v_ce, f"copy engine: every chunk staged through {a.slots} slots")
+    ce_rec, ms_ce = streamed(v_ce, stream_pushes, f"copy engine: every chunk staged through {a.slots} slots")
     R.checked(v_ce, inp, stream_pushes[0])
+    v_ad = R.verifier(timing=True, adaptive=True, zero_copy_ctas=e2e_ctas)
+    ad_rec, ms_ad = streamed(v_ad, stream_pushes, f"adaptive: per round the copy engine, or in-place reads on "
+                                                  f"{e2e_ctas} CTAs when measured 10% faster")
+    ad_rec["adaptive_state"] = v_ad.adaptive_state()
+    R.checked(v_ad, inp, stream_pushes[0])
     link_after = link_probe(inp, dev, xs)
     link_gbs = max(link_before, link_after)
-    for r in (e2e_rec, ce_rec):
+    for r in (e2e_rec, ce_rec, ad_rec):
         r["link_frac"] = r["hist_gb_per_s"] / link_gbs
     e2e_value, ms_e2e_job = job_throughput(B * nq, ms_e2e, world, dev)
     h2d_step = hist_bytes + sum((ly["q_h"].numel() + ly["kc_h"].numel() + ly["vc_h"].numel()) * 2
@@ -783,22 +794,25 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
                   "d2h_bytes_per_step": int(d2h_step), "ms_per_step": ms_e2e_job}
     rec["streamed"] = dict(e2e_rec, link_gbs=link_gbs, link_gbs_before_after=[link_before, link_after])
     rec["streamed_copy_engine"] = ce_rec
+    rec["streamed_adaptive"] = ad_rec
 
-    # ---- zero-copy: pinned host history read in place by the chunk kernel over the host link
+    # ---- in-place reads on other CTA budgets
     zc = {}
-    caps = [int(x) for x in a.zero_copy_ctas.split(",") if x.strip() != ""] if full else [32]
+    caps = [int(x) for x in a.zero_copy_ctas.split(",") if x.strip() != "" and int(x) != e2e_ctas] if full else []
     zc_ctx = {}
     for cap in caps:
         vz = R.verifier(zero_copy=True, zero_copy_ctas=cap)
-        zc_pushes = [inp.parts(ly["kh_h"], ly["vh_h"], True) for ly in inp.layers]
-        ms = R.timed(lambda vz=vz, zp=zc_pushes: R.host_step(vz, inp, lambda li: zp[li]), steps, warmup)
-        R.checked(vz, inp, zc_pushes[0])
+        ms = R.timed(lambda vz=vz: R.host_step(vz, inp, lambda li: whole_pushes[li]), steps, warmup)
+        R.checked(vz, inp, whole_pushes[0])
         val, ms_job = job_throughput(B * nq, ms, world, dev)
         zc[str(cap)] = {"value": val, "unit": UNIT, "ms_per_step": ms_job,
                         "hist_gb_per_s": hist_bytes / (ms / 1e3) / 1e9,
                         "link_frac": hist_bytes / (ms / 1e3) / 1e9 / link_gbs,
                         "ctas": cap if cap > 0 else torch.cuda.get_device_properties(dev).multi_processor_count}
-        zc_ctx[cap] = (vz, zc_pushes, ms)
+        zc_ctx[cap] = (vz, whole_pushes, ms)
+    zc[str(e2e_ctas)] = {"value": e2e_rec["value"], "unit": UNIT, "ms_per_step": e2e_rec["ms_per_step"],
+                         "hist_gb_per_s": e2e_rec["hist_gb_per_s"], "link_frac": e2e_rec["link_frac"],
+                         "ctas": e2e_ctas, "what": "the e2e context"}
     rec["streamed_zero_copy"] = zc
 
     if full:
@@ -850,13 +864,14 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
             time.sleep(1.0)
             draft_alone = dl.stop()
             v_st = R.verifier(staged_ctas=a.staged_ctas, timing=True)
-            st_rec, ms_st = streamed(v_st, f"copy engine, staged chunk launches on {a.staged_ctas} CTAs")
+            st_rec, ms_st = streamed(v_st, stream_pushes, f"copy engine, staged chunk launches on {a.staged_ctas} CTAs")
             rec["streamed_copy_engine_staged"] = dict(st_rec, link_frac=st_rec["hist_gb_per_s"] / link_gbs)
-            modes = [("adaptive_copy_engine", v_e2e, stream_pushes, ms_e2e),
+            modes = [(f"in_place_{e2e_ctas}_ctas", v_e2e, whole_pushes, ms_e2e),
                      ("copy_engine", v_ce, stream_pushes, ms_ce),
-                     (f"copy_engine_staged_{a.staged_ctas}_ctas", v_st, stream_pushes, ms_st)]
+                     (f"copy_engine_staged_{a.staged_ctas}_ctas", v_st, stream_pushes, ms_st),
+                     ("adaptive", v_ad, stream_pushes, ms_ad)]
             for cap, (vz, zp, ms) in zc_ctx.items():
-                modes.append((f"zero_copy_{cap}_ctas", vz, zp, ms))
+                modes.append((f"in_place_{cap}_ctas", vz, zp, ms))
             tp = {"draft": "bf16 GEMM 4096^3, CUDA-graph replays of 8 on a lowest-priority stream",
                   "draft_tflops_alone": draft_alone, "modes": {},
                   "baseline": "each mode's Target steps timed alone right before its co-run"}
@@ -878,7 +893,7 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
                     m["co_per_step_ms"] = {k: ws[k] / cov for k in ("copy_busy_ms", "copy_gap_ms", "chunk_kernel_ms",
                                                                     "zero_copy_kernel_ms", "transfer_busy_ms")}
                     m["co_copy_rate_gbs"] = copy_rates(vx.window_intervals(), push_bytes * tp_steps) \
-                        if ws["n_rounds"] == tp_steps * L else None
+                        if pushes is stream_pushes and ws["n_rounds"] == tp_steps * L else None
                 tp["modes"][name] = m
             # the same steps with Draft steps admitted by the scheduler instead of a free-running Draft (a new
             # scheduler per mode, each against its own baseline timed right before)
@@ -886,8 +901,8 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
                                         "svx_sched_try_admit, checked by svx_sched_check_start, ACKed",
                                "modes": {}}
             for name, vx, pushes, _ms in modes:
-                if name == "copy_engine" or name.startswith(f"zero_copy_{max(zc_ctx) if zc_ctx else -1}"):
-                    continue  # the adaptive and staged copy engines and the small zero-copy budget suffice
+                if name in ("copy_engine", "adaptive"):
+                    continue  # in-place reads on both budgets and the copy engine on a few SMs
                 fn = (lambda vx=vx, pushes=pushes: R.host_step(vx, inp, lambda li: pushes[li]))
                 ms_alone = R.timed(fn, tp_steps, 1)
                 _ms, rec_ad = run_admitted(R, fn, 2 * tp_steps, ms_alone, AdmittedDraft(dev, B))
@@ -899,6 +914,7 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
         vz.close()
     v_e2e.close()
     v_ce.close()
+    v_ad.close()
     rec["_inputs"] = inp
     return rec
 
@@ -966,8 +982,8 @@ def main(argv=None):
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": head["config"],
            "e2e": head["e2e"], "gpu_launches": head["launches_per_step"] * head["steps"],
            "roofline": head["roofline"], "clocks": clocks}
-    for k in ("streamed", "streamed_copy_engine", "resident", "restore_then_verify", "streamed_zero_copy",
-              "target_priority"):
+    for k in ("streamed", "streamed_copy_engine", "streamed_adaptive", "streamed_copy_engine_staged", "resident",
+              "restore_then_verify", "streamed_zero_copy", "target_priority"):
         if k in head:
             out[k] = head[k]
     if cpu:
