@@ -13,7 +13,7 @@ candidate chain), chunks of 8192 tokens.
   e2e    the same metric through the same API with HOST buffers: Q and the
          candidate KV copied from pinned host memory, the committed history of
          every layer read from pinned host memory over the host link by the chunk
-         kernel itself (in-place reads on 32 CTAs), O and LSE copied back and read
+         kernel itself (in-place reads on up to every SM), O and LSE copied back and read
          on the host, all inside the timed region.  Overlap figures come from the
          same context's timing window over the same timed steps.  The copy engine
          (chunks staged through triple-buffered slots, the next layer's copies
@@ -63,10 +63,12 @@ def parse_args(argv=None):
                     help="the workload with another head dimension (same tokens, heads and queries)")
     ap.add_argument("--sub-workloads", default=SUB_WORKLOADS,
                     help="comma list of further workloads measured briefly under 'workloads' (empty = none)")
-    ap.add_argument("--zero-copy-ctas", default="8,32",
+    ap.add_argument("--zero-copy-ctas", default="8,32,64",
                     help="comma list of CTA caps for the zero-copy streamed variant (0 = all SMs; empty = skip)")
+    ap.add_argument("--e2e-ctas", type=int, default=0,
+                    help="CTAs of the e2e context's in-place chunk launches (reads of pinned host history)")
     ap.add_argument("--adaptive-ctas", type=int, default=32,
-                    help="CTAs of a chunk launch that reads slow host regions in place (adaptive streaming)")
+                    help="CTAs of the adaptive context's chunk launches when it reads in place")
     ap.add_argument("--staged-ctas", type=int, default=16,
                     help="CTA budget of staged chunk launches in the Target-priority variant of the copy engine")
     ap.add_argument("--no-draft-load", dest="draft_load", action="store_false",
@@ -75,6 +77,9 @@ def parse_args(argv=None):
     ap.add_argument("--resident-chunk", default="whole", choices=["whole", "plan"],
                     help="device-resident history pushed as one part per request, or in the plan's chunks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-in-place", action="store_true",
+                    help="only the e2e context's in-place steps (inputs, then --warmup and --steps steps), for a "
+                         "profiler to capture its launches; prints their mean step time")
     ap.add_argument("--cpu-sample-pairs", type=int, default=0,
                     help="(layer, request, KV head) pairs in each CPU sample (default: one per core)")
     return ap.parse_args(argv)
@@ -784,17 +789,20 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
                "resident_chunk_kernel_ms_per_step": res_chunk_ms_step}
         return out, ms
 
-    e2e_ctas = a.adaptive_ctas
+    e2e_ctas = a.e2e_ctas
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    e2e_name = f"in_place_{e2e_ctas}_ctas" if e2e_ctas > 0 else "in_place_all_sms"
     v_e2e = R.verifier(timing=True, zero_copy=True, zero_copy_ctas=e2e_ctas)
     e2e_rec, ms_e2e = streamed(v_e2e, whole_pushes, f"in-place reads: the chunk kernel reads each layer's pinned host "
-                                                    f"history over the host link on {e2e_ctas} CTAs")
+                                                    f"history over the host link on "
+                                                    f"{e2e_ctas if e2e_ctas > 0 else f'up to {n_sms}'} CTAs")
     R.checked(v_e2e, inp, whole_pushes[0])
     v_ce = R.verifier(timing=True)
     ce_rec, ms_ce = streamed(v_ce, stream_pushes, f"copy engine: every chunk staged through {a.slots} slots")
     R.checked(v_ce, inp, stream_pushes[0])
-    v_ad = R.verifier(timing=True, adaptive=True, zero_copy_ctas=e2e_ctas)
+    v_ad = R.verifier(timing=True, adaptive=True, zero_copy_ctas=a.adaptive_ctas)
     ad_rec, ms_ad = streamed(v_ad, stream_pushes, f"adaptive: per round the copy engine, or in-place reads on "
-                                                  f"{e2e_ctas} CTAs when measured 10% faster")
+                                                  f"{a.adaptive_ctas} CTAs when measured 10% faster")
     ad_rec["adaptive_state"] = v_ad.adaptive_state()
     R.checked(v_ad, inp, stream_pushes[0])
     link_after = link_probe(inp, dev, xs)
@@ -823,11 +831,11 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
         zc[str(cap)] = {"value": val, "unit": UNIT, "ms_per_step": ms_job,
                         "hist_gb_per_s": hist_bytes / (ms / 1e3) / 1e9,
                         "link_frac": hist_bytes / (ms / 1e3) / 1e9 / link_gbs,
-                        "ctas": cap if cap > 0 else torch.cuda.get_device_properties(dev).multi_processor_count}
+                        "ctas": cap if cap > 0 else n_sms}
         zc_ctx[cap] = (vz, whole_pushes, ms)
     zc[str(e2e_ctas)] = {"value": e2e_rec["value"], "unit": UNIT, "ms_per_step": e2e_rec["ms_per_step"],
                          "hist_gb_per_s": e2e_rec["hist_gb_per_s"], "link_frac": e2e_rec["link_frac"],
-                         "ctas": e2e_ctas, "what": "the e2e context"}
+                         "ctas": e2e_ctas if e2e_ctas > 0 else n_sms, "what": "the e2e context"}
     rec["streamed_zero_copy"] = zc
 
     if full:
@@ -881,7 +889,7 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
             v_st = R.verifier(staged_ctas=a.staged_ctas, timing=True)
             st_rec, ms_st = streamed(v_st, stream_pushes, f"copy engine, staged chunk launches on {a.staged_ctas} CTAs")
             rec["streamed_copy_engine_staged"] = dict(st_rec, link_frac=st_rec["hist_gb_per_s"] / link_gbs)
-            modes = [(f"in_place_{e2e_ctas}_ctas", v_e2e, whole_pushes, ms_e2e),
+            modes = [(e2e_name, v_e2e, whole_pushes, ms_e2e),
                      ("copy_engine", v_ce, stream_pushes, ms_ce),
                      (f"copy_engine_staged_{a.staged_ctas}_ctas", v_st, stream_pushes, ms_st),
                      ("adaptive", v_ad, stream_pushes, ms_ad)]
@@ -964,6 +972,19 @@ def main(argv=None):
     cs = torch.cuda.Stream(device=dev, priority=-1)
     xs = torch.cuda.Stream(device=dev, priority=-1)
 
+    if a.profile_in_place:  # the e2e context's launches alone (the first chunk launch is the first in-place one)
+        inp = Inputs(w, dev, resident=False)
+        R = Runner(a, w, dev, world, cs, xs)
+        vz = R.verifier(zero_copy=True, zero_copy_ctas=a.e2e_ctas)
+        pushes = [inp.parts(ly["kh_h"], ly["vh_h"], True) for ly in inp.layers]
+        ms = R.timed(lambda: R.host_step(vz, inp, lambda li: pushes[li]), a.steps, a.warmup)
+        R.checked(vz, inp, pushes[0])
+        vz.close()
+        if rank == 0:
+            print(json.dumps({"profile_in_place": True, "ms_per_step": ms, "ctas": a.e2e_ctas,
+                              "hist_gb_per_s": w.hist_bytes * w.n_layers / (ms / 1e3) / 1e9,
+                              "config": workload_config(w, a)}))
+        return 0
     clk = ClockSampler(local).__enter__()  # sampled over every timed region
     head = measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full=True)
     inp = head.pop("_inputs")

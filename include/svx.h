@@ -207,7 +207,9 @@ svx_status svx_debug_delay_copy(svx_ctx ctx, int64_t nth, int32_t delay_ms);
  * svx_create or svx_verify_static on this thread. */
 const char* svx_last_error(svx_ctx ctx);
 
-/* Per-round timing (needs SVX_FLAG_TIMING).  Waits for the last finished round to complete. */
+/* Per-round timing (needs SVX_FLAG_TIMING).  Waits for the last finished round to complete.  A round that
+ * opens a new timing window (after svx_window_reset, or past a window's limits) reuses the window's
+ * events, so the previous round's figures are no longer available from then on. */
 typedef struct {
   double round_ms;        /* first event of the round to the end of its finish kernel */
   double copy_busy_ms;    /* sum over pushes of H2D copy time on the copy stream */
