@@ -48,6 +48,14 @@ METRIC = "verify-attn tokens/s; streamed-KV GB/s vs host-link & HBM roofline"
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 SUB_WORKLOADS = "tiny,qwen3,internlm,tree"
+# The pages' own figures for the method, all end to end with real models on other hardware: context for
+# the numbers above, not a target for this path.
+PAGES_CONTEXT = {
+    "hardware": "2x NVIDIA A800 80GB PCIe Gen4 (TP = 2), 240 GB host memory; precision not stated",
+    "vs_offloading_baseline": "1.41x (Qwen3) and 1.32x (InternLM2.5) average output throughput over TriForce",
+    "vs_split_gpu_parallel_sd": "+55.4% output throughput per GPU versus SPECTRE+Offload on separate GPUs",
+    "stream_and_reduce_vs_restore_then_verify": "+83.2% (Qwen3) and +117.1% (InternLM2.5), q = 4, 16K inputs",
+}
 
 
 def parse_args(argv=None):
@@ -891,10 +899,10 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
             rec["streamed_copy_engine_staged"] = dict(st_rec, link_frac=st_rec["hist_gb_per_s"] / link_gbs)
             modes = [(e2e_name, v_e2e, whole_pushes, ms_e2e),
                      ("copy_engine", v_ce, stream_pushes, ms_ce),
-                     (f"copy_engine_staged_{a.staged_ctas}_ctas", v_st, stream_pushes, ms_st),
-                     ("adaptive", v_ad, stream_pushes, ms_ad)]
+                     (f"copy_engine_staged_{a.staged_ctas}_ctas", v_st, stream_pushes, ms_st)]
             for cap, (vz, zp, ms) in zc_ctx.items():
-                modes.append((f"in_place_{cap}_ctas", vz, zp, ms))
+                if cap in (8, 32):  # the budgets that leave most SMs to a co-running Draft
+                    modes.append((f"in_place_{cap}_ctas", vz, zp, ms))
             tp = {"draft": "bf16 GEMM 4096^3, CUDA-graph replays of 8 on a lowest-priority stream",
                   "draft_tflops_alone": draft_alone, "modes": {},
                   "baseline": "each mode's Target steps timed alone right before its co-run"}
@@ -924,8 +932,8 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
                                         "svx_sched_try_admit, checked by svx_sched_check_start, ACKed",
                                "modes": {}}
             for name, vx, pushes, _ms in modes:
-                if name in ("copy_engine", "adaptive"):
-                    continue  # in-place reads on both budgets and the copy engine on a few SMs
+                if name in ("copy_engine", e2e_name):
+                    continue  # in-place reads on few SMs and the copy engine's launches on a few SMs
                 fn = (lambda vx=vx, pushes=pushes: R.host_step(vx, inp, lambda li: pushes[li]))
                 ms_alone = R.timed(fn, tp_steps, 1)
                 _ms, rec_ad = run_admitted(R, fn, 2 * tp_steps, ms_alone, AdmittedDraft(dev, B))
@@ -1026,6 +1034,7 @@ def main(argv=None):
         out["cpu_baseline"] = cpu
     if subs:
         out["workloads"] = subs
+    out["pages_context"] = PAGES_CONTEXT
     if rank == 0:
         print(json.dumps(out))
     if world > 1:

@@ -326,7 +326,7 @@ def test_full_depth_rounds_back_to_back_with_prefetch(svx):
         check_parity(o_gpu, l_gpu, *oracle_out(w, x, rows=rows), rows=rows)
 
 
-ZC = [SMALL[0], SMALL[1], SMALL[3], SMALL[8]]
+ZC = [SMALL[0], SMALL[1], SMALL[3], SMALL[8], SMALL[14], SMALL[15]]  # tiny, ragged, tree64, kscale, head pairs
 
 
 @pytest.mark.parametrize("w", ZC, ids=[w.name for w in ZC])
