@@ -72,7 +72,7 @@ def parse_args(argv=None):
     ap.add_argument("--sub-workloads", default=SUB_WORKLOADS,
                     help="comma list of further workloads measured briefly under 'workloads' (empty = none)")
     ap.add_argument("--zero-copy-ctas", default="8,32,64",
-                    help="comma list of CTA caps for the zero-copy streamed variant (0 = all SMs; empty = skip)")
+                    help="comma list of CTA caps for further in-place (zero-copy) streamed variants (0 = all SMs; empty = skip)")
     ap.add_argument("--e2e-ctas", type=int, default=0,
                     help="CTAs of the e2e context's in-place chunk launches (reads of pinned host history)")
     ap.add_argument("--adaptive-ctas", type=int, default=32,
@@ -676,7 +676,8 @@ def link_probe(inp, dev, xs):
 
 def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
     """All timed figures of one workload.  `full`: the headline record (every variant); otherwise a
-    shorter sub-record (resident value, kernel roofline, streamed e2e with overlap, zero-copy on 32 CTAs)."""
+    shorter sub-record (resident value, kernel roofline, and the e2e, copy-engine and adaptive streamed
+    steps with their overlap figures)."""
     import torch
     B, nq, L = w.n_req, w.n_query, w.n_layers
     steps = a.steps if full else min(a.steps, 20)
