@@ -128,9 +128,11 @@ class _GemmLoad:
         self.c = torch.empty((n, n), device="cuda", dtype=torch.bfloat16)
         self.stop = False
         self.count = 0
+        self.device = torch.cuda.current_device()
 
     def _run(self):
         torch = self.torch
+        torch.cuda.set_device(self.device)  # a new host thread has no current device of its own
         ev = torch.cuda.Event()
         while not self.stop:
             with torch.cuda.stream(self.stream):
@@ -293,3 +295,31 @@ def test_adaptive_streaming_moves_to_in_place_reads_when_copies_are_slow(svx):
     # bytes read in place count as host bytes, and the in-place kernels count as transfer time
     assert stats[1]["h2d_bytes"] == w.hist_bytes and stats[1]["copy_busy_ms"] == 0.0
     assert stats[1]["transfer_busy_ms"] > 0.0
+
+
+def test_a_window_past_its_round_limit_starts_again(svx):
+    """A timing window holds at most 4096 rounds: the round after the limit opens a new window, whose
+    figures cover only its own rounds; the round statistics stay available and each round is correct."""
+    import torch
+    w = W.Workload("wrap", 1, 4, 1, 64, (300,), 300, 2, seed=78)
+    x, t = gpu_inputs(w, resident=True)
+    o = torch.empty((1, 4, 2, 64), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, 4, 2), dtype=torch.float32, device="cuda")
+    parts = [(0, 0, 300, t["kh"][0].data_ptr(), t["vh"][0].data_ptr())]
+    with svx.Verifier(1, 4, 1, 64, 2, 300, timing=True) as v:
+        v.window_reset()
+        for r in range(4096 + 5):
+            v.round_begin(t["q"], w.hist_len)
+            v.candidate_attn(t["kc"], t["vc"])
+            v.push_raw(parts)
+            v.round_finish(o, lse, timeout_ms=60000 if r == 4096 + 4 else 0)
+            if r == 4095:
+                ws = v.window_stats()
+                assert ws["n_rounds"] == 4096 and ws["n_pushes"] == 4096
+        ws = v.window_stats()
+        assert ws["n_rounds"] == 5 and ws["n_pushes"] == 5 and ws["device_bytes"] == 5 * w.hist_bytes
+        assert v.window_intervals().shape == (5, 4) and v.window_rounds().shape == (5, 3)
+        st = v.stats()
+        assert st["chunk_kernel_ms"] > 0 and st["n_chunk_launches"] == 1
+    torch.cuda.synchronize()
+    check_parity(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), *oracle_out(w, x))
