@@ -75,7 +75,7 @@ def parse_args(argv=None):
                     help="comma list of CTA caps for further in-place (zero-copy) streamed variants (0 = all SMs; empty = skip)")
     ap.add_argument("--e2e-ctas", type=int, default=0,
                     help="CTAs of the e2e context's in-place chunk launches (reads of pinned host history)")
-    ap.add_argument("--adaptive-ctas", type=int, default=32,
+    ap.add_argument("--adaptive-ctas", type=int, default=0,
                     help="CTAs of the adaptive context's chunk launches when it reads in place")
     ap.add_argument("--staged-ctas", type=int, default=16,
                     help="CTA budget of staged chunk launches in the Target-priority variant of the copy engine")
@@ -811,7 +811,8 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
     R.checked(v_ce, inp, stream_pushes[0])
     v_ad = R.verifier(timing=True, adaptive=True, zero_copy_ctas=a.adaptive_ctas)
     ad_rec, ms_ad = streamed(v_ad, stream_pushes, f"adaptive: per round the copy engine, or in-place reads on "
-                                                  f"{a.adaptive_ctas} CTAs when measured 10% faster")
+                                                  f"{a.adaptive_ctas if a.adaptive_ctas > 0 else f'up to {n_sms}'} "
+                                                  f"CTAs when measured 10% faster")
     ad_rec["adaptive_state"] = v_ad.adaptive_state()
     R.checked(v_ad, inp, stream_pushes[0])
     link_after = link_probe(inp, dev, xs)
