@@ -952,6 +952,164 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
     return rec
 
 
+def measure_width(a, dev, world, cs, xs, rounds=48, seed=7):
+    """The I/O-aware dynamic verification width (section 4.2) on real rounds: the qwen3-shaped layer,
+    history read in place from pinned host memory; each round runs at the width the library's controller
+    chose (q drafts, q + 1 queries and candidates) and feeds it the round's measured kernel time (the
+    transfer fused with the attention) plus a synthetic Draft cost and acceptance (no Draft model here):
+    q x 0.3 ms to draft, 0.1 ms of rejection correction, each request's drafts accepted with probability
+    0.75 each until the first rejection.  Reports the widths chosen and the committed tokens per second
+    (all requests of the Cohort)."""
+    import torch
+    from speculative_decoding_verification_chunked_gb300 import svx
+    widths, acc, t_tok, t_corr = [2, 4, 6, 8], 0.75, 0.3, 0.1
+    w = W.named("qwen3").with_(n_query=max(widths) + 1)
+    B, Hq, Hkv, d = w.n_req, w.n_q_heads, w.n_kv_heads, w.head_dim
+    inp = Inputs(w, dev, resident=False)
+    R = Runner(a, w, dev, world, cs, xs)
+    ly = inp.layers[0]
+    pushes = inp.parts(ly["kh_h"], ly["vh_h"], True)
+    g = torch.Generator(device=dev).manual_seed(seed)
+    per_q = {}
+    for q in widths:
+        nq = q + 1
+        per_q[q] = dict(q=(torch.randn((B, Hq, nq, d), generator=g, device=dev)).to(torch.bfloat16),
+                        kc=(torch.randn((B, nq, Hkv, d), generator=g, device=dev)).to(torch.bfloat16),
+                        vc=(torch.randn((B, nq, Hkv, d), generator=g, device=dev)).to(torch.bfloat16),
+                        o=torch.empty((B, Hq, nq, d), dtype=torch.bfloat16, device=dev),
+                        lse=torch.empty((B, Hq, nq), dtype=torch.float32, device=dev))
+    rng = np.random.default_rng(seed)
+    ctl = svx.WidthController(widths, ema=0.5, threshold=0.05, n_init=3)
+    v = R.verifier(zero_copy=True, zero_copy_ctas=a.e2e_ctas, timing=True)
+    chosen, total_ms, committed = [], 0.0, 0.0
+    for r in range(rounds):
+        q = ctl.next_width()
+        t = per_q[q]
+        v.round_begin(t["q"], w.hist_len)
+        v.candidate_attn(t["kc"], t["vc"])
+        for p in pushes:
+            v.push_raw(p)
+        v.round_finish(t["o"], t["lse"], timeout_ms=60000 if r == rounds - 1 else 0)
+        st = v.stats()
+        # each request's drafts are accepted until the first rejection; it commits that prefix plus the
+        # Target's own token; the controller sees the Cohort's mean
+        ok = rng.random((B, q)) < acc
+        per_req = 1.0 + np.where(ok.all(axis=1), q, np.argmin(ok, axis=1))
+        u = float(per_req.mean())
+        attn = st["chunk_kernel_ms"] + st["finish_kernel_ms"]
+        ctl.record(q, q * t_tok, st["chunk_kernel_ms"], attn, t_corr, u)
+        chosen.append(q)
+        total_ms += q * t_tok + st["round_ms"] + t_corr
+        committed += float(per_req.sum())
+    v.close()
+    costs = {q: ctl.cost(q) for q in widths}
+    steady = chosen[len(widths) * 3:]
+    return {"what": "dynamic verification width on the qwen3-shaped layer (in-place reads); Draft cost and "
+                    "acceptance synthetic: q x 0.3 ms, 0.1 ms correction, acceptance 0.75 per draft",
+            "rounds": rounds, "widths_chosen": {str(q): chosen.count(q) for q in widths},
+            "after_sampling": {str(q): steady.count(q) for q in widths},
+            "cost_ms_per_committed_token": {str(q): c for q, c in costs.items()},
+            "committed_tokens_per_s": committed / (total_ms / 1e3)}
+
+
+def measure_tiering(a, dev, world, cs, xs, rounds=40, seed=9, T=512, g=256):
+    """Commit-aware tiering (section 4.1, Eqs. 4-5) beside streaming rounds: on the qwen3-shaped layer each
+    request's Sealed History [0, H) is read in place from pinned host memory and its Active Tail [H, C)
+    in place from HBM; after every round the accepted candidates (a seeded number, 1-5 per request) are
+    committed to the tail, and whenever Eq. 5 moves the endpoint the rows [H, E) migrate to host memory
+    on a side stream while the next rounds run; H advances once a migration has completed.  Reports the
+    round time with and without migrations and the migration's device-to-host rate."""
+    import torch
+    from speculative_decoding_verification_chunked_gb300 import svx
+    w = W.named("qwen3")
+    B, Hq, Hkv, d, nq = w.n_req, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_query
+    C0 = w.hist_len[0]
+    tail0 = T + g  # initial Active Tail
+    cap = C0 + 6 * rounds * 2
+    row = Hkv * d
+    inp = Inputs(w, dev, resident=False)
+    R = Runner(a, w, dev, world, cs, xs)
+    ly = inp.layers[0]
+    bf = torch.bfloat16
+    # host copy of each request's history (capacity for the committed growth), device tail buffers
+    host_k = torch.zeros((B, cap, Hkv, d), dtype=bf, pin_memory=True)
+    host_v = torch.zeros((B, cap, Hkv, d), dtype=bf, pin_memory=True)
+    dev_k = torch.zeros((B, cap, Hkv, d), dtype=bf, device=dev)
+    dev_v = torch.zeros((B, cap, Hkv, d), dtype=bf, device=dev)
+    for b in range(B):
+        host_k[b, :C0].copy_(ly["kh_h"][b])
+        host_v[b, :C0].copy_(ly["vh_h"][b])
+        dev_k[b, C0 - tail0:C0].copy_(ly["kh_h"][b][C0 - tail0:])
+        dev_v[b, C0 - tail0:C0].copy_(ly["vh_h"][b][C0 - tail0:])
+    torch.cuda.synchronize(dev)
+    rb = row * 2
+    mig_stream = torch.cuda.Stream(device=dev)
+    rng = np.random.default_rng(seed)
+    v = R.verifier(zero_copy=True, zero_copy_ctas=a.e2e_ctas)
+
+    def run(migrate: bool):
+        tiers = [svx.Tier(C0 - tail0, C0 - tail0, C0 - tail0) for _ in range(B)]
+        for tr in tiers:
+            tr.round(C0, C0 + nq)
+        times, moved, mig_events = [], 0, []
+        for r in range(rounds):
+            hist = [tr.C for tr in tiers]
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cs)
+            v.round_begin(ly["q_d"], hist)
+            v.candidate_attn(ly["kc_d"], ly["vc_d"])
+            v.push_raw([(b, 0, tr.H, host_k[b].data_ptr(), host_v[b].data_ptr()) for b, tr in enumerate(tiers)])
+            v.push_raw([(b, tr.H, tr.C - tr.H, dev_k[b, tr.H].data_ptr(), dev_v[b, tr.H].data_ptr())
+                        for b, tr in enumerate(tiers)])
+            v.round_finish(ly["o_d"], ly["lse_d"], timeout_ms=60000 if r == rounds - 1 else 0)
+            e1.record(cs)
+            # commit: the accepted candidates' KV joins the Active Tail (the rejected ones are released)
+            acc = rng.integers(1, nq + 1, size=B)
+            with torch.cuda.stream(cs):
+                for b, tr in enumerate(tiers):
+                    c = tr.C
+                    dev_k[b, c:c + acc[b]].copy_(ly["kc_d"][b, :acc[b]])
+                    dev_v[b, c:c + acc[b]].copy_(ly["vc_d"][b, :acc[b]])
+                    tr.commit(c + int(acc[b]))
+                    tr.round(tr.C, tr.C + nq)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+            if migrate:
+                for b, tr in enumerate(tiers):
+                    if tr.pending is not None:
+                        tr.poll()
+                    if tr.pending is None:
+                        m0 = torch.cuda.Event(enable_timing=True)
+                        m1 = torch.cuda.Event(enable_timing=True)
+                        mig_stream.wait_stream(cs)  # the committed rows are written
+                        m0.record(mig_stream)
+                        H = tr.H
+                        E = tr.migrate(T, g, rb, dev_k[b, H].data_ptr(), dev_v[b, H].data_ptr(), host_k[b].data_ptr(),
+                                       host_v[b].data_ptr(), stream=mig_stream)
+                        m1.record(mig_stream)
+                        if E > H:
+                            moved += 2 * (E - H) * rb
+                            mig_events.append((m0, m1))
+        torch.cuda.synchronize(dev)
+        for tr in tiers:
+            if tr.pending is not None:
+                tr.release()
+        mig_ms = sum(m0.elapsed_time(m1) for m0, m1 in mig_events)
+        return statistics.median(times), moved, mig_ms, len(mig_events), tiers
+
+    ms_plain, _, _, _, _ = run(False)
+    ms_tier, moved, mig_ms, n_mig, tiers = run(True)
+    v.close()
+    return {"what": "rounds on the qwen3-shaped layer with the Sealed History read in place from host and the "
+                    "Active Tail from HBM, accepted candidates committed each round; with and without "
+                    "asynchronous Eq. 5 migrations of [H, E) to host memory (T = 512, g = 256)",
+            "rounds": rounds, "round_ms_median_without_migration": ms_plain,
+            "round_ms_median_with_migration": ms_tier, "slowdown": ms_tier / ms_plain - 1.0,
+            "migrations": n_mig, "migrated_bytes": int(moved),
+            "migration_gb_per_s": moved / (mig_ms / 1e3) / 1e9 if mig_ms > 0 else None,
+            "final_H": [tr.H for tr in tiers], "final_C": [tr.C for tr in tiers]}
+
+
 def main(argv=None):
     a = parse_args(argv)
     rank, world, local = dist_init()
@@ -1020,6 +1178,13 @@ def main(argv=None):
         r.pop("_inputs")
         torch.cuda.empty_cache()
         subs[name] = r
+    method = {}
+    for key, fn in (("dynamic_width", measure_width), ("tiering", measure_tiering)):
+        try:
+            method[key] = fn(a, dev, world, cs, xs)
+        except Exception as e:  # a failing sub-record is reported, not silently dropped
+            method[key] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
     clk.__exit__(None, None, None)
     clocks = clk.summary()
 
@@ -1036,6 +1201,7 @@ def main(argv=None):
         out["cpu_baseline"] = cpu
     if subs:
         out["workloads"] = subs
+    out["method"] = method
     out["pages_context"] = PAGES_CONTEXT
     if rank == 0:
         print(json.dumps(out))
