@@ -122,7 +122,7 @@ typedef struct {
  * recent ms per GB (decayed sums of time and bytes over about the last 100 pushes).  The engine is chosen per round, when it begins, so no round mixes them:
  * round 0 is staged and round 1 read in place (each engine measured once); after that, rounds are
  * staged through the copy engine unless in-place reads on zero_copy_ctas SMs were measured 10% faster
- * per byte (and then read in place until the copy engine is back within 2% of them), and one whole round
+ * per byte (and then read in place until the copy engine is measured 5% faster than them), and one whole round
  * uses the other engine after 8 rounds, then 16, 32, ... up to 1024
  * while the preference holds (back to 8 when it changes), so a change of either rate is followed.
  * Results do not depend on the choice (both paths run the same arithmetic); only the transfer engine

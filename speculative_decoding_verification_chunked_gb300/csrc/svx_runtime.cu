@@ -46,7 +46,7 @@ struct PushEvents {
 constexpr int kRateRing = 4096;      // pushes whose transfer time is still to be read
 constexpr double kAdaptDecay = 0.99;     // per-sample decay of the time and byte sums (~100 pushes)
 constexpr double kAdaptMargin = 0.10;   // in-place reads must be this much faster to replace the copy engine
-constexpr double kAdaptBack = 0.02;     // and the copy engine within this much of them to come back
+constexpr double kAdaptBack = 0.05;     // and the copy engine this much faster than them to come back
 constexpr int64_t kExploreFirst = 8;    // rounds between two measurements of the other engine, at first
 constexpr int64_t kExploreMax = 1024;   // ... doubling after each measurement up to this
 
@@ -592,15 +592,16 @@ void harvest_rates(svx_ctx c) {
 // round mixes the engines (an in-place kernel ahead of staged ones on the compute stream would hold back
 // their slots, and so the copy engine).  Round 0 is staged, round 1 read in place (each engine measured
 // once); then the copy engine unless in-place reads were measured kAdaptMargin faster per byte (once
-// preferred, until the copy engine is back within kAdaptBack of them), and a whole round on the other
-// engine every explore_gap rounds, the gap doubling while the preference holds.
+// preferred, until the copy engine is measured kAdaptBack faster than them: a copy engine whose pushes
+// are fast or slow by turns would otherwise pull the choice back and forth), and a whole round on the
+// other engine every explore_gap rounds, the gap doubling while the preference holds.
 bool choose_round_in_place(svx_ctx c) {
   harvest_rates(c);
   const int64_t r = c->adapt_rounds++;
   if (r == 0) return false;
   if (r == 1) return true;
   const bool measured = c->ce_ms_per_gb >= 0.0 && c->ip_ms_per_gb >= 0.0;
-  const bool pref = measured && (c->prefer_ip ? !(c->ce_ms_per_gb < c->ip_ms_per_gb * (1.0 + kAdaptBack))
+  const bool pref = measured && (c->prefer_ip ? !(c->ce_ms_per_gb * (1.0 + kAdaptBack) < c->ip_ms_per_gb)
                                               : c->ip_ms_per_gb * (1.0 + kAdaptMargin) < c->ce_ms_per_gb);
   if (pref != c->prefer_ip) {  // the preference changed: measure the other engine again soon
     c->prefer_ip = pref;
