@@ -47,6 +47,9 @@ SMALL = [
     # head dimension 64 with an even KV-head count and <= 32 rows per head: two heads per tile row
     W.Workload("pair_r32", 3, 64, 2, 64, (1000, 1, 300), 256, 1, seed=26),   # 32 rows per head, one pair
     W.Workload("pair_h6", 2, 12, 6, 64, (777, 129), 128, 5, seed=27),        # 10 rows per head, three pairs
+    # head dimension 64 without head pairs: 16 KiB ring slots, the PV product's upper half not kept
+    W.Workload("tree_d64", 3, 16, 4, 64, (200, 1300, 1), 128, 16, tree=True, seed=29),  # 64 rows: row split
+    W.Workload("odd_d64", 2, 6, 3, 64, (700, 1031), 256, 5, seed=30),  # odd KV-head count: one head per tile
 ]
 
 
@@ -326,7 +329,8 @@ def test_full_depth_rounds_back_to_back_with_prefetch(svx):
         check_parity(o_gpu, l_gpu, *oracle_out(w, x, rows=rows), rows=rows)
 
 
-ZC = [SMALL[0], SMALL[1], SMALL[3], SMALL[8], SMALL[14], SMALL[15]]  # tiny, ragged, tree64, kscale, head pairs
+ZC = [SMALL[0], SMALL[1], SMALL[3], SMALL[8], SMALL[14], SMALL[15], SMALL[16], SMALL[17]]  # tiny, ragged, tree64,
+# kscale, head pairs, d = 64 with one head per tile
 
 
 @pytest.mark.parametrize("w", ZC, ids=[w.name for w in ZC])
