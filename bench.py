@@ -29,7 +29,9 @@ the float64 CPU oracle on a bounded sample of each step instead.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -79,6 +81,8 @@ def parse_args(argv=None):
                     help="CTAs of the adaptive context's chunk launches when it reads in place")
     ap.add_argument("--staged-ctas", type=int, default=16,
                     help="CTA budget of staged chunk launches in the Target-priority variant of the copy engine")
+    ap.add_argument("--tp-sub-workloads", default="qwen3,internlm,tree",
+                    help="sub-workloads that also get the Target-priority record (Draft beside the streamed step)")
     ap.add_argument("--no-draft-load", dest="draft_load", action="store_false",
                     help="skip timing the streamed step beside a low-priority bf16 GEMM loop (Target priority)")
     ap.add_argument("--slots", type=int, default=3, choices=[2, 3])
@@ -573,15 +577,24 @@ class Runner:
         torch.cuda.synchronize(self.dev)
         if between is not None:
             between()
-        barrier(self.world)
-        torch.cuda.synchronize(self.dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(self.cs)
-        for _ in range(steps):
-            step_fn()
-        e1.record(self.cs)
-        torch.cuda.synchronize(self.dev)
-        barrier(self.world)
+        # Python's cycle collector stays out of the timed steps: a collection there can free an earlier
+        # workload's pinned host buffers (cudaFreeHost of tens of GB stalls the device for ~100 ms)
+        gc.collect()
+        gc_on = gc.isenabled()
+        gc.disable()
+        try:
+            barrier(self.world)
+            torch.cuda.synchronize(self.dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.cs)
+            for _ in range(steps):
+                step_fn()
+            e1.record(self.cs)
+            torch.cuda.synchronize(self.dev)
+            barrier(self.world)
+        finally:
+            if gc_on:
+                gc.enable()
         return e0.elapsed_time(e1) / steps
 
     def round_of(self, v, ly, pushes, timeout_ms=0):
@@ -831,7 +844,10 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
 
     # ---- in-place reads on other CTA budgets
     zc = {}
-    caps = [int(x) for x in a.zero_copy_ctas.split(",") if x.strip() != "" and int(x) != e2e_ctas] if full else []
+    with_tp = a.draft_load and (full or w.name in [n.strip() for n in a.tp_sub_workloads.split(",")])
+    caps = [int(x) for x in a.zero_copy_ctas.split(",") if x.strip() != "" and int(x) != e2e_ctas]
+    if not full:  # a sub-record measures the budgets that leave most SMs to a Draft, if it reports one
+        caps = [c_ for c_ in caps if c_ in (8, 32)] if with_tp else []
     zc_ctx = {}
     for cap in caps:
         vz = R.verifier(zero_copy=True, zero_copy_ctas=cap)
@@ -890,59 +906,66 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
                                               "waits for the restore)"}
         del restore_k, restore_v
 
-        # ---- Target priority: the streamed step again beside a low-priority Draft GEMM loop
-        if a.draft_load:
-            dl = DraftLoad(dev)
+    # ---- Target priority: the streamed step again beside a low-priority Draft GEMM loop
+    if with_tp:
+        dl = DraftLoad(dev)
+        dl.start()
+        time.sleep(1.0)
+        draft_alone = dl.stop()
+        v_st = R.verifier(staged_ctas=a.staged_ctas, timing=True)
+        st_rec, ms_st = streamed(v_st, stream_pushes, f"copy engine, staged chunk launches on {a.staged_ctas} CTAs")
+        rec["streamed_copy_engine_staged"] = dict(st_rec, link_frac=st_rec["hist_gb_per_s"] / link_gbs)
+        modes = [(e2e_name, v_e2e, whole_pushes, ms_e2e),
+                 ("copy_engine", v_ce, stream_pushes, ms_ce),
+                 (f"copy_engine_staged_{a.staged_ctas}_ctas", v_st, stream_pushes, ms_st)]
+        for cap, (vz, zp, ms) in zc_ctx.items():
+            if cap in (8, 32):  # the budgets that leave most SMs to a co-running Draft
+                modes.append((f"in_place_{cap}_ctas", vz, zp, ms))
+        tp = {"draft": "bf16 GEMM 4096^3, CUDA-graph replays of 8 on a lowest-priority stream",
+              "draft_tflops_alone": draft_alone, "modes": {},
+              "baseline": "each mode's Target steps timed alone right before its co-run"}
+        tp_steps = max(3, min(steps, 10))
+
+        def tp_n(ms_step):
+            """Steps per timed region: at least tp_steps, and about a second of steps for short ones, so that
+            one host hiccup does not decide a mean."""
+            return max(tp_steps, min(200, int(math.ceil(1000.0 / max(ms_step, 1e-3)))))
+
+        for name, vx, pushes, ms_mode in modes:
+            timing = bool(vx.cfg.flags & 1)
+            n = tp_n(ms_mode)
+            ms_alone = R.timed(lambda vx=vx, pushes=pushes: R.host_step(vx, inp, lambda li: pushes[li]), n, 1)
             dl.start()
-            time.sleep(1.0)
-            draft_alone = dl.stop()
-            v_st = R.verifier(staged_ctas=a.staged_ctas, timing=True)
-            st_rec, ms_st = streamed(v_st, stream_pushes, f"copy engine, staged chunk launches on {a.staged_ctas} CTAs")
-            rec["streamed_copy_engine_staged"] = dict(st_rec, link_frac=st_rec["hist_gb_per_s"] / link_gbs)
-            modes = [(e2e_name, v_e2e, whole_pushes, ms_e2e),
-                     ("copy_engine", v_ce, stream_pushes, ms_ce),
-                     (f"copy_engine_staged_{a.staged_ctas}_ctas", v_st, stream_pushes, ms_st)]
-            for cap, (vz, zp, ms) in zc_ctx.items():
-                if cap in (8, 32):  # the budgets that leave most SMs to a co-running Draft
-                    modes.append((f"in_place_{cap}_ctas", vz, zp, ms))
-            tp = {"draft": "bf16 GEMM 4096^3, CUDA-graph replays of 8 on a lowest-priority stream",
-                  "draft_tflops_alone": draft_alone, "modes": {},
-                  "baseline": "each mode's Target steps timed alone right before its co-run"}
-            tp_steps = max(3, min(steps, 10))
-            for name, vx, pushes, _ms in modes:
-                timing = bool(vx.cfg.flags & 1)
-                ms_alone = R.timed(lambda vx=vx, pushes=pushes: R.host_step(vx, inp, lambda li: pushes[li]), tp_steps,
-                                   1)
-                dl.start()
-                time.sleep(0.2)
-                ms_co = R.timed(lambda vx=vx, pushes=pushes: R.host_step(vx, inp, lambda li: pushes[li]), tp_steps, 1,
-                                between=vx.window_reset if timing else None)
-                tf = dl.stop()
-                m = {"delta_T": (ms_co - ms_alone) / ms_alone, "target_ms_alone": ms_alone, "target_ms_co": ms_co,
-                     "draft_tflops_co": tf}
-                if timing:  # where the Target's time went beside the Draft: slower copies, or a stalled pipeline
-                    ws = vx.window_stats()
-                    cov = ws["n_rounds"] / L
-                    m["co_per_step_ms"] = {k: ws[k] / cov for k in ("copy_busy_ms", "copy_gap_ms", "chunk_kernel_ms",
-                                                                    "zero_copy_kernel_ms", "transfer_busy_ms")}
-                    m["co_copy_rate_gbs"] = copy_rates(vx.window_intervals(), push_bytes * tp_steps) \
-                        if pushes is stream_pushes and ws["n_rounds"] == tp_steps * L else None
-                tp["modes"][name] = m
-            # the same steps with Draft steps admitted by the scheduler instead of a free-running Draft (a new
-            # scheduler per mode, each against its own baseline timed right before)
-            tp["admission"] = {"draft": "one bf16 GEMM 4096^3 per Draft step, admitted per request by "
-                                        "svx_sched_try_admit, checked by svx_sched_check_start, ACKed",
-                               "modes": {}}
-            for name, vx, pushes, _ms in modes:
-                if name in ("copy_engine", e2e_name):
-                    continue  # in-place reads on few SMs and the copy engine's launches on a few SMs
-                fn = (lambda vx=vx, pushes=pushes: R.host_step(vx, inp, lambda li: pushes[li]))
-                ms_alone = R.timed(fn, tp_steps, 1)
-                _ms, rec_ad = run_admitted(R, fn, 2 * tp_steps, ms_alone, AdmittedDraft(dev, B))
-                tp["admission"]["modes"][name] = rec_ad
-            R.checked(v_st, inp, stream_pushes[0])
-            v_st.close()
-            rec["target_priority"] = tp
+            time.sleep(0.2)
+            ms_co = R.timed(lambda vx=vx, pushes=pushes: R.host_step(vx, inp, lambda li: pushes[li]), n, 1,
+                            between=vx.window_reset if timing else None)
+            tf = dl.stop()
+            m = {"delta_T": (ms_co - ms_alone) / ms_alone, "target_ms_alone": ms_alone, "target_ms_co": ms_co,
+                 "draft_tflops_co": tf, "steps": n}
+            if timing:  # where the Target's time went beside the Draft: slower copies, or a stalled pipeline
+                ws = vx.window_stats()
+                cov = ws["n_rounds"] / L
+                m["co_per_step_ms"] = {k: ws[k] / cov for k in ("copy_busy_ms", "copy_gap_ms", "chunk_kernel_ms",
+                                                                "zero_copy_kernel_ms", "transfer_busy_ms")}
+                m["co_copy_rate_gbs"] = copy_rates(vx.window_intervals(), push_bytes * n) \
+                    if pushes is stream_pushes and ws["n_rounds"] == n * L else None
+            tp["modes"][name] = m
+        # the same steps with Draft steps admitted by the scheduler instead of a free-running Draft (a new
+        # scheduler per mode, each against its own baseline timed right before)
+        tp["admission"] = {"draft": "one bf16 GEMM 4096^3 per Draft step, admitted per request by "
+                                    "svx_sched_try_admit, checked by svx_sched_check_start, ACKed",
+                           "modes": {}}
+        for name, vx, pushes, ms_mode in modes:
+            if name in ("copy_engine", e2e_name):
+                continue  # in-place reads on few SMs and the copy engine's launches on a few SMs
+            fn = (lambda vx=vx, pushes=pushes: R.host_step(vx, inp, lambda li: pushes[li]))
+            n = tp_n(ms_mode)
+            ms_alone = R.timed(fn, n, 1)
+            _ms, rec_ad = run_admitted(R, fn, 2 * n, ms_alone, AdmittedDraft(dev, B))
+            tp["admission"]["modes"][name] = rec_ad
+        R.checked(v_st, inp, stream_pushes[0])
+        v_st.close()
+        rec["target_priority"] = tp
     for vz, _zp, _ms in zc_ctx.values():
         vz.close()
     v_e2e.close()
@@ -1167,6 +1190,7 @@ def main(argv=None):
                          f"= that fraction of the step's tokens over the sample's time"}
         pool.close()
     del inp
+    gc.collect()  # the headline's pinned history is freed here, not in a later timed region
     torch.cuda.empty_cache()
     subs = {}
     for name in [n.strip() for n in a.sub_workloads.split(",") if n.strip()]:
@@ -1176,6 +1200,7 @@ def main(argv=None):
         ws = ws.with_(seed=ws.seed + 1000 * rank)
         r = measure(a, ws, dev, world, cs, xs, hbm_peak, hbm_src, full=False)
         r.pop("_inputs")
+        gc.collect()
         torch.cuda.empty_cache()
         subs[name] = r
     method = {}

@@ -264,12 +264,15 @@ void destroy_all(svx_ctx c) {
   if (c->xs) cudaStreamSynchronize(c->xs);
   for (auto s : c->xs_more) cudaStreamSynchronize(s);
   for (auto* p : c->slot_buf) cudaFree(p);
-  for (auto e : c->fork_ev) cudaEventDestroy(e);
+  for (auto e : c->fork_ev)
+    if (e) cudaEventDestroy(e);
   for (auto& v : c->join_ev)
     for (auto e : v) cudaEventDestroy(e);
   for (auto s : c->xs_more) cudaStreamDestroy(s);
-  for (auto e : c->slot_ready) cudaEventDestroy(e);
-  for (auto e : c->slot_free) cudaEventDestroy(e);
+  for (auto e : c->slot_ready)
+    if (e) cudaEventDestroy(e);
+  for (auto e : c->slot_free)
+    if (e) cudaEventDestroy(e);
   for (auto& pe : c->ev_push) {
     cudaEventDestroy(pe.copy0); cudaEventDestroy(pe.copy1); cudaEventDestroy(pe.k0); cudaEventDestroy(pe.k1);
   }
@@ -411,13 +414,12 @@ svx_status svx_create(const svx_config* cfg, svx_ctx* out) {
       return bail(SVX_ERR_OOM, "staging slot allocation failed");
     }
     c->slot_buf.push_back(static_cast<__nv_bfloat16*>(p));
-    cudaEvent_t a = make_event(false), b = make_event(false);
-    if (!a || !b) return bail(SVX_ERR_CUDA, "event creation failed");
-    c->slot_ready.push_back(a);
-    c->slot_free.push_back(b);
-    cudaEvent_t f = make_event(false);
-    if (!f) return bail(SVX_ERR_CUDA, "event creation failed");
-    c->fork_ev.push_back(f);
+    // each event joins the context before it is checked, so a failure frees the ones already made
+    c->slot_ready.push_back(make_event(false));
+    c->slot_free.push_back(make_event(false));
+    c->fork_ev.push_back(make_event(false));
+    if (!c->slot_ready.back() || !c->slot_free.back() || !c->fork_ev.back())
+      return bail(SVX_ERR_CUDA, "event creation failed");
     c->join_ev.emplace_back();
     for (size_t i = 0; i < c->xs_more.size(); ++i) {
       cudaEvent_t j = make_event(false);
