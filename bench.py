@@ -89,6 +89,8 @@ def parse_args(argv=None):
     ap.add_argument("--resident-chunk", default="whole", choices=["whole", "plan"],
                     help="device-resident history pushed as one part per request, or in the plan's chunks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-method", dest="method", action="store_false",
+                    help="skip the method sub-records (dynamic width, tiering)")
     ap.add_argument("--profile-in-place", action="store_true",
                     help="only the e2e context's in-place steps (inputs, then --warmup and --steps steps), for a "
                          "profiler to capture its launches; prints their mean step time")
@@ -727,7 +729,10 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
             v_res.round_finish(ly["o_d"], ly["lse_d"])
 
     R.timed(resident_step_events, steps, 1, between=kern_ev.clear)
-    kern = [(e[0].elapsed_time(e[1]), toks) for e, toks in kern_ev]
+    # The timed region starts on an idle GPU, so the first launch's interval also holds the host's time to
+    # submit it; from the second on, the host runs ahead and each interval is the launch alone.
+    per_step = len(kern_ev) // steps
+    kern = [(e[0].elapsed_time(e[1]), toks) for e, toks in kern_ev[per_step if steps > 1 else 0:]]
     k1_ms = statistics.mean(k for k, _ in kern)
     k1_bytes = statistics.mean(t for _, t in kern) * row_bytes * 2
     # the same step captured once in a CUDA graph and replayed: the shapes are fixed, so the host cost of
@@ -1204,7 +1209,7 @@ def main(argv=None):
         torch.cuda.empty_cache()
         subs[name] = r
     method = {}
-    for key, fn in (("dynamic_width", measure_width), ("tiering", measure_tiering)):
+    for key, fn in ((("dynamic_width", measure_width), ("tiering", measure_tiering)) if a.method else ()):
         try:
             method[key] = fn(a, dev, world, cs, xs)
         except Exception as e:  # a failing sub-record is reported, not silently dropped

@@ -711,6 +711,11 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       const int64_t qrow0 =
           (static_cast<int64_t>(b) * P.n_q_heads + static_cast<int64_t>(head) * P.group) * P.n_query;
 
+      // this segment's state slot rows; their headers (written by earlier launches of the round, or stale)
+      // are fetched now and read back at the segment's end (~1 us off the launch's tail)
+      const int slot = P.slot_base + sg.slot;
+      const int64_t srow0 = static_cast<int64_t>(slot) * P.slot_stride + qrow0 + r0;
+      if (tid < nr) cp_async16(hdr_s + static_cast<uint32_t>(tid) * 16u, P.ws_h + srow0 + tid, 16);
       if (!q_loaded) load_q(x);
       q_loaded = false;
       if (q4 == 0) mref[lane] = -INFINITY;
@@ -843,9 +848,6 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       if (ok && prev >= 0) {
         // this warpgroup's segment state (m = mref, l = sum over threads, a = acc), merged into the
         // slot's state when that is from this round (an earlier launch of the round)
-        const int slot = P.slot_base + sg.slot;
-        const int64_t srow0 = static_cast<int64_t>(slot) * P.slot_stride + qrow0 + r0;
-        if (tid < nr) cp_async16(hdr_s + static_cast<uint32_t>(tid) * 16u, P.ws_h + srow0 + tid, 16);
 #pragma unroll
         for (int j = 0; j < 2 * NK; ++j) {
           float v = lsum[j];
