@@ -59,3 +59,32 @@ def test_step_overlap_takes_the_union_of_transfers_inside_each_step():
     (t0, b0), (t1, b1) = so
     assert abs(t0 - 4.7) < 1e-9 and abs(b0 - 3.5) < 1e-9  # [0, 2] and the in-place kernel [2.5, 4]
     assert abs(t1 - 4.7) < 1e-9 and abs(b1 - 3.9) < 1e-9  # [10, 12] and [12.1, 14]
+
+
+def test_default_run_records_and_profiling_switches():
+    a = bench.parse_args([])
+    assert a.workload == "fulldepth" and a.method and a.draft_load
+    assert [n for n in a.sub_workloads.split(",")] == ["tiny", "qwen3", "internlm", "tree"]
+    assert set(a.tp_sub_workloads.split(",")) == {"qwen3", "internlm", "tree"}
+    p = bench.parse_args(["--no-method", "--no-draft-load", "--sub-workloads="])
+    assert not p.method and not p.draft_load and p.sub_workloads == ""
+
+
+def test_code_digest_ignores_comments_only():
+    import tempfile
+    with tempfile.TemporaryDirectory() as d:
+        f1, f2, f3 = (os.path.join(d, n) for n in ("a.cu", "b.cu", "c.cu"))
+        open(f1, "w").write("int x = 1;  // one\n\n// note\nint y = 2;\n")
+        open(f2, "w").write("int x = 1;\nint y = 2;   // two\n")
+        open(f3, "w").write("int x = 1;\nint y = 3;\n")
+        assert bench.code_digest(f1) == bench.code_digest(f2)
+        assert bench.code_digest(f1) != bench.code_digest(f3)
+
+
+def test_committed_traffic_summary_matches_the_kernel_source():
+    """The DRAM-traffic summary under profiles/ was taken on the chunk kernel as it is: the benchmark
+    reports its figures as roofline.traffic only then."""
+    for name, d in (("fulldepth", 128), ("qwen3", 128), ("internlm", 128), ("tree", 128), ("qwen3", 64),
+                    ("internlm", 64), ("tree", 64)):
+        t = bench.profiled_traffic(W.named(name).with_(head_dim=d))
+        assert t is not None and t > 0, (name, d)
