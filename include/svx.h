@@ -175,7 +175,11 @@ svx_status svx_candidate_attn(svx_ctx ctx, const void* k_dev, const void* v_dev,
  * gave up (2 s) in this round or in any round since the last finish with timeout_ms > 0: the
  * context's device error word keeps an expiry until such a finish reads it, reports it and clears
  * it.  The outputs of the round whose kernel gave up are invalid.  The context is ready for the
- * next round either way; its work is stream-ordered after this round's. */
+ * next round either way; its work is stream-ordered after this round's.  In the bounds-checked
+ * library (libsvx_checked.so, built with -DSVX_BOUNDS_CHECK; the pages have no counterpart) every
+ * kernel also checks that its global reads and writes lie in the buffers its launch describes, skips
+ * one that does not and raises the same word (bit 4, and bit 8 + the site), which this call then
+ * reports the same way. */
 svx_status svx_round_finish(svx_ctx ctx, void* o_dev, float* lse_dev, int32_t timeout_ms);
 
 /* Test hook of the failure path (the pages have no counterpart).  Enqueues on the compute stream,
@@ -356,7 +360,8 @@ svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_t n_kv_head
 
 /* Reads and clears the static scratch's device error word on the calling thread's current device:
  * *expired = 1 if a kernel of some svx_verify_static call since the last check gave up a bounded
- * wait (2 s; that call's outputs are invalid), else 0.  Waits for all work on the device
+ * wait (2 s; that call's outputs are invalid), or, in the bounds-checked library, skipped an access
+ * outside its buffers, else 0.  Waits for all work on the device
  * (cudaDeviceSynchronize), so call it outside latency-critical loops and outside stream capture.
  * Allocates nothing.  Errors: SVX_ERR_INVALID_ARG, _CUDA; message from svx_last_error(NULL). */
 svx_status svx_static_check(int32_t* expired);

@@ -40,6 +40,47 @@ cudaError_t launch_pdl(void (*kernel)(Params), dim3 grid, dim3 block, size_t sme
 }
 
 
+// Device error word bits.  Kernels only ever set bits (atomicOr); the host reads and clears the word.
+constexpr int kErrWait = 1;     // a bounded wait of the tensor-core chunk kernel gave up
+constexpr int kErrExpire = 2;   // the expire-wait test hook's bounded wait ran out
+constexpr int kErrBounds = 4;   // bounds-checked build: an access outside its buffer was skipped;
+                                // bit 8 + site names where (BoundsSite)
+
+// Bounds-checked build (-DSVX_BOUNDS_CHECK, libsvx_checked.so): each kernel checks that the global
+// ranges it reads and writes lie in the buffers its parameters describe, and skips an access that
+// does not (a load reads nothing, a store is dropped) after raising kErrBounds.  The stand-in for a
+// memory checker on GPUs where none may run.  In the normal build the checks compile away.
+#if defined(SVX_BOUNDS_CHECK)
+constexpr bool kBoundsChecked = true;
+#else
+constexpr bool kBoundsChecked = false;
+#endif
+enum BoundsSite : int {
+  kSiteTcKV = 0,    // tensor-core chunk kernel: K/V tile rows of a part
+  kSiteTcQ = 1,     // tensor-core chunk kernel: Q rows
+  kSiteTcState = 2, // tensor-core chunk kernel: state-slot rows
+  kSiteFmaKV = 3,   // FMA chunk kernel: K/V rows
+  kSiteFmaQ = 4,    // FMA chunk kernel: Q rows
+  kSiteFmaState = 5,
+  kSiteFinState = 6,  // finish kernel: state-slot rows
+  kSiteFinIn = 7,     // finish kernel: Q and candidate K/V
+  kSiteFinOut = 8,    // finish kernel: O and LSE
+};
+
+// True when [p, p + n) lies inside [base, base + extent) (element counts); in the checked build a
+// false result raises kErrBounds with the site's bit.
+template <typename T>
+__device__ __forceinline__ bool in_bounds(const T* p, int64_t n, const T* base, int64_t extent, int* err,
+                                          int site) {
+  if constexpr (!kBoundsChecked) {
+    return true;
+  } else {
+    const bool ok = base != nullptr && n >= 0 && p >= base && p + n <= base + extent;
+    if (!ok) atomicOr(err, kErrBounds | (1 << (8 + site)));
+    return ok;
+  }
+}
+
 constexpr int kMaxReq = 256;
 constexpr int kMaxPartsPerLaunch = 64;  // keeps the kernel parameter block near 2.5 KiB
 constexpr int kHistSlots = 8;           // state slots per query row (history segments)
@@ -68,8 +109,9 @@ struct ChunkParams {
   const __nv_bfloat16* q;  // [B][Hq][nq][d]
   RowState* ws_h;          // [slots][slot_stride]
   float* ws_a;             // [slots][slot_stride][d]
-  int* err;                // device error word (bounded waits that gave up)
+  int* err;                // device error word (bounded waits that gave up, checked-build bounds)
   int64_t slot_stride;     // state rows per slot (max_req * Hq * max_query)
+  int64_t q_rows;          // rows of q: n_req * Hq * nq (the bounds-checked build's extent of q)
   int64_t total_tiles;     // tensor-core kernel: tiles of one CTA group (all parts, one head and row block)
   float q_scale;           // softmax scale * log2(e)
   uint32_t epoch;          // this round
@@ -92,6 +134,7 @@ struct ChunkParams {
 struct FinishParams {
   RowState* ws_h;  // headers are read, then marked unwritten (epoch 0)
   const float* ws_a;
+  int* err;        // device error word (checked-build bounds)
   int64_t slot_stride;
   __nv_bfloat16* o;              // [B][Hq][nq][d]
   float* lse;                    // [B][Hq][nq]

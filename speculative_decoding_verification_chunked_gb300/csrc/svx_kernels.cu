@@ -102,8 +102,11 @@ __global__ void __launch_bounds__(128) chunk_attn_fma(const __grid_constant__ Ch
     for (int c = threadIdx.x; c < TILE * CPR; c += 128) {
       const int t = c / CPR, cc = c % CPR;
       const int64_t tok = t0 + t;
-      const bool ok = tok < n_tok;
-      const int64_t off = ok ? tok * kv_stride + static_cast<int64_t>(g) * D + cc * 8 : 0;
+      int64_t off = tok * kv_stride + static_cast<int64_t>(g) * D + cc * 8;
+      // (checked build) a row past the part, or a piece outside it, reads nothing
+      const bool ok = tok < n_tok && in_bounds(part.k + off, 8, part.k, n_tok * kv_stride, P.err, kSiteFmaKV) &&
+                      in_bounds(part.v + off, 8, part.v, n_tok * kv_stride, P.err, kSiteFmaKV);
+      if (!ok) off = 0;
       cp_async16(sK + (buf * TILE + t) * KSTR + cc * 8, part.k + off, ok ? 16 : 0);
       cp_async16(sV + (buf * TILE + t) * D + cc * 8, part.v + off, ok ? 16 : 0);
     }
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(128) chunk_attn_fma(const __grid_constant__ Ch
   for (int i = threadIdx.x; i < kRowsPerBlock * D / 2; i += 128) {
     const int rr = (2 * i) / D, c = (2 * i) % D;
     float2 qv = make_float2(0.f, 0.f);
-    if (rr < nr) {
+    if (rr < nr && in_bounds(P.q + (row_base + r0 + rr) * D + c, 2, P.q, P.q_rows * D, P.err, kSiteFmaQ)) {
       const uint32_t w = *reinterpret_cast<const uint32_t*>(P.q + (row_base + r0 + rr) * D + c);
       qv = make_float2(bf16_lo(w) * P.q_scale, bf16_hi(w) * P.q_scale);
     }
@@ -223,6 +226,7 @@ __global__ void __launch_bounds__(128) chunk_attn_fma(const __grid_constant__ Ch
     if (i < nrw) {
       const int rr = warp + 4 * i;
       const float lt = warp_sum(l[i]);
+      if (!in_bounds(P.ws_h + slot_row0 + rr, 1, P.ws_h, kHistSlots * P.slot_stride, P.err, kSiteFmaState)) continue;
       RowState* hp = P.ws_h + slot_row0 + rr;
       float* ap = P.ws_a + (slot_row0 + rr) * D + lane * VPL;
       const RowState old = *hp;
@@ -286,7 +290,9 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const __grid_con
 #pragma unroll
   for (int s = 0; s < kHistSlots; ++s) {
     hs[s] = RowState{kNegInf, 0.f, 0u, 0u};
-    if ((smask >> s) & 1u) {
+    if (((smask >> s) & 1u) &&
+        in_bounds(P.ws_h + static_cast<int64_t>(s) * P.slot_stride + row, 1, P.ws_h, kHistSlots * P.slot_stride,
+                  P.err, kSiteFinState)) {
       const int64_t idx = static_cast<int64_t>(s) * P.slot_stride + row;
       hs[s] = P.ws_h[idx];
       const float* ap = P.ws_a + idx * D + lane * VPL;
@@ -312,8 +318,9 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const __grid_con
     }
     float q[VPL];
     const __nv_bfloat16* qp = P.q + row * D + lane * VPL;
+    const bool q_ok = in_bounds(qp, VPL, P.q, n_rows * D, P.err, kSiteFinIn);
 #pragma unroll
-    for (int c = 0; c < VPL; ++c) q[c] = __bfloat162float(qp[c]) * P.q_scale;
+    for (int c = 0; c < VPL; ++c) q[c] = q_ok ? __bfloat162float(qp[c]) * P.q_scale : 0.f;
     const int g = h / P.group;
     // visible candidates in batches of kCandBatch: all their K and V loads are issued first, so a
     // batch costs one memory round trip instead of one per candidate
@@ -333,8 +340,13 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const __grid_con
       float kk[kCandBatch][VPL], vv[kCandBatch][VPL];
 #pragma unroll
       for (int t = 0; t < kCandBatch; ++t) {
-        if (idx[t] >= 0) {
-          const int64_t kv = ((static_cast<int64_t>(b) * P.n_cand + idx[t]) * P.n_kv_heads + g) * D + lane * VPL;
+        const int64_t kv_ext = static_cast<int64_t>(P.n_req) * P.n_cand * P.n_kv_heads * D;
+        const int64_t kv = ((static_cast<int64_t>(b) * P.n_cand + max(idx[t], 0)) * P.n_kv_heads + g) * D + lane * VPL;
+        if (idx[t] >= 0 && !(in_bounds(P.k_cand + kv, VPL, P.k_cand, kv_ext, P.err, kSiteFinIn) &&
+                             in_bounds(P.v_cand + kv, VPL, P.v_cand, kv_ext, P.err, kSiteFinIn))) {
+#pragma unroll
+          for (int c = 0; c < VPL; ++c) kk[t][c] = vv[t][c] = 0.f;
+        } else if (idx[t] >= 0) {
 #pragma unroll
           for (int c = 0; c < VPL; ++c) {
             kk[t][c] = __bfloat162float(P.k_cand[kv + c]);
@@ -380,10 +392,13 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const __grid_con
     while (used) {
       const int s = __ffs(used) - 1;
       used &= used - 1;
-      P.ws_h[static_cast<int64_t>(s) * P.slot_stride + row].epoch = 0u;
+      P.ws_h[static_cast<int64_t>(s) * P.slot_stride + row].epoch = 0u;  // read above: in bounds
     }
   }
   __nv_bfloat16* op = P.o + row * D + lane * VPL;
+  if (!(in_bounds(op, VPL, P.o, n_rows * D, P.err, kSiteFinOut) &&
+        in_bounds(P.lse + row, 1, P.lse, n_rows, P.err, kSiteFinOut)))
+    return;
   if (l > 0.f) {
     const float inv = 1.f / l;
 #pragma unroll
@@ -421,7 +436,7 @@ cudaError_t launch_chunk_attn(const ChunkParams& p, int head_dim, cudaStream_t s
 
 namespace {
 // A bounded wait on an mbarrier phase that nothing completes: it runs out after limit_ns of global
-// time and raises the device error word (bit 2), the way a chunk kernel's waits end when their
+// time and raises the device error word (kErrExpire), the way a chunk kernel's waits end when their
 // producer never delivers.  Test hook of the failure path; one thread, no fault.
 __global__ void expire_wait_kernel(int* err, uint64_t limit_ns) {
   __shared__ __align__(8) unsigned long long bar;
@@ -441,7 +456,7 @@ __global__ void expire_wait_kernel(int* err, uint64_t limit_ns) {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     if (t - t0 > limit_ns) {
-      atomicOr(err, 2);
+      atomicOr(err, kErrExpire);
       return;
     }
   }

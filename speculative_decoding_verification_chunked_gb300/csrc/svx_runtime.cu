@@ -528,6 +528,7 @@ svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, int cta_cap) {
     p.ws_a = c->ws_a;
     p.err = c->d_err;
     p.slot_stride = c->slot_stride;
+    p.q_rows = static_cast<int64_t>(c->n_req) * c->cfg.n_q_heads * c->n_query;
     p.q_scale = c->q_scale;
     p.epoch = c->epoch;
     p.n_q_heads = c->cfg.n_q_heads;
@@ -934,6 +935,7 @@ svx_status svx_round_finish(svx_ctx c, void* o_dev, float* lse_dev, int32_t time
   std::memset(&p, 0, sizeof(p));
   p.ws_h = c->ws_h;
   p.ws_a = c->ws_a;
+  p.err = c->d_err;
   p.slot_stride = c->slot_stride;
   p.epoch = c->epoch;
   p.o = static_cast<__nv_bfloat16*>(o_dev);
@@ -985,7 +987,10 @@ svx_status svx_round_finish(svx_ctx c, void* o_dev, float* lse_dev, int32_t time
         SVX_CUDA(c, cudaMemcpy(&dev_err, c->d_err, sizeof(int), cudaMemcpyDeviceToHost));
         if (dev_err) {  // the round's outputs are invalid; the word is cleared, so the context runs on
           SVX_CUDA(c, cudaMemset(c->d_err, 0, sizeof(int)));
-          return fail(c, SVX_ERR_CUDA, "a kernel gave up waiting (device error word %d)", dev_err);
+          return fail(c, SVX_ERR_CUDA, "%s (device error word 0x%x)",
+                      (dev_err & svx::kErrBounds) ? "a kernel skipped an access outside its buffers (checked build)"
+                                                  : "a kernel gave up waiting",
+                      dev_err);
         }
         break;
       }

@@ -153,6 +153,7 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
   p.ws_a = ws_a;
   p.err = d_err;
   p.slot_stride = rows;
+  p.q_rows = rows;
   p.q_scale = sc * 1.4426950408889634f;
   p.epoch = sd.epoch;
   p.n_q_heads = n_q_heads;
@@ -206,6 +207,7 @@ extern "C" svx_status svx_verify_static(int32_t n_req, int32_t n_q_heads, int32_
   std::memset(&f, 0, sizeof(f));
   f.ws_h = ws_h;
   f.ws_a = ws_a;
+  f.err = d_err;
   f.slot_stride = rows;
   f.o = static_cast<__nv_bfloat16*>(o_dev);
   f.lse = lse_dev;

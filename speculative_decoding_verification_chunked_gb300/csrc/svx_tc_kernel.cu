@@ -352,7 +352,7 @@ struct Waiter {
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
       if (global_ns() - t0 > kWaitLimitNs) {
-        atomicOr(err, 1);
+        atomicOr(err, kErrWait);
         return;
       }
   }
@@ -366,7 +366,7 @@ struct Waiter {
         if (*abort) return false;
         if (global_ns() - t0 > kWaitLimitNs) {
           *abort = 1u;
-          atomicOr(err, 1);
+          atomicOr(err, kErrWait);
           return false;
         }
       }
@@ -468,7 +468,8 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       const PartDesc& pd = P.parts[sg.part];
       const int64_t n_tok = pd.n_tok;
       // a group's head (or, for head pairs, pair p: heads 2p and 2p + 1, dimensions 128p .. 128p + 127)
-      const __nv_bfloat16* src = (is_v ? pd.v : pd.k) + static_cast<int64_t>(sg.g) * TD;
+      const __nv_bfloat16* const kv_base = is_v ? pd.v : pd.k;
+      const __nv_bfloat16* src = kv_base + static_cast<int64_t>(sg.g) * TD;
       for (int64_t t = 0; t < sg.n_tiles; ++t, ++i) {
         const int slot = static_cast<int>(i % nst);
         const uint32_t use = static_cast<uint32_t>(i / nst);
@@ -482,7 +483,11 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
         // r0 + RPI*j (j < TOK/RPI); rows past n_tok read nothing
         constexpr int PC = TD / 8, RPI = 32 / PC;
         const int c = lane % PC, r0 = lane / PC;
-        const int64_t valid_rows = (n_tok - tok0 < TOK) ? (n_tok - tok0) : static_cast<int64_t>(TOK);
+        int64_t valid_rows = (n_tok - tok0 < TOK) ? (n_tok - tok0) : static_cast<int64_t>(TOK);
+        // (checked build) the tile's rows of this head lie in the part; else nothing is read
+        if (!in_bounds(src + tok0 * kv_stride, (valid_rows - 1) * kv_stride + TD, kv_base, n_tok * kv_stride, P.err,
+                       kSiteTcKV))
+          valid_rows = 0;
         const __nv_bfloat16* ps = src + (tok0 + r0) * kv_stride + c * 8;
         const int64_t step = RPI * kv_stride;
         const uint32_t so0 = static_cast<uint32_t>(c >> 3) * HALF_BYTES + static_cast<uint32_t>(r0) * 128u;
@@ -592,7 +597,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
             t_idle = now;
           } else if (now - t_idle > kWaitLimitNs) {
             *W.abort = 1u;
-            atomicOr(W.err, 1);
+            atomicOr(W.err, kErrWait);
             break;
           }
         }
@@ -669,9 +674,10 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
     auto load_q = [&](int64_t xq) {
       const Seg sq = seg_at(P, split, grp, xq, x_end, hint_q);
       if constexpr (PAIR) {
-        const int nrows = min(NCOL, P.group * P.n_query);
+        int nrows = min(NCOL, P.group * P.n_query);
         const int64_t qrow0 = (static_cast<int64_t>(P.parts[sq.part].req) * P.n_q_heads +
                                static_cast<int64_t>(2 * sq.g + wg) * P.group) * P.n_query;
+        if (!in_bounds(P.q + qrow0 * DH, static_cast<int64_t>(nrows) * DH, P.q, P.q_rows * DH, P.err, kSiteTcQ)) nrows = 0;
 #pragma unroll
         for (int idx = tid; idx < NCOL * (TILE_D / 8); idx += 128) {
           const int r = idx / (TILE_D / 8), ch = idx % (TILE_D / 8);
@@ -681,9 +687,10 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
         }
       } else {
         const int rblk = sq.rb * C::ROWS;
-        const int nrows = min(C::ROWS, P.group * P.n_query - rblk);
+        int nrows = min(C::ROWS, P.group * P.n_query - rblk);
         const int64_t qrow0 = (static_cast<int64_t>(P.parts[sq.part].req) * P.n_q_heads +
                                static_cast<int64_t>(sq.g) * P.group) * P.n_query + rblk;
+        if (!in_bounds(P.q + qrow0 * DH, static_cast<int64_t>(nrows) * DH, P.q, P.q_rows * DH, P.err, kSiteTcQ)) nrows = 0;
 #pragma unroll
         for (int idx = tid; idx < NCOL * (DH / 8); idx += 128) {
           const int c = wg * NCOL + idx / (DH / 8), ch = idx % (DH / 8);
@@ -715,7 +722,9 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
       // are fetched now and read back at the segment's end (~1 us off the launch's tail)
       const int slot = P.slot_base + sg.slot;
       const int64_t srow0 = static_cast<int64_t>(slot) * P.slot_stride + qrow0 + r0;
-      if (tid < nr) cp_async16(hdr_s + static_cast<uint32_t>(tid) * 16u, P.ws_h + srow0 + tid, 16);
+      // (checked build) this warpgroup's state rows lie in the workspace; else they are neither read nor written
+      const bool st_ok = in_bounds(P.ws_h + srow0, nr, P.ws_h, kHistSlots * P.slot_stride, P.err, kSiteTcState);
+      if (tid < nr && st_ok) cp_async16(hdr_s + static_cast<uint32_t>(tid) * 16u, P.ws_h + srow0 + tid, 16);
       if (!q_loaded) load_q(x);
       q_loaded = false;
       if (q4 == 0) mref[lane] = -INFINITY;
@@ -845,7 +854,7 @@ __global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1) chunk_attn_tc(const _
         prev = i;
       }
       if (ok && prev >= 0) ok = accumulate(prev);
-      if (ok && prev >= 0) {
+      if (ok && prev >= 0 && st_ok) {
         // this warpgroup's segment state (m = mref, l = sum over threads, a = acc), merged into the
         // slot's state when that is from this round (an earlier launch of the round)
 #pragma unroll

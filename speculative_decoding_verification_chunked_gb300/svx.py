@@ -13,7 +13,11 @@ from typing import Optional, Sequence
 
 import numpy as np
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsvx.so")
+# SVX_LIBRARY=checked loads the bounds-checked build (libsvx_checked.so) instead of libsvx.so.
+_LIB_NAME = {"": "libsvx.so", "checked": "libsvx_checked.so"}.get(os.environ.get("SVX_LIBRARY", ""))
+if _LIB_NAME is None:
+    raise ImportError(f"SVX_LIBRARY={os.environ['SVX_LIBRARY']!r}: expected unset or 'checked'")
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), _LIB_NAME)
 
 OK, ERR_INVALID_ARG, ERR_BAD_STATE, ERR_OOM, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = range(7)
 STATUS_NAMES = {0: "SVX_OK", 1: "SVX_ERR_INVALID_ARG", 2: "SVX_ERR_BAD_STATE", 3: "SVX_ERR_OOM",
