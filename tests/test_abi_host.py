@@ -17,7 +17,7 @@ HEADER = os.path.join(ROOT, "include", "svx.h")
 @pytest.fixture(scope="module")
 def svx():
     from speculative_decoding_verification_chunked_gb300 import build
-    if not os.path.exists(build.LIB):
+    if not (os.path.exists(build.LIB) and os.path.exists(build.LIB_CHECKED)):
         build.build()
     from speculative_decoding_verification_chunked_gb300 import svx as mod
     return mod
@@ -36,6 +36,19 @@ def test_library_exports_every_declared_symbol(svx):
         assert hasattr(svx.lib, n), n
     assert sorted(svx.SYMBOLS) == names
     assert "sm_103a" in svx.version()
+
+
+def test_bounds_checked_library_exports_the_same_symbols(svx):
+    """libsvx_checked.so (the bounds-checked build) is a drop-in for libsvx.so: same ABI."""
+    import ctypes
+    from speculative_decoding_verification_chunked_gb300 import build
+    checked = ctypes.CDLL(build.LIB_CHECKED)
+    for n in header_functions():
+        assert hasattr(checked, n), n
+    sizes = (ctypes.c_int64 * 16)()
+    checked.svx_abi_sizes.restype = ctypes.c_int32
+    n = checked.svx_abi_sizes(sizes, 16)
+    assert list(sizes[:n]) == list(svx.abi_sizes().values())
 
 
 def test_plan_matches_oracle_on_named_workloads(svx):
