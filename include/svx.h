@@ -119,7 +119,7 @@ typedef struct {
  * copy engine slowed by half beside a co-running GEMM while in-place reads did not.  With this flag the
  * context times its pushes' transfers (CUDA events around each push's copies, or around the chunk kernel
  * of a push read in place; read without waiting once they have completed) and keeps each engine's
- * recent ms per GB (decayed sums of time and bytes over about the last 100 pushes).  The engine is chosen per round, when it begins, so no round mixes them:
+ * recent ms per GB (decayed sums of time and bytes over about the last 500 pushes).  The engine is chosen per round, when it begins, so no round mixes them:
  * round 0 is staged and round 1 read in place (each engine measured once); after that, rounds are
  * staged through the copy engine unless in-place reads on zero_copy_ctas SMs were measured 10% faster
  * per byte (and then read in place until the copy engine is measured 5% faster than them), and one whole round

@@ -44,7 +44,10 @@ struct PushEvents {
 // Adaptive streaming (SVX_FLAG_ADAPTIVE): the context measures both transfer engines on its own pushes
 // and uses the faster one.
 constexpr int kRateRing = 4096;      // pushes whose transfer time is still to be read
-constexpr double kAdaptDecay = 0.99;     // per-sample decay of the time and byte sums (~100 pushes)
+// Per-sample decay of the time and byte sums: ~500 pushes, a whole multi-layer step.  The copy engine's
+// rate can differ from one host buffer (layer) to the next; a memory of a few layers made the choice
+// follow single layers and flip back and forth.
+constexpr double kAdaptDecay = 0.998;
 constexpr double kAdaptMargin = 0.10;   // in-place reads must be this much faster to replace the copy engine
 constexpr double kAdaptBack = 0.05;     // and the copy engine this much faster than them to come back
 constexpr int64_t kExploreFirst = 8;    // rounds between two measurements of the other engine, at first
