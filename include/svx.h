@@ -207,6 +207,14 @@ svx_status svx_debug_expire_wait(svx_ctx ctx, int32_t wait_ms);
 svx_status svx_debug_fail_copy(svx_ctx ctx, int64_t nth);
 svx_status svx_debug_delay_copy(svx_ctx ctx, int64_t nth, int32_t delay_ms);
 
+/* Test hook of the bounds-checked library (the pages have no counterpart).  From the next chunk launch
+ * on, until svx_round_finish, the launches describe q as holding at most `rows` rows (rows < 0: the real
+ * count again).  The real buffer is larger, so no access ever leaves it: in libsvx_checked.so the chunk
+ * kernel skips its q loads past `rows` and raises the device error word, which svx_round_finish
+ * (timeout_ms > 0) reports as SVX_ERR_CUDA; in libsvx.so the checks do not exist and the round is
+ * unchanged.  It shows that the checked build's checks run and are reported. */
+svx_status svx_debug_clip_q_rows(svx_ctx ctx, int64_t rows);
+
 /* Message for the last failing call on ctx (never NULL; "" if none).  NULL ctx: last failure of
  * svx_create or svx_verify_static on this thread. */
 const char* svx_last_error(svx_ctx ctx);

@@ -150,6 +150,7 @@ struct svx_ctx_s {
   // host-side fault injection (test hooks): copy submissions counted from the arming call
   int64_t copy_seq = 0, fail_at = 0, delay_at = 0;
   int32_t delay_ms = 0;
+  int64_t clip_q_rows = -1;  // the q extent the chunk launches state (< 0: the real one)
 
   std::string err;
 };
@@ -341,7 +342,11 @@ uint32_t nonempty_splits(int64_t n_tok, int splits) {
 
 extern "C" {
 
+#if defined(SVX_BOUNDS_CHECK)
+const char* svx_version(void) { return "svx 0.2.0 (sm_103a, bounds-checked)"; }
+#else
 const char* svx_version(void) { return "svx 0.2.0 (sm_103a)"; }
+#endif
 
 int32_t svx_abi_sizes(int64_t* out, int32_t cap) {
   const int64_t sz[] = {static_cast<int64_t>(sizeof(svx_config)),     static_cast<int64_t>(sizeof(svx_part)),
@@ -532,6 +537,7 @@ svx_status launch_parts(svx_ctx c, std::vector<PartDesc>& parts, int cta_cap) {
     p.err = c->d_err;
     p.slot_stride = c->slot_stride;
     p.q_rows = static_cast<int64_t>(c->n_req) * c->cfg.n_q_heads * c->n_query;
+    if (c->clip_q_rows >= 0) p.q_rows = std::min(p.q_rows, c->clip_q_rows);
     p.q_scale = c->q_scale;
     p.epoch = c->epoch;
     p.n_q_heads = c->cfg.n_q_heads;
@@ -959,6 +965,7 @@ svx_status svx_round_finish(svx_ctx c, void* o_dev, float* lse_dev, int32_t time
   for (int b = 0; b < c->n_req; ++b) p.slot_mask[b] = c->slot_mask[static_cast<size_t>(b)];
   const bool timing = (c->cfg.flags & SVX_FLAG_TIMING) != 0;
   c->state = RoundState::kIdle;
+  c->clip_q_rows = -1;
   const RoundEvents* re = timing ? &c->ev_round[static_cast<size_t>(c->n_round)] : nullptr;
   if (re) SVX_CUDA(c, cudaEventRecord(re->f0, c->cs));
   SVX_CUDA(c, svx::launch_finish(p, c->cfg.head_dim, c->cs));
@@ -1266,6 +1273,12 @@ svx_status svx_adaptive_state(svx_ctx c, double* ce_ms_per_gb, double* ip_ms_per
 svx_status svx_debug_fail_copy(svx_ctx c, int64_t nth) {
   if (!c || nth < 0) return SVX_ERR_INVALID_ARG;
   c->fail_at = nth > 0 ? c->copy_seq + nth : 0;
+  return SVX_OK;
+}
+
+svx_status svx_debug_clip_q_rows(svx_ctx c, int64_t rows) {
+  if (!c) return SVX_ERR_INVALID_ARG;
+  c->clip_q_rows = rows < 0 ? -1 : rows;
   return SVX_OK;
 }
 

@@ -117,6 +117,7 @@ _SIGS = {
     "svx_debug_expire_wait": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     "svx_debug_fail_copy": (ctypes.c_int, [_P, ctypes.c_int64]),
     "svx_debug_delay_copy": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int32]),
+    "svx_debug_clip_q_rows": (ctypes.c_int, [_P, ctypes.c_int64]),
     "svx_plan_tc": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
                                    ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32),
                                    ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64),
@@ -614,6 +615,11 @@ class Verifier:
     def debug_delay_copy(self, nth: int, delay_ms: int):
         """Test hook: the host sleeps delay_ms before the nth copy submission from now (0 disarms)."""
         self._check(lib.svx_debug_delay_copy(self._h, nth, delay_ms))
+
+    def debug_clip_q_rows(self, rows: int):
+        """Test hook of the bounds-checked build: the chunk launches until round_finish state that q has at
+        most `rows` rows (< 0: the real count)."""
+        self._check(lib.svx_debug_clip_q_rows(self._h, rows))
 
     def stats(self) -> dict:
         s = Stats()

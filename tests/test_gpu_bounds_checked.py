@@ -7,6 +7,7 @@ the device error word.  Every round of the parity tests ends with svx_round_fini
 every no-allocation round with svx_static_check, which report a raised word as an error; so these tests
 passing on the checked library means no kernel computed an address outside its buffers on any of their
 shapes (ragged tails, trees, d = 64 head pairs, more than 2^31 elements, full-size sampled rounds).
+tests/test_gpu_bounds_hook.py, run here too, shows that the checks fire and are reported.
 """
 import os
 import subprocess
@@ -30,7 +31,8 @@ def test_parity_suite_on_the_bounds_checked_library():
                             "print(svx._LIB_PATH)"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert probe.returncode == 0 and probe.stdout.strip().endswith("libsvx_checked.so"), probe.stdout + probe.stderr
     cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
-           "tests/test_gpu_parity.py", "tests/test_gpu_causality.py", "tests/test_zz_no_alloc.py"]
+           "tests/test_gpu_parity.py", "tests/test_gpu_causality.py", "tests/test_gpu_bounds_hook.py",
+           "tests/test_zz_no_alloc.py"]
     r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=2400)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
     assert " passed" in r.stdout and " failed" not in r.stdout
