@@ -641,17 +641,22 @@ def copy_rates(iv, push_bytes):
             "below_150_frac": float((r < 150).mean()), "pushes": int(ok.sum())}
 
 
-def step_overlap(iv, rounds, pushes_per_step: int, layers: int):
+def step_overlap(iv, rounds, layers: int):
     """Per step of a timing window: (T_step, T_transfer) in ms.  T_step runs from the step's first round
-    begin to its last finish-kernel end; T_transfer is the length of the union, inside the step, of its
-    pushes' copy intervals and of the chunk kernels of pushes read in place (no copy interval)."""
-    n_steps = min(len(rounds) // layers, len(iv) // pushes_per_step)
+    begin to its last finish-kernel end; T_transfer is the length of the union, inside the step, of the
+    pushes' copy intervals and of the chunk kernels of pushes read in place (no copy interval).  Steps are
+    separated by the host reading each step's result, so every interval belongs to the step it lies in
+    (an adaptive context launches an in-place round's pushes together, so the number of intervals per
+    step varies)."""
+    iv = np.asarray(iv, dtype=np.float64).reshape(-1, 4)
+    has_copy = np.isfinite(iv[:, 0])
+    ta = np.where(has_copy, iv[:, 0], iv[:, 2])
+    tb = np.where(has_copy, iv[:, 1], iv[:, 3])
     out = []
-    for s in range(n_steps):
+    for s in range(len(rounds) // layers):
         t0, t1 = rounds[s * layers, 0], rounds[(s + 1) * layers - 1, 2]
-        seg = iv[s * pushes_per_step:(s + 1) * pushes_per_step]
-        tr = [(a, b) if np.isfinite(a) else (k0, k1) for a, b, k0, k1 in seg]
-        tr.sort()
+        sel = (tb > t0) & (ta < t1)
+        tr = sorted(zip(ta[sel].tolist(), tb[sel].tolist()))
         busy, cur = 0.0, None
         for a, b in tr:
             a, b = max(a, t0), min(b, t1)
@@ -790,7 +795,7 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
         ms = R.timed(lambda: R.host_step(v, inp, lambda li: pushes[li]), steps, warmup, between=v.window_reset)
         ws = v.window_stats()
         iv = v.window_intervals()
-        so = step_overlap(iv, v.window_rounds(), len(pushes[0]) * L, L)
+        so = step_overlap(iv, v.window_rounds(), L)
         val, ms_job = job_throughput(B * nq, ms, world, dev)
         covered = ws["n_rounds"] / L  # steps in the window (all timed steps unless it filled up)
         per_step = {k: ws[k] / covered for k in ("window_ms", "copy_busy_ms", "copy_gap_ms", "chunk_kernel_ms",
@@ -800,9 +805,14 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
         out = {"value": val, "unit": UNIT, "ms_per_step": ms_job, "what": label,
                "hist_gb_per_s": hist_bytes / (ms / 1e3) / 1e9,
                "per_step_ms": per_step,
-               "in_place_push_frac": ws["n_zero_copy_pushes"] / max(1, ws["n_pushes"]),
+               # rounds read in place (an adaptive context launches an in-place round's pushes together,
+               # so it counts one in-place push per such round)
+               "in_place_round_frac": min(1.0, ws["n_zero_copy_pushes"] / max(1, ws["n_rounds"])),
+               # per-push copy rates when every planned push has its own interval (an adaptive context's
+               # in-place rounds launch their pushes together)
                "copy_rate_gbs": (copy_rates(iv, push_bytes * steps)
-                                 if pushes is stream_pushes and ws["n_rounds"] == steps * L else None),
+                                 if pushes is stream_pushes and ws["n_rounds"] == steps * L
+                                 and len(iv) == len(push_bytes) * steps else None),
                # chunk compute hidden under transfer: the time of chunk kernels over staged parts that lies
                # inside transfer intervals; a kernel that reads host memory in place is the transfer itself
                # (1.0 when every push is read in place)
@@ -952,8 +962,9 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
                 cov = ws["n_rounds"] / L
                 m["co_per_step_ms"] = {k: ws[k] / cov for k in ("copy_busy_ms", "copy_gap_ms", "chunk_kernel_ms",
                                                                 "zero_copy_kernel_ms", "transfer_busy_ms")}
-                m["co_copy_rate_gbs"] = copy_rates(vx.window_intervals(), push_bytes * n) \
-                    if pushes is stream_pushes and ws["n_rounds"] == n * L else None
+                ivx = vx.window_intervals()
+                m["co_copy_rate_gbs"] = copy_rates(ivx, push_bytes * n) \
+                    if pushes is stream_pushes and ws["n_rounds"] == n * L and len(ivx) == len(push_bytes) * n else None
             tp["modes"][name] = m
         # the same steps with Draft steps admitted by the scheduler instead of a free-running Draft (a new
         # scheduler per mode, each against its own baseline timed right before)

@@ -117,9 +117,14 @@ typedef struct {
  * on the host: on GB300 hosts some pinned buffers were read at 5-150 GB/s by the copy engine while SM
  * loads of the same buffers (SVX_FLAG_ZERO_COPY on 32 SMs) held the ~210 GB/s of the host link, and the
  * copy engine slowed by half beside a co-running GEMM while in-place reads did not.  With this flag the
- * context times its pushes' transfers (CUDA events around each push's copies, or around the chunk kernel
- * of a push read in place; read without waiting once they have completed) and keeps each engine's
- * recent ms per GB (decayed sums of time and bytes over about the last 500 pushes).  The engine is chosen per round, when it begins, so no round mixes them:
+ * context times its pushes' transfers (CUDA events around each push's copies, or around the chunk
+ * kernels of a round read in place; read without waiting once they have completed) and keeps each
+ * engine's recent ms per GB (decayed sums of time and bytes over about the last 500 samples).  The engine
+ * is chosen per round, when it begins, so no round mixes them.  A round read in place launches its parts
+ * when svx_round_finish is called: a request's parts that continue one another (next tokens, next rows of
+ * the same buffer) merge into one, and a launch holds at most one part per request, so pushing chunk by
+ * chunk costs one launch per round as a rule; the timing window counts those launches as one push.
+ * Choice:
  * round 0 is staged and round 1 read in place (each engine measured once); after that, rounds are
  * staged through the copy engine unless in-place reads on zero_copy_ctas SMs were measured 10% faster
  * per byte (and then read in place until the copy engine is measured 5% faster than them), and one whole round

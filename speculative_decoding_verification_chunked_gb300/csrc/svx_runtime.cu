@@ -146,6 +146,15 @@ struct svx_ctx_s {
   bool prefer_ip = false;              // the engine the measurements favour
   bool round_ip = false;               // the open round reads its host parts in place
   int n_zc_push = 0;                 // pushes of the open round read in place by the adaptive policy
+  // An adaptive round read in place launches its parts when it finishes, merged per request (see
+  // flush_deferred): a chunk-by-chunk push sequence then costs one launch per round, not one per chunk.
+  struct DeferredPart {
+    PartDesc d;
+    int64_t tok_start;
+  };
+  std::vector<DeferredPart> deferred;
+  int64_t deferred_host_bytes = 0;
+  bool deferred_zero_copy = false;
 
   // host-side fault injection (test hooks): copy submissions counted from the arming call
   int64_t copy_seq = 0, fail_at = 0, delay_at = 0;
@@ -494,6 +503,9 @@ svx_status svx_round_begin(svx_ctx c, int32_t n_req, int32_t n_query, const void
   c->h2d_bytes = c->dev_bytes = 0;
   c->n_launch = c->n_copies = 0;
   c->n_zc_push = 0;
+  c->deferred.clear();
+  c->deferred_host_bytes = 0;
+  c->deferred_zero_copy = false;
   c->round_ip = (c->cfg.flags & SVX_FLAG_ADAPTIVE) ? choose_round_in_place(c) : false;
   c->epoch = c->epoch == 0xffffffffu ? 1u : c->epoch + 1u;
   if (c->cfg.flags & SVX_FLAG_TIMING) {
@@ -875,6 +887,14 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
     }
     c->parts_seen.push_back({p.req, p.tok_start, p.n_tok});
   }
+  if (adaptive && c->round_ip && n_host == 0) {
+    // a round the adaptive policy reads in place stages nothing: its parts wait for round_finish
+    for (int i = 0; i < n_parts; ++i)
+      c->deferred.push_back({desc[static_cast<size_t>(i)], parts[i].tok_start});
+    c->deferred_host_bytes += host_bytes;
+    c->deferred_zero_copy = c->deferred_zero_copy || zero_copy;
+    return SVX_OK;
+  }
   if (pe) {
     pe->has_copy = n_host > 0;
     pe->zero_copy = zero_copy;
@@ -899,6 +919,86 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
   if (slot >= 0) SVX_CUDA(c, cudaEventRecord(c->slot_free[static_cast<size_t>(slot)], c->cs));
   return SVX_OK;
 }
+
+namespace {
+
+// Launches the parts an adaptive in-place round deferred.  A part that continues the previous part of
+// its request (next tokens, K and V right after it in memory) is merged into it, so a request pushed
+// chunk by chunk from one buffer becomes one part.  A launch holds at most one part per request (two
+// CTAs must not merge into the same state rows at once); a part that cannot join goes to a later launch
+// of the round, stream-ordered after it.  Timed as one push; its kernel time is an in-place sample.
+svx_status flush_deferred(svx_ctx c) {
+  if (c->deferred.empty()) return SVX_OK;
+  const int64_t row_elems = static_cast<int64_t>(c->cfg.n_kv_heads) * c->cfg.head_dim;
+  std::vector<std::vector<PartDesc>> batches;
+  std::vector<std::vector<int64_t>> batch_end;  // per batch: the request's part's end token, or -1
+  std::vector<std::vector<int>> batch_at;       // per batch: the request's index in the batch, or -1
+  for (const auto& dp : c->deferred) {
+    const int b = dp.d.req;
+    bool placed = false;
+    for (size_t k = 0; k < batches.size() && !placed; ++k) {
+      const int at = batch_at[k][static_cast<size_t>(b)];
+      if (at < 0) {
+        batch_at[k][static_cast<size_t>(b)] = static_cast<int>(batches[k].size());
+        batches[k].push_back(dp.d);
+        batch_end[k][static_cast<size_t>(b)] = dp.tok_start + dp.d.n_tok;
+        placed = true;
+      } else {
+        PartDesc& cur = batches[k][static_cast<size_t>(at)];
+        const int64_t n = cur.n_tok;
+        if (batch_end[k][static_cast<size_t>(b)] == dp.tok_start && dp.d.k == cur.k + n * row_elems &&
+            dp.d.v == cur.v + n * row_elems && n + dp.d.n_tok <= INT32_MAX) {
+          cur.n_tok = static_cast<int32_t>(n + dp.d.n_tok);
+          batch_end[k][static_cast<size_t>(b)] += dp.d.n_tok;
+          placed = true;
+        }
+      }
+    }
+    if (!placed) {
+      batches.emplace_back(1, dp.d);
+      batch_end.emplace_back(static_cast<size_t>(c->n_req), -1);
+      batch_at.emplace_back(static_cast<size_t>(c->n_req), -1);
+      batch_end.back()[static_cast<size_t>(b)] = dp.tok_start + dp.d.n_tok;
+      batch_at.back()[static_cast<size_t>(b)] = 0;
+    }
+  }
+  const bool timing = (c->cfg.flags & SVX_FLAG_TIMING) != 0 && c->n_push < kWindowPushes;
+  if (timing && c->n_push >= static_cast<int>(c->ev_push.size())) {
+    PushEvents pe{make_event(true), make_event(true), make_event(true), make_event(true), false, false};
+    if (!pe.copy0 || !pe.copy1 || !pe.k0 || !pe.k1) return fail(c, SVX_ERR_CUDA, "event creation failed");
+    c->ev_push.push_back(pe);
+  }
+  PushEvents* pe = timing ? &c->ev_push[static_cast<size_t>(c->n_push)] : nullptr;
+  if (pe) {
+    pe->has_copy = false;
+    pe->zero_copy = c->deferred_zero_copy;
+    SVX_CUDA(c, cudaEventRecord(pe->k0, c->cs));
+  }
+  RateSample* rs = nullptr;
+  if (c->deferred_host_bytes > 0) {
+    rs = next_sample(c);
+    if (!rs) return fail(c, SVX_ERR_CUDA, "event creation failed");
+    SVX_CUDA(c, cudaEventRecord(rs->e0, c->cs));
+  }
+  for (auto& batch : batches) {
+    svx_status st = launch_parts(c, batch, c->deferred_zero_copy ? c->cfg.zero_copy_ctas : 0);
+    if (st != SVX_OK) return st;
+  }
+  if (rs) {
+    SVX_CUDA(c, cudaEventRecord(rs->e1, c->cs));
+    commit_sample(c, rs, c->deferred_host_bytes, true);
+  }
+  if (pe) {
+    SVX_CUDA(c, cudaEventRecord(pe->k1, c->cs));
+    ++c->n_push;
+  }
+  c->deferred.clear();
+  c->deferred_host_bytes = 0;
+  c->deferred_zero_copy = false;
+  return SVX_OK;
+}
+
+}  // namespace
 
 svx_status svx_candidate_attn(svx_ctx c, const void* k_dev, const void* v_dev, int32_t n_cand,
                               const int32_t* parent_host) {
@@ -937,8 +1037,13 @@ svx_status svx_round_finish(svx_ctx c, void* o_dev, float* lse_dev, int32_t time
   std::string why;
   if (!coverage_impl(c->n_req, c->hist_len.data(), c->parts_seen, &why)) {
     c->state = RoundState::kIdle;  // the round is abandoned; its enqueued work is harmless
+    c->deferred.clear();           // and its deferred parts are never launched
     if (c->cfg.flags & SVX_FLAG_TIMING) c->n_push = c->round_push0;  // and it leaves the timing window
     return fail(c, SVX_ERR_INVALID_ARG, "chunk coverage check failed: %s", why.c_str());
+  }
+  {
+    const svx_status st = flush_deferred(c);
+    if (st != SVX_OK) return st;
   }
   FinishParams p;
   std::memset(&p, 0, sizeof(p));

@@ -54,11 +54,15 @@ def test_step_overlap_takes_the_union_of_transfers_inside_each_step():
     iv = np.array([[0.0, 2.0, 2.0, 2.5], [nan, nan, 2.5, 4.0],
                    [10.0, 12.0, 12.0, 12.4], [12.1, 14.0, 14.0, 14.3]])
     rounds = np.array([[-0.5, 4.0, 4.2], [9.8, 14.3, 14.5]])
-    so = bench.step_overlap(iv, rounds, 2, 1)
+    so = bench.step_overlap(iv, rounds, 1)
     assert len(so) == 2
     (t0, b0), (t1, b1) = so
     assert abs(t0 - 4.7) < 1e-9 and abs(b0 - 3.5) < 1e-9  # [0, 2] and the in-place kernel [2.5, 4]
     assert abs(t1 - 4.7) < 1e-9 and abs(b1 - 3.9) < 1e-9  # [10, 12] and [12.1, 14]
+    # a step with a different number of intervals (an adaptive in-place round launched once) is cut by time
+    iv2 = np.array([[0.0, 2.0, 2.0, 2.5], [nan, nan, 2.5, 4.0], [nan, nan, 10.2, 14.0]])
+    (t0, b0), (t1, b1) = bench.step_overlap(iv2, rounds, 1)
+    assert abs(b0 - 3.5) < 1e-9 and abs(b1 - 3.8) < 1e-9
 
 
 def test_default_run_records_and_profiling_switches():

@@ -290,8 +290,11 @@ def test_adaptive_streaming_moves_to_in_place_reads_when_copies_are_slow(svx):
             torch.cuda.synchronize()
             check_parity(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), *ref)
     assert stats[0]["n_zero_copy_pushes"] == 0  # staged: the copy engine's first measurement
-    assert stats[1]["n_zero_copy_pushes"] == 4  # read in place: the other engine's first measurement
-    assert stats[2]["n_zero_copy_pushes"] == 4  # the copy engine was measured slow
+    assert stats[0]["n_chunk_launches"] == 4
+    # read in place: the other engine's first measurement.  The round's four pushes launch together when it
+    # finishes, each request's chunks merged into one part (they are consecutive rows of one buffer)
+    assert stats[1]["n_zero_copy_pushes"] == 1 and stats[1]["n_chunk_launches"] == 1
+    assert stats[2]["n_zero_copy_pushes"] == 1  # the copy engine was measured slow
     # bytes read in place count as host bytes, and the in-place kernels count as transfer time
     assert stats[1]["h2d_bytes"] == w.hist_bytes and stats[1]["copy_busy_ms"] == 0.0
     assert stats[1]["transfer_busy_ms"] > 0.0
@@ -323,3 +326,51 @@ def test_a_window_past_its_round_limit_starts_again(svx):
         assert st["chunk_kernel_ms"] > 0 and st["n_chunk_launches"] == 1
     torch.cuda.synchronize()
     check_parity(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), *oracle_out(w, x))
+
+
+@pytest.mark.parametrize("order", ["reversed", "split_buffers"])
+def test_an_adaptive_in_place_round_merges_only_what_continues(svx, order):
+    """An adaptive round read in place launches its parts when it finishes.  A chunk merges into its
+    request's part only when it continues it (next tokens, next rows of the same buffer); otherwise it goes
+    to a later launch of the round, so no launch holds two parts of one request.  Pushed in reverse order,
+    or from a separate buffer per chunk, the round needs several launches and still matches the oracle."""
+    import torch
+    w = W.Workload("defer", 2, 16, 4, 128, (4096, 3000), 1024, 5, seed=79)
+    x, t = gpu_inputs(w)
+    row_bytes = w.n_kv_heads * w.head_dim * 2
+    pushes = _pushes(svx, w, t, row_bytes)
+    keep = []
+    if order == "reversed":
+        pushes = pushes[::-1]
+    else:  # every chunk copied into its own pinned buffer, one spare row after it, so that no chunk's rows
+        # can end where the next chunk's buffer starts
+        new = []
+        for ps in pushes:
+            row = []
+            for b, t0, n, _k, _v in ps:
+                kb = torch.empty((n + 1,) + tuple(t["kh"][b].shape[1:]), dtype=torch.bfloat16).pin_memory()
+                vb = torch.empty((n + 1,) + tuple(t["vh"][b].shape[1:]), dtype=torch.bfloat16).pin_memory()
+                kb[:n].copy_(t["kh"][b][t0:t0 + n])
+                vb[:n].copy_(t["vh"][b][t0:t0 + n])
+                keep += [kb, vb]
+                row.append((b, t0, n, kb.data_ptr(), vb.data_ptr()))
+            new.append(row)
+        pushes = new
+    o = torch.empty((w.n_req, w.n_q_heads, w.n_query, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.n_req, w.n_q_heads, w.n_query), dtype=torch.float32, device="cuda")
+    ref = oracle_out(w, x)
+    with svx.Verifier(w.n_req, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_query, w.chunk_tokens, n_slots=3,
+                      timing=True, adaptive=True, zero_copy_ctas=16) as v:
+        for rnd in range(2):  # round 0 staged, round 1 read in place
+            v.round_begin(t["q"], w.hist_len)
+            v.candidate_attn(t["kc"], t["vc"])
+            for p in pushes:
+                v.push_raw(p)
+            v.round_finish(o, lse, timeout_ms=60000)
+            st = v.stats()
+            torch.cuda.synchronize()
+            check_parity(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), *ref)
+        assert st["n_zero_copy_pushes"] == 1 and st["copy_busy_ms"] == 0.0
+        # request 0 has 4 chunks, request 1 has 3: none merges, so one launch per chunk rank
+        assert st["n_chunk_launches"] == 4, st["n_chunk_launches"]
+        assert st["h2d_bytes"] == w.hist_bytes
