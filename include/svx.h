@@ -69,10 +69,12 @@ typedef struct svx_ctx_s* svx_ctx;
 #define SVX_FLAG_TIMING 1u           /* record CUDA events around copies and kernels (svx_round_stats) */
 #define SVX_FLAG_NO_TENSOR_CORES 2u  /* run the history chunk kernel on FP32 FMA instead of tcgen05 */
 #define SVX_FLAG_ZERO_COPY 4u        /* read pinned host parts in place over the host link (no staging copy);
-                                        the chunk kernel then runs at link speed on zero_copy_ctas SMs */
-#define SVX_FLAG_ADAPTIVE 8u         /* stage pinned host parts through the copy engine, but read in place
-                                        (as SVX_FLAG_ZERO_COPY) those whose host memory the copy engine has
-                                        been measured to read slowly: see below */
+                                        the chunk kernel then runs at link speed on zero_copy_ctas SMs.
+                                        Each push is one launch here, so a push of each request's whole
+                                        history (any n_tok) beats chunk-sized pushes */
+#define SVX_FLAG_ADAPTIVE 8u         /* per round, stage pinned host parts through the copy engine or read
+                                        them in place (as SVX_FLAG_ZERO_COPY), whichever was measured
+                                        faster: see below */
 
 /* Context configuration.  Shapes are fixed for the context's lifetime (the
  * Cohort compatibility rule of section 4.2: one layer shape, verification
