@@ -33,7 +33,8 @@
  * human-readable message for the last failing call on that context.  No call
  * throws, aborts or exits.  After SVX_ERR_CUDA from a failed CUDA call the
  * context should be destroyed; the report of a kernel's expired bounded wait
- * (svx_round_finish) is the exception, and the context runs on.
+ * (svx_round_finish), or in the bounds-checked library of a skipped access, is
+ * the exception, and the context runs on.
  *
  * Threads: a context is used by one host thread at a time.
  *
