@@ -71,8 +71,9 @@ typedef struct svx_ctx_s* svx_ctx;
 #define SVX_FLAG_NO_TENSOR_CORES 2u  /* run the history chunk kernel on FP32 FMA instead of tcgen05 */
 #define SVX_FLAG_ZERO_COPY 4u        /* read pinned host parts in place over the host link (no staging copy);
                                         the chunk kernel then runs at link speed on zero_copy_ctas SMs.
-                                        Each push is one launch here, so a push of each request's whole
-                                        history (any n_tok) beats chunk-sized pushes */
+                                        A round's pushes (host and device parts) launch together at
+                                        svx_round_finish, a request's consecutive chunks merged into one
+                                        part (see SVX_FLAG_ADAPTIVE below) */
 #define SVX_FLAG_ADAPTIVE 8u         /* per round, stage pinned host parts through the copy engine or read
                                         them in place (as SVX_FLAG_ZERO_COPY), whichever was measured
                                         faster: see below */
@@ -247,7 +248,8 @@ typedef struct {
                                      parts in place); 1 - exposed / chunk_kernel_ms is the compute hidden
                                      under transfer */
   double transfer_busy_ms; /* length of the union of the transfer intervals */
-  int32_t n_zero_copy_pushes; /* pushes whose chunk kernel read host parts in place */
+  int32_t n_zero_copy_pushes; /* push intervals whose chunk kernels read host parts in place: a round read
+                                 in place launches its pushes together and counts once */
 } svx_stats;
 svx_status svx_round_stats(svx_ctx ctx, svx_stats* out);
 
@@ -261,7 +263,8 @@ svx_status svx_round_stats(svx_ctx ctx, svx_stats* out);
  * the compute stream (from the moment the staging slot is ready), chunk_kernel_exposed_ms the
  * kernel time outside every copy interval, and copy_gap_ms the copy stream's idle time between its
  * first copy and its last.  1 - max(0, window_ms - copy_busy_ms) / (the same chunks' kernel time
- * with resident history) is the hidden fraction of compute over the whole step. */
+ * with resident history) is the hidden fraction of compute over the whole step.  A round read in
+ * place launches its pushes together at svx_round_finish: they form one push interval. */
 typedef struct {
   double window_ms;        /* first round's begin (or the window's first copy, if that started earlier)
                               to the last finished round's finish-kernel end */

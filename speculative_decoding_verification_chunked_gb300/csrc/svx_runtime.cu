@@ -146,8 +146,9 @@ struct svx_ctx_s {
   bool prefer_ip = false;              // the engine the measurements favour
   bool round_ip = false;               // the open round reads its host parts in place
   int n_zc_push = 0;                 // pushes of the open round read in place by the adaptive policy
-  // An adaptive round read in place launches its parts when it finishes, merged per request (see
-  // flush_deferred): a chunk-by-chunk push sequence then costs one launch per round, not one per chunk.
+  // A round read in place (SVX_FLAG_ZERO_COPY, or an adaptive round read in place) launches its parts
+  // when it finishes, merged per request (see flush_deferred): a chunk-by-chunk push sequence then costs
+  // one launch per round, not one per chunk.
   struct DeferredPart {
     PartDesc d;
     int64_t tok_start;
@@ -887,8 +888,9 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
     }
     c->parts_seen.push_back({p.req, p.tok_start, p.n_tok});
   }
-  if (adaptive && c->round_ip && n_host == 0) {
-    // a round the adaptive policy reads in place stages nothing: its parts wait for round_finish
+  if (n_host == 0 && ((c->cfg.flags & SVX_FLAG_ZERO_COPY) || (adaptive && c->round_ip))) {
+    // a round read in place (every round with SVX_FLAG_ZERO_COPY, or one the adaptive policy reads in
+    // place) stages nothing: its parts wait for round_finish
     for (int i = 0; i < n_parts; ++i)
       c->deferred.push_back({desc[static_cast<size_t>(i)], parts[i].tok_start});
     c->deferred_host_bytes += host_bytes;
@@ -922,7 +924,7 @@ svx_status svx_push_chunk(svx_ctx c, const svx_part* parts, int32_t n_parts) {
 
 namespace {
 
-// Launches the parts an adaptive in-place round deferred.  A part that continues the previous part of
+// Launches the parts a round read in place deferred.  A part that continues the previous part of
 // its request (next tokens, K and V right after it in memory) is merged into it, so a request pushed
 // chunk by chunk from one buffer becomes one part.  A launch holds at most one part per request (two
 // CTAs must not merge into the same state rows at once); a part that cannot join goes to a later launch
