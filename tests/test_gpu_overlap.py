@@ -374,3 +374,33 @@ def test_an_adaptive_in_place_round_merges_only_what_continues(svx, order):
         # request 0 has 4 chunks, request 1 has 3: none merges, so one launch per chunk rank
         assert st["n_chunk_launches"] == 4, st["n_chunk_launches"]
         assert st["h2d_bytes"] == w.hist_bytes
+
+
+@pytest.mark.parametrize("order", ["forward", "reversed"])
+def test_a_zero_copy_round_launches_once_when_its_chunks_continue(svx, order):
+    """SVX_FLAG_ZERO_COPY: a round's pushes launch together when it finishes.  Chunks pushed in plan
+    order continue one another (consecutive rows of each request's buffer) and merge into one part per
+    request, one launch; pushed in reverse they cannot merge and need one launch per chunk rank.  Both
+    match the oracle."""
+    import torch
+    w = W.Workload("zcmerge", 3, 16, 4, 128, (4096, 3000, 130), 1024, 5, seed=80)
+    x, t = gpu_inputs(w)
+    row_bytes = w.n_kv_heads * w.head_dim * 2
+    pushes = _pushes(svx, w, t, row_bytes)
+    if order == "reversed":
+        pushes = pushes[::-1]
+    o = torch.empty((w.n_req, w.n_q_heads, w.n_query, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.n_req, w.n_q_heads, w.n_query), dtype=torch.float32, device="cuda")
+    with svx.Verifier(w.n_req, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_query, w.chunk_tokens, n_slots=3,
+                      timing=True, zero_copy=True, zero_copy_ctas=32) as v:
+        v.round_begin(t["q"], w.hist_len)
+        v.candidate_attn(t["kc"], t["vc"])
+        for p in pushes:
+            v.push_raw(p)
+        v.round_finish(o, lse, timeout_ms=60000)
+        st = v.stats()
+    torch.cuda.synchronize()
+    check_parity(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+                 *oracle_out(w, x))
+    assert st["n_copies"] == 0 and st["h2d_bytes"] == w.hist_bytes and st["n_zero_copy_pushes"] == 1
+    assert st["n_chunk_launches"] == (1 if order == "forward" else len(pushes))
