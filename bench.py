@@ -570,9 +570,11 @@ class Runner:
                             n_slots=self.a.slots, device=self.dev.index, compute_stream=self.cs, copy_stream=self.xs,
                             **kw)
 
-    def timed(self, step_fn, steps, warmup, between=None):
+    def timed(self, step_fn, steps, warmup, between=None, lead_ms=0.0):
         """Mean ms per step over `steps` steps after `warmup`, CUDA events on the compute stream, a barrier and
-        a device synchronisation on both sides.  `between()` runs after the warm-up, before the timing."""
+        a device synchronisation on both sides.  `between()` runs after the warm-up, before the timing.
+        lead_ms > 0: the compute stream first spins that long (before the start event), so the host has
+        enqueued the steps' work before the GPU reaches it (for timing single launches inside the steps)."""
         torch = self.torch
         for _ in range(warmup):
             step_fn()
@@ -587,6 +589,9 @@ class Runner:
         try:
             barrier(self.world)
             torch.cuda.synchronize(self.dev)
+            if lead_ms > 0:
+                with torch.cuda.stream(self.cs):
+                    torch.cuda._sleep(int(lead_ms * 2.0e6))  # ~2 GHz SM clock
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(self.cs)
             for _ in range(steps):
@@ -733,9 +738,10 @@ def measure(a, w, dev, world, cs, xs, hbm_peak, hbm_src, full: bool) -> dict:
                 kern_ev.append((e, sum(n for _b, _t, n, _k, _v in p)))
             v_res.round_finish(ly["o_d"], ly["lse_d"])
 
-    R.timed(resident_step_events, steps, 1, between=kern_ev.clear)
-    # The timed region starts on an idle GPU, so the first launch's interval also holds the host's time to
-    # submit it; from the second on, the host runs ahead and each interval is the launch alone.
+    # The GPU first spins for about the host's time to enqueue every timed round, so that each launch's
+    # interval is the launch alone, never the host's time to submit it (short launches, as a single qwen3
+    # layer's 90 us, would otherwise wait on the host).  The first timed step is dropped as well.
+    R.timed(resident_step_events, steps, 1, between=kern_ev.clear, lead_ms=min(200.0, 0.2 * steps * L))
     per_step = len(kern_ev) // steps
     kern = [(e[0].elapsed_time(e[1]), toks) for e, toks in kern_ev[per_step if steps > 1 else 0:]]
     k1_ms = statistics.mean(k for k, _ in kern)
